@@ -1,0 +1,207 @@
+"""Python binding of the routed-expert layer C ABI (``include/moe.h``).
+
+Argument marshalling only: every step of the layer runs in the sm_103a
+kernels of ``_build/libmoe_gb300.so``.  Tensors are torch CUDA tensors (the
+caller owns them); bf16 buffers are ``torch.bfloat16``, fp32 ``torch.float32``,
+indices ``torch.int32``, all contiguous.  Calls enqueue on the current torch
+CUDA stream (or ``stream=``) and never synchronise.
+
+Importing this package fails loudly if the library has not been built
+(``python combine_expert_gemm_gb300/build.py``); there is no fallback.
+"""
+import ctypes
+import os
+
+import torch
+
+from .build import LIB
+
+__all__ = ["Shape", "MoEError", "lib", "route", "dispatch", "expert_ffn", "combine",
+           "combine_backward", "dispatch_backward", "read_device_error",
+           "route_workspace_bytes", "expert_ffn_workspace_bytes", "capacity", "LayerBuffers",
+           "layer_forward"]
+
+if not os.path.exists(LIB):
+    raise ImportError(f"{LIB} is missing: build it with `python combine_expert_gemm_gb300/build.py` "
+                      "(or __graft_entry__.build()); there is no CPU fallback")
+
+_lib = ctypes.CDLL(LIB)
+
+
+def lib():
+    return _lib
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("d", ctypes.c_int32), ("N", ctypes.c_int32),
+                ("K", ctypes.c_int32), ("h", ctypes.c_int32), ("cap", ctypes.c_int32)]
+
+    def __repr__(self):
+        return f"Shape(T={self.T}, d={self.d}, N={self.N}, K={self.K}, h={self.h}, cap={self.cap})"
+
+    @property
+    def R(self):
+        return self.N * self.cap
+
+
+_P = ctypes.c_void_p
+_SP = ctypes.POINTER(Shape)
+_SZ = ctypes.c_size_t
+_SIG = {
+    "moe_status_string": ([ctypes.c_int], ctypes.c_char_p),
+    "moe_route_workspace_bytes": ([_SP], _SZ),
+    "moe_expert_ffn_workspace_bytes": ([_SP], _SZ),
+    "moe_route": ([_SP] + [_P] * 9 + [_P, _SZ, _P], ctypes.c_int),
+    "moe_dispatch": ([_SP, _P, _P, _P, _P], ctypes.c_int),
+    "moe_expert_ffn": ([_SP] + [_P] * 10 + [_P, _SZ, _P], ctypes.c_int),
+    "moe_combine": ([_SP, _P, _P, _P, _P, _P], ctypes.c_int),
+    "moe_combine_backward": ([_SP, _P, _P, _P, _P, _P, _P, _P], ctypes.c_int),
+    "moe_dispatch_backward": ([_SP, _P, _P, _P, _P], ctypes.c_int),
+    "moe_read_device_error": ([_P, ctypes.POINTER(ctypes.c_int32), _P], ctypes.c_int),
+}
+for _name, (_args, _res) in _SIG.items():
+    _f = getattr(_lib, _name)
+    _f.argtypes = _args
+    _f.restype = _res
+
+EXPORTED = tuple(_SIG)
+
+
+class MoEError(RuntimeError):
+    def __init__(self, code, where):
+        self.code = code
+        msg = _lib.moe_status_string(code).decode()
+        super().__init__(f"{where}: {msg} (status {code})")
+
+
+def _check(code, where):
+    if code != 0:
+        raise MoEError(code, where)
+
+
+def capacity(T, K, N, cf_num, cf_den=1):
+    """ceil(cf * T * K / N) with cf = cf_num / cf_den, in integers."""
+    return (cf_num * T * K + cf_den * N - 1) // (cf_den * N)
+
+
+def _ptr(t, dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name}: must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+_bf16, _f32, _i32 = torch.bfloat16, torch.float32, torch.int32
+
+
+def route_workspace_bytes(shape):
+    return int(_lib.moe_route_workspace_bytes(ctypes.byref(shape)))
+
+
+def expert_ffn_workspace_bytes(shape):
+    return int(_lib.moe_expert_ffn_workspace_bytes(ctypes.byref(shape)))
+
+
+def route(shape, x, w_router, bias, topk_idx, topk_gate, route_row, expert_count, expert_offset,
+          expert_demand, ws, stream=None):
+    _check(_lib.moe_route(ctypes.byref(shape), _ptr(x, _bf16, "x"), _ptr(w_router, _f32, "w_router"),
+                          _ptr(bias, _f32, "bias"), _ptr(topk_idx, _i32, "topk_idx"),
+                          _ptr(topk_gate, _f32, "topk_gate"), _ptr(route_row, _i32, "route_row"),
+                          _ptr(expert_count, _i32, "expert_count"),
+                          _ptr(expert_offset, _i32, "expert_offset"),
+                          _ptr(expert_demand, _i32, "expert_demand"), _ptr(ws, None, "ws"),
+                          ws.numel() * ws.element_size(), _stream(stream)), "moe_route")
+
+
+def dispatch(shape, x, route_row, x_disp, stream=None):
+    _check(_lib.moe_dispatch(ctypes.byref(shape), _ptr(x, _bf16, "x"),
+                             _ptr(route_row, _i32, "route_row"), _ptr(x_disp, _bf16, "x_disp"),
+                             _stream(stream)), "moe_dispatch")
+
+
+def expert_ffn(shape, x_disp, expert_count, expert_offset, w_gate, w_up, w_down, h_act, g_save,
+               u_save, y_disp, ws, stream=None):
+    _check(_lib.moe_expert_ffn(ctypes.byref(shape), _ptr(x_disp, _bf16, "x_disp"),
+                               _ptr(expert_count, _i32, "expert_count"),
+                               _ptr(expert_offset, _i32, "expert_offset"),
+                               _ptr(w_gate, _bf16, "w_gate"), _ptr(w_up, _bf16, "w_up"),
+                               _ptr(w_down, _bf16, "w_down"), _ptr(h_act, _bf16, "h_act"),
+                               _ptr(g_save, _bf16, "g_save"), _ptr(u_save, _bf16, "u_save"),
+                               _ptr(y_disp, _bf16, "y_disp"), _ptr(ws, None, "ws"),
+                               ws.numel() * ws.element_size(), _stream(stream)), "moe_expert_ffn")
+
+
+def combine(shape, y_disp, route_row, topk_gate, y, stream=None):
+    _check(_lib.moe_combine(ctypes.byref(shape), _ptr(y_disp, _bf16, "y_disp"),
+                            _ptr(route_row, _i32, "route_row"), _ptr(topk_gate, _f32, "topk_gate"),
+                            _ptr(y, _bf16, "y"), _stream(stream)), "moe_combine")
+
+
+def combine_backward(shape, dy, y_disp, route_row, topk_gate, dy_disp, dgate, stream=None):
+    _check(_lib.moe_combine_backward(ctypes.byref(shape), _ptr(dy, _bf16, "dy"),
+                                     _ptr(y_disp, _bf16, "y_disp"),
+                                     _ptr(route_row, _i32, "route_row"),
+                                     _ptr(topk_gate, _f32, "topk_gate"),
+                                     _ptr(dy_disp, _bf16, "dy_disp"), _ptr(dgate, _f32, "dgate"),
+                                     _stream(stream)), "moe_combine_backward")
+
+
+def dispatch_backward(shape, dx_disp, route_row, dx, stream=None):
+    _check(_lib.moe_dispatch_backward(ctypes.byref(shape), _ptr(dx_disp, _bf16, "dx_disp"),
+                                      _ptr(route_row, _i32, "route_row"), _ptr(dx, _f32, "dx"),
+                                      _stream(stream)), "moe_dispatch_backward")
+
+
+def read_device_error(ws, stream=None):
+    code = ctypes.c_int32(0)
+    _check(_lib.moe_read_device_error(_ptr(ws, None, "ws"), ctypes.byref(code), _stream(stream)),
+           "moe_read_device_error")
+    return code.value
+
+
+class LayerBuffers:
+    """Device buffers of one layer instance, allocated once before the loop
+    (capacity-shaped, so no allocation depends on the routing)."""
+
+    def __init__(self, shape, device="cuda", save_for_backward=False):
+        T, d, N, K, h, R = shape.T, shape.d, shape.N, shape.K, shape.h, shape.R
+        e = dict(device=device)
+        self.shape = shape
+        self.topk_idx = torch.empty((T, K), dtype=_i32, **e)
+        self.topk_gate = torch.empty((T, K), dtype=_f32, **e)
+        self.route_row = torch.empty((T, K), dtype=_i32, **e)
+        self.expert_count = torch.empty(N, dtype=_i32, **e)
+        self.expert_offset = torch.empty(N + 1, dtype=_i32, **e)
+        self.expert_demand = torch.empty(N, dtype=_i32, **e)
+        self.route_ws = torch.zeros(max(route_workspace_bytes(shape), 256), dtype=torch.uint8, **e)
+        self.ffn_ws = torch.zeros(max(expert_ffn_workspace_bytes(shape), 256), dtype=torch.uint8, **e)
+        self.x_disp = torch.empty((R, d), dtype=_bf16, **e)
+        self.h_act = torch.empty((R, h), dtype=_bf16, **e)
+        self.g_save = torch.empty((R, h), dtype=_bf16, **e) if save_for_backward else None
+        self.u_save = torch.empty((R, h), dtype=_bf16, **e) if save_for_backward else None
+        self.y_disp = torch.empty((R, d), dtype=_bf16, **e)
+        self.y = torch.empty((T, d), dtype=_bf16, **e)
+
+
+def layer_forward(buf, x, w_router, bias, w_gate, w_up, w_down, stream=None):
+    """Route -> dispatch -> grouped SwiGLU experts -> combine into buf.y (4 C-ABI calls)."""
+    s = buf.shape
+    route(s, x, w_router, bias, buf.topk_idx, buf.topk_gate, buf.route_row, buf.expert_count,
+          buf.expert_offset, buf.expert_demand, buf.route_ws, stream)
+    dispatch(s, x, buf.route_row, buf.x_disp, stream)
+    expert_ffn(s, buf.x_disp, buf.expert_count, buf.expert_offset, w_gate, w_up, w_down,
+               buf.h_act, buf.g_save, buf.u_save, buf.y_disp, buf.ffn_ws, stream)
+    combine(s, buf.y_disp, buf.route_row, buf.topk_gate, buf.y, stream)
+    return buf.y

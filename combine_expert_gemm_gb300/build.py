@@ -1,0 +1,69 @@
+"""Builds the sm_103a shared library ``_build/libmoe_gb300.so`` with nvcc.
+
+Each ``csrc/*.cu`` compiles to an object in parallel, then nvcc links them
+into one shared library (static CUDA runtime, no libcuda link: the tensor-map
+encoder is fetched through the runtime's driver entry-point query).
+"""
+import glob
+import os
+import subprocess
+import sys
+from concurrent.futures import ThreadPoolExecutor
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+CSRC = os.path.join(HERE, "csrc")
+OUT_DIR = os.path.join(HERE, "_build")
+LIB = os.path.join(OUT_DIR, "libmoe_gb300.so")
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+NVCC = os.environ.get("NVCC", "nvcc")
+CFLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
+                 "-Xcompiler", "-fvisibility=hidden", "-I", os.path.join(ROOT, "include")]
+
+
+def _sources():
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+
+
+def _deps():
+    return (_sources() + glob.glob(os.path.join(CSRC, "*.cuh")) +
+            [os.path.join(ROOT, "include", "moe.h"), __file__])
+
+
+def up_to_date() -> bool:
+    if not os.path.exists(LIB):
+        return False
+    t = os.path.getmtime(LIB)
+    return all(os.path.getmtime(p) <= t for p in _deps())
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    if not force and up_to_date():
+        return LIB
+    os.makedirs(OUT_DIR, exist_ok=True)
+    srcs = _sources()
+    extra = ["-Xptxas", "-v"] if verbose else []
+
+    def compile_one(src):
+        obj = os.path.join(OUT_DIR, os.path.basename(src)[:-3] + ".o")
+        r = subprocess.run([NVCC] + CFLAGS + extra + ["-c", src, "-o", obj],
+                           capture_output=True, text=True)
+        return src, obj, r
+
+    with ThreadPoolExecutor(len(srcs)) as ex:
+        results = list(ex.map(compile_one, srcs))
+    failed = [(s, r) for s, _, r in results if r.returncode != 0]
+    for s, _, r in results:
+        if verbose or r.returncode != 0:
+            sys.stderr.write(r.stdout + r.stderr)
+    if failed:
+        raise RuntimeError("nvcc failed for: " + ", ".join(os.path.basename(s) for s, _ in failed))
+    tmp = LIB + f".tmp{os.getpid()}"
+    subprocess.run([NVCC] + ARCH + ["-shared", "-o", tmp] + [o for _, o, _ in results],
+                   check=True)
+    os.replace(tmp, LIB)
+    return LIB
+
+
+if __name__ == "__main__":
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))

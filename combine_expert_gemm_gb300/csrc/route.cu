@@ -1,0 +1,361 @@
+// Routing: router logits, top-K and gates, fixed-capacity slots, route map.
+//
+// OLMo-core MoE report, "Section 05: Expert Parallelism", Figure 15 (K indices
+// and K weights per token, larger first, summing to one), 5.4 and Figure 16
+// (row = offset of the expert + number of earlier accepted routes to it; the
+// capacity decision precedes any data movement; -1 marks a dropped route);
+// "Section 08: Synchronization-Free Training", Table 14 (route map, counts and
+// int32 cumulative offsets produced and kept on the device).  AWS Neuron
+// "Expert Parallelism (EP)", "Router Weights" (logits for every expert).
+//
+// Four launches, none of which waits on another CTA:
+//   1. route_logits_topk: per tile of tokens, fp32 logits for all experts in
+//      shared memory (one fused multiply-add chain over j ascending per
+//      logit, so the values are reproducible bit for bit), then one warp per
+//      token selects the top K and computes the gates.
+//   2. route_block_rank: per block of 256 tokens, a per-warp bitmask of the
+//      tokens choosing each expert gives every route its rank among earlier
+//      routes to the same expert inside the block, and the block's count per
+//      expert.  Bitmask OR is order-free, so the ranks are deterministic.
+//   3. route_scan: one CTA scans the per-block counts for every expert
+//      (giving each block its base slot), clamps demand to capacity and scans
+//      the counts into the cumulative offsets.
+//   4. route_assign: slot = block base + rank; row = offset + slot, or -1 past
+//      capacity.
+#include "moe_common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kJC = 32;          // j-chunk of the logit tiles
+constexpr int kRankBlock = 256;  // tokens per block of the slot ranking
+
+__device__ __forceinline__ float canon(float v) { return isnan(v) ? -INFINITY : v; }
+
+__device__ __forceinline__ bool beats(float a, int ia, float b, int ib) {
+    return a > b || (a == b && ia < ib);
+}
+
+// TB tokens x EC experts per pass; 256 threads, each a 4 x 4 register tile.
+template <int TB, int EC>
+__global__ void __launch_bounds__(kThreads)
+route_logits_topk(int T, int d, int N, int K, const uint16_t *__restrict__ x,
+                  const float *__restrict__ w_r, const float *__restrict__ bias,
+                  int32_t *__restrict__ topk_idx, float *__restrict__ topk_gate) {
+    static_assert((TB / 4) * (EC / 4) == kThreads, "thread tile");
+    constexpr int XS = TB + 4;  // padded row of the transposed x tile
+    constexpr int WS = EC + 4;
+    extern __shared__ __align__(16) float smem[];
+    float *xs = smem;                 // [kJC][XS]
+    float *wsm = xs + kJC * XS;       // [kJC][WS]
+    float *lg = wsm + kJC * WS;       // [TB][N]
+
+    const int tid = threadIdx.x;
+    const int t0 = blockIdx.x * TB;
+    const int tx = tid % (EC / 4), ty = tid / (EC / 4);
+
+    for (int ec0 = 0; ec0 < N; ec0 += EC) {
+        float acc[4][4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) acc[a][b] = 0.0f;
+
+        for (int j0 = 0; j0 < d; j0 += kJC) {
+            const int jn = min(kJC, d - j0);  // multiple of 8
+            __syncthreads();
+            for (int i = tid; i < TB * (kJC / 8); i += kThreads) {
+                const int tok = i / (kJC / 8), jp = (i % (kJC / 8)) * 8;
+                uint4 v = make_uint4(0, 0, 0, 0);
+                if (t0 + tok < T && jp < jn)
+                    v = *reinterpret_cast<const uint4 *>(x + (int64_t)(t0 + tok) * d + j0 + jp);
+                const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    xs[(jp + 2 * q) * XS + tok] = bf16_lo(w4[q]);
+                    xs[(jp + 2 * q + 1) * XS + tok] = bf16_hi(w4[q]);
+                }
+            }
+            for (int i = tid; i < EC * (kJC / 8); i += kThreads) {
+                const int e = i / (kJC / 8), jp = (i % (kJC / 8)) * 8;
+                float4 a = make_float4(0, 0, 0, 0), b = a;
+                if (ec0 + e < N && jp < jn) {
+                    const float4 *src =
+                        reinterpret_cast<const float4 *>(w_r + (int64_t)(ec0 + e) * d + j0 + jp);
+                    a = src[0];
+                    b = src[1];
+                }
+                const float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+                for (int q = 0; q < 8; ++q) wsm[(jp + q) * WS + e] = f[q];
+            }
+            __syncthreads();
+#pragma unroll 4
+            for (int jj = 0; jj < jn; ++jj) {
+                const float4 xv = *reinterpret_cast<const float4 *>(xs + jj * XS + ty * 4);
+                const float4 wv = *reinterpret_cast<const float4 *>(wsm + jj * WS + tx * 4);
+                const float xa[4] = {xv.x, xv.y, xv.z, xv.w};
+                const float wb[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+                for (int a = 0; a < 4; ++a)
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) acc[a][b] = __fmaf_rn(xa[a], wb[b], acc[a][b]);
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const int e = ec0 + tx * 4 + b;
+            if (e < N) {
+                const float bb = bias ? bias[e] : 0.0f;
+#pragma unroll
+                for (int a = 0; a < 4; ++a)
+                    lg[(ty * 4 + a) * N + e] = bias ? __fadd_rn(acc[a][b], bb) : acc[a][b];
+            }
+        }
+    }
+    __syncthreads();
+
+    // top-K and gates, one warp per token
+    const int lane = tid & 31, warp = tid >> 5;
+    for (int tt = warp; tt < TB; tt += kThreads / 32) {
+        const int t = t0 + tt;
+        if (t >= T) break;
+        const float *l = lg + tt * N;
+        uint32_t taken = 0;  // bit q: expert lane + 32 q already chosen
+        int my_idx = 0;
+        float my_val = 0.0f, top = 0.0f, ex = 0.0f;
+        for (int k = 0; k < K; ++k) {
+            float bv = -INFINITY;
+            int bi = 0x7FFFFFFF;
+            for (int q = 0, e = lane; e < N; ++q, e += 32) {
+                if (taken & (1u << q)) continue;
+                const float v = canon(l[e]);
+                if (beats(v, e, bv, bi)) { bv = v; bi = e; }
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, off);
+                const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, off);
+                if (beats(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+            }
+            if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+            if (k == 0) top = bv;
+            if (lane == k) { my_idx = bi; my_val = bv; }
+        }
+        if (lane < K) ex = (my_val == top) ? 1.0f : expf(my_val - top);
+        float s = ex;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, off);
+        if (lane < K) {
+            topk_idx[(int64_t)t * K + lane] = my_idx;
+            topk_gate[(int64_t)t * K + lane] = ex / s;
+        }
+    }
+}
+
+// Per block of 256 tokens: rank of each route among earlier routes of the
+// block to the same expert (written to route_row for now) and the block's
+// count per expert.
+__global__ void __launch_bounds__(kRankBlock)
+route_block_rank(int T, int N, int K, const int32_t *__restrict__ topk_idx,
+                 int32_t *__restrict__ route_row, int32_t *__restrict__ block_count) {
+    extern __shared__ uint32_t sm[];
+    uint32_t *mask = sm;                       // [8][N]: bit lane of warp w chose e
+    uint32_t *wpre = sm + (kRankBlock / 32) * N;  // [8][N]: routes to e in earlier warps
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int i = tid; i < (kRankBlock / 32) * N; i += kRankBlock) mask[i] = 0;
+    __syncthreads();
+    const int t = blockIdx.x * kRankBlock + tid;
+    int e_of[kMaxK];
+    if (t < T) {
+        for (int k = 0; k < K; ++k) {
+            e_of[k] = topk_idx[(int64_t)t * K + k];
+            atomicOr(&mask[warp * N + e_of[k]], 1u << lane);
+        }
+    }
+    __syncthreads();
+    for (int e = tid; e < N; e += kRankBlock) {
+        uint32_t run = 0;
+        for (int w = 0; w < kRankBlock / 32; ++w) {
+            wpre[w * N + e] = run;
+            run += __popc(mask[w * N + e]);
+        }
+        block_count[(int64_t)blockIdx.x * N + e] = (int32_t)run;
+    }
+    __syncthreads();
+    if (t < T) {
+        const uint32_t lt = (1u << lane) - 1u;
+        for (int k = 0; k < K; ++k) {
+            const int e = e_of[k];
+            route_row[(int64_t)t * K + k] =
+                (int32_t)(wpre[warp * N + e] + __popc(mask[warp * N + e] & lt));
+        }
+    }
+}
+
+// One CTA of 1024 threads: thread e turns the per-block counts of expert e
+// into per-block base slots, then all threads scan the clamped counts.
+__global__ void __launch_bounds__(1024)
+route_scan(int nblk, int N, int cap, int32_t *__restrict__ block_count,
+           int32_t *__restrict__ expert_count, int32_t *__restrict__ expert_offset,
+           int32_t *__restrict__ expert_demand) {
+    __shared__ int32_t warp_sum[32];
+    const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
+    int32_t cnt = 0;
+    if (e < N) {
+        int32_t run = 0;
+        int b = 0;
+        for (; b + 8 <= nblk; b += 8) {
+            int32_t c[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) c[q] = block_count[(int64_t)(b + q) * N + e];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                block_count[(int64_t)(b + q) * N + e] = run;
+                run += c[q];
+            }
+        }
+        for (; b < nblk; ++b) {
+            const int32_t c = block_count[(int64_t)b * N + e];
+            block_count[(int64_t)b * N + e] = run;
+            run += c;
+        }
+        expert_demand[e] = run;
+        cnt = min(run, cap);
+        expert_count[e] = cnt;
+    }
+    // exclusive scan of cnt over e
+    int32_t incl = cnt;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+        if (lane >= off) incl += v;
+    }
+    if (lane == 31) warp_sum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int32_t v = warp_sum[lane];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int32_t u = __shfl_up_sync(0xFFFFFFFFu, v, off);
+            if (lane >= off) v += u;
+        }
+        warp_sum[lane] = v;  // inclusive over warps
+    }
+    __syncthreads();
+    const int32_t base = warp > 0 ? warp_sum[warp - 1] : 0;
+    if (e < N) expert_offset[e] = base + incl - cnt;
+    if (e == N - 1) expert_offset[N] = base + incl;
+}
+
+__global__ void route_assign(int T, int N, int K, int cap, const int32_t *__restrict__ topk_idx,
+                             const int32_t *__restrict__ block_base,
+                             const int32_t *__restrict__ expert_offset,
+                             int32_t *__restrict__ route_row) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (int64_t)T * K) return;
+    const int t = (int)(i / K);
+    const int e = topk_idx[i];
+    const int32_t slot = block_base[(int64_t)(t / kRankBlock) * N + e] + route_row[i];
+    route_row[i] = slot < cap ? expert_offset[e] + slot : -1;
+}
+
+template <int TB, int EC>
+moe_status launch_logits(const moe_shape *s, const uint16_t *x, const float *w, const float *b,
+                         int32_t *idx, float *gate, cudaStream_t st) {
+    const size_t smem =
+        sizeof(float) * ((size_t)kJC * (TB + 4) + (size_t)kJC * (EC + 4) + (size_t)TB * s->N);
+    static size_t configured = 0;
+    if (smem > 48 * 1024 && smem > configured) {
+        if (cudaFuncSetAttribute(route_logits_topk<TB, EC>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        configured = smem;
+    }
+    const int grid = (s->T + TB - 1) / TB;
+    route_logits_topk<TB, EC><<<grid, kThreads, smem, st>>>(s->T, s->d, s->N, s->K, x, w, b, idx,
+                                                             gate);
+    return launch_status();
+}
+
+}  // namespace
+
+size_t route_ws_bytes(const moe_shape *s) {
+    const size_t nblk = (size_t)(s->T + kRankBlock - 1) / kRankBlock;
+    const size_t bc = (nblk * (size_t)s->N * sizeof(int32_t) + 255) & ~(size_t)255;
+    return 256 + bc;
+}
+
+// Enqueues the four routing kernels; `status` is the device status word and
+// `block_count` a [ceil(T/256), N] int32 scratch array.
+moe_status route_enqueue(const moe_shape *s, const moe_bf16 *x, const float *w_router,
+                         const float *bias, int32_t *topk_idx, float *topk_gate,
+                         int32_t *route_row, int32_t *expert_count, int32_t *expert_offset,
+                         int32_t *expert_demand, int32_t *block_count, cudaStream_t st) {
+    const int nblk = (s->T + kRankBlock - 1) / kRankBlock;
+    moe_status r = MOE_OK;
+    if (s->T > 0) {
+        const int n = s->N;
+        if (n <= 8) r = launch_logits<512, 8>(s, x, w_router, bias, topk_idx, topk_gate, st);
+        else if (n <= 16) r = launch_logits<256, 16>(s, x, w_router, bias, topk_idx, topk_gate, st);
+        else if (n <= 32) r = launch_logits<128, 32>(s, x, w_router, bias, topk_idx, topk_gate, st);
+        else if (n <= 64) r = launch_logits<64, 64>(s, x, w_router, bias, topk_idx, topk_gate, st);
+        else r = launch_logits<32, 128>(s, x, w_router, bias, topk_idx, topk_gate, st);
+        if (r != MOE_OK) return r;
+        const size_t smem = sizeof(uint32_t) * 2 * (kRankBlock / 32) * (size_t)s->N;
+        static bool configured = false;
+        if (smem > 48 * 1024 && !configured) {
+            if (cudaFuncSetAttribute(route_block_rank, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     2 * (kRankBlock / 32) * kMaxN * (int)sizeof(uint32_t)) !=
+                cudaSuccess)
+                return MOE_ERR_CUDA;
+            configured = true;
+        }
+        route_block_rank<<<nblk, kRankBlock, smem, st>>>(s->T, s->N, s->K, topk_idx, route_row,
+                                                          block_count);
+        if ((r = launch_status()) != MOE_OK) return r;
+    }
+    route_scan<<<1, 1024, 0, st>>>(nblk, s->N, s->cap, block_count, expert_count, expert_offset,
+                                   expert_demand);
+    if ((r = launch_status()) != MOE_OK) return r;
+    if (s->T > 0) {
+        const int64_t routes = (int64_t)s->T * s->K;
+        const int grid = (int)((routes + 255) / 256);
+        route_assign<<<grid, 256, 0, st>>>(s->T, s->N, s->K, s->cap, topk_idx, block_count,
+                                           expert_offset, route_row);
+        r = launch_status();
+    }
+    return r;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+MOE_API size_t moe_route_workspace_bytes(const moe_shape *s) {
+    if (check_shape(s) != MOE_OK) return 0;
+    return route_ws_bytes(s);
+}
+
+MOE_API moe_status moe_route(const moe_shape *s, const moe_bf16 *x, const float *w_router,
+                             const float *bias, int32_t *topk_idx, float *topk_gate,
+                             int32_t *route_row, int32_t *expert_count, int32_t *expert_offset,
+                             int32_t *expert_demand, void *ws, size_t ws_bytes,
+                             cudaStream_t stream) {
+    moe_status r = check_shape(s);
+    if (r != MOE_OK) return r;
+    if (!expert_count || !expert_offset || !expert_demand || !ws) return MOE_ERR_INVALID_ARG;
+    if (s->T > 0 && (!x || !w_router || !topk_idx || !topk_gate || !route_row))
+        return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < route_ws_bytes(s) || (reinterpret_cast<uintptr_t>(ws) & 255u))
+        return MOE_ERR_WORKSPACE;
+    if (!aligned16(x) || !aligned16(w_router) || !aligned16(topk_idx) || !aligned16(topk_gate) ||
+        !aligned16(route_row) || !aligned16(expert_count) || !aligned16(expert_offset) ||
+        !aligned16(expert_demand) || (bias && !aligned16(bias)))
+        return MOE_ERR_ALIGNMENT;
+    int32_t *block_count = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + 256);
+    return route_enqueue(s, x, w_router, bias, topk_idx, topk_gate, route_row, expert_count,
+                         expert_offset, expert_demand, block_count, stream);
+}

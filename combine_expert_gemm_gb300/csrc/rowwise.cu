@@ -1,0 +1,234 @@
+// Rowwise movement between token order and the packed capacity buffers.
+//
+// OLMo-core MoE report, "Section 05: Expert Parallelism", 5.6 and Table 8:
+// dispatch forward is a PUT of x_t to each accepted route's row, combine
+// forward a GET of the K expert rows with the router-weighted reduction done at
+// the token, and the backward pair applies the transposed movements with the
+// same route map; negative rows are skipped and contribute zero.  Figure 19:
+// the token row is read once and fanned out by its source.
+//
+// One warp per token; every access is a 16-byte vector (8 bf16); the K route
+// rows and gates of the token are read once by lanes 0..K-1 and broadcast with
+// shuffles.  All four kernels are HBM-bound.
+#include "moe_common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kSeg = 8;  // 16-byte chunks per lane per pass (2048 bf16 per warp pass)
+
+__device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8]) {
+    f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
+    f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+    f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
+    f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+    return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                      pack_bf16x2(f[6], f[7]));
+}
+
+__global__ void __launch_bounds__(kThreads)
+dispatch_rows(int T, int nchunk, int K, const uint4 *__restrict__ x,
+              const int32_t *__restrict__ route_row, uint4 *__restrict__ x_disp) {
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const int32_t my_row = lane < K ? route_row[(int64_t)t * K + lane] : -1;
+    const uint4 *src = x + (int64_t)t * nchunk;
+    for (int c0 = 0; c0 < nchunk; c0 += 32 * kSeg) {
+        uint4 v[kSeg];
+#pragma unroll
+        for (int u = 0; u < kSeg; ++u) {
+            const int c = c0 + u * 32 + lane;
+            if (c < nchunk) v[u] = __ldcs(src + c);
+        }
+        for (int k = 0; k < K; ++k) {
+            const int32_t r = __shfl_sync(0xFFFFFFFFu, my_row, k);
+            if (r < 0) continue;
+            uint4 *dst = x_disp + (int64_t)r * nchunk;
+#pragma unroll
+            for (int u = 0; u < kSeg; ++u) {
+                const int c = c0 + u * 32 + lane;
+                if (c < nchunk) dst[c] = v[u];
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads)
+combine_rows(int T, int nchunk, int K, const uint4 *__restrict__ y_disp,
+             const int32_t *__restrict__ route_row, const float *__restrict__ gate,
+             uint4 *__restrict__ y) {
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const int32_t my_row = lane < K ? route_row[(int64_t)t * K + lane] : -1;
+    const float my_g = lane < K ? gate[(int64_t)t * K + lane] : 0.0f;
+    // the chunk loop is warp-uniform so that every shuffle has all 32 lanes
+    for (int c0 = 0; c0 < nchunk; c0 += 32) {
+        const int c = c0 + lane;
+        const bool on = c < nchunk;
+        uint4 v[kMaxK];
+#pragma unroll
+        for (int k = 0; k < kMaxK; ++k) {
+            if (k >= K) break;
+            const int32_t r = __shfl_sync(0xFFFFFFFFu, my_row, k);
+            if (r >= 0 && on) v[k] = __ldcs(y_disp + (int64_t)r * nchunk + c);
+        }
+        float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+        for (int k = 0; k < kMaxK; ++k) {
+            if (k >= K) break;
+            const int32_t r = __shfl_sync(0xFFFFFFFFu, my_row, k);
+            const float g = __shfl_sync(0xFFFFFFFFu, my_g, k);
+            if (r < 0 || !on) continue;
+            float f[8];
+            unpack8(v[k], f);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = __fmaf_rn(g, f[i], acc[i]);
+        }
+        if (on) y[(int64_t)t * nchunk + c] = pack8(acc);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads)
+combine_bwd_rows(int T, int nchunk, int K, const uint4 *__restrict__ dy,
+                 const uint4 *__restrict__ y_disp, const int32_t *__restrict__ route_row,
+                 const float *__restrict__ gate, uint4 *__restrict__ dy_disp,
+                 float *__restrict__ dgate) {
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const int32_t my_row = lane < K ? route_row[(int64_t)t * K + lane] : -1;
+    const float my_g = lane < K ? gate[(int64_t)t * K + lane] : 0.0f;
+    const uint4 *src = dy + (int64_t)t * nchunk;
+    for (int k = 0; k < K; ++k) {
+        const int32_t r = __shfl_sync(0xFFFFFFFFu, my_row, k);
+        const float g = __shfl_sync(0xFFFFFFFFu, my_g, k);
+        float part = 0.0f;
+        if (r >= 0) {
+            for (int c = lane; c < nchunk; c += 32) {
+                float f[8], o[8];
+                unpack8(src[c], f);
+                unpack8(__ldcs(y_disp + (int64_t)r * nchunk + c), o);
+                float p[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    p[i] = __fmul_rn(g, f[i]);
+                    part = __fmaf_rn(f[i], o[i], part);
+                }
+                dy_disp[(int64_t)r * nchunk + c] = pack8(p);
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xFFFFFFFFu, part, off);
+        if (lane == 0) dgate[(int64_t)t * K + k] = r >= 0 ? part : 0.0f;
+    }
+}
+
+__global__ void __launch_bounds__(kThreads)
+dispatch_bwd_rows(int T, int nchunk, int K, const uint4 *__restrict__ dx_disp,
+                  const int32_t *__restrict__ route_row, float4 *__restrict__ dx) {
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const int32_t my_row = lane < K ? route_row[(int64_t)t * K + lane] : -1;
+    for (int c0 = 0; c0 < nchunk; c0 += 32) {  // warp-uniform (shuffles inside)
+        const int c = c0 + lane;
+        const bool on = c < nchunk;
+        uint4 v[kMaxK];
+#pragma unroll
+        for (int k = 0; k < kMaxK; ++k) {
+            if (k >= K) break;
+            const int32_t r = __shfl_sync(0xFFFFFFFFu, my_row, k);
+            if (r >= 0 && on) v[k] = __ldcs(dx_disp + (int64_t)r * nchunk + c);
+        }
+        float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+        for (int k = 0; k < kMaxK; ++k) {
+            if (k >= K) break;
+            const int32_t r = __shfl_sync(0xFFFFFFFFu, my_row, k);
+            if (r < 0 || !on) continue;
+            float f[8];
+            unpack8(v[k], f);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], f[i]);
+        }
+        if (!on) continue;
+        float4 *o = dx + ((int64_t)t * nchunk + c) * 2;
+        __stcs(o, make_float4(acc[0], acc[1], acc[2], acc[3]));
+        __stcs(o + 1, make_float4(acc[4], acc[5], acc[6], acc[7]));
+    }
+}
+
+inline int grid_for(int T) { return (T + kWarps - 1) / kWarps; }
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+MOE_API moe_status moe_dispatch(const moe_shape *s, const moe_bf16 *x, const int32_t *route_row,
+                                moe_bf16 *x_disp, cudaStream_t stream) {
+    moe_status r = check_shape(s);
+    if (r != MOE_OK) return r;
+    if (s->T == 0 || s->cap == 0) return MOE_OK;  // no row can be written
+    if (!x || !route_row || !x_disp) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(route_row) || !aligned16(x_disp)) return MOE_ERR_ALIGNMENT;
+    dispatch_rows<<<grid_for(s->T), kThreads, 0, stream>>>(
+        s->T, s->d / 8, s->K, reinterpret_cast<const uint4 *>(x), route_row,
+        reinterpret_cast<uint4 *>(x_disp));
+    return launch_status();
+}
+
+MOE_API moe_status moe_combine(const moe_shape *s, const moe_bf16 *y_disp,
+                               const int32_t *route_row, const float *topk_gate, moe_bf16 *y,
+                               cudaStream_t stream) {
+    moe_status r = check_shape(s);
+    if (r != MOE_OK) return r;
+    if (s->T == 0) return MOE_OK;
+    if (!route_row || !topk_gate || !y || (s->cap > 0 && !y_disp)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(y_disp) || !aligned16(route_row) || !aligned16(topk_gate) || !aligned16(y))
+        return MOE_ERR_ALIGNMENT;
+    combine_rows<<<grid_for(s->T), kThreads, 0, stream>>>(
+        s->T, s->d / 8, s->K, reinterpret_cast<const uint4 *>(y_disp), route_row, topk_gate,
+        reinterpret_cast<uint4 *>(y));
+    return launch_status();
+}
+
+MOE_API moe_status moe_combine_backward(const moe_shape *s, const moe_bf16 *dy,
+                                        const moe_bf16 *y_disp, const int32_t *route_row,
+                                        const float *topk_gate, moe_bf16 *dy_disp, float *dgate,
+                                        cudaStream_t stream) {
+    moe_status r = check_shape(s);
+    if (r != MOE_OK) return r;
+    if (s->T == 0) return MOE_OK;
+    if (!dy || !route_row || !topk_gate || !dgate || (s->cap > 0 && (!y_disp || !dy_disp)))
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16(dy) || !aligned16(y_disp) || !aligned16(route_row) || !aligned16(topk_gate) ||
+        !aligned16(dy_disp) || !aligned16(dgate))
+        return MOE_ERR_ALIGNMENT;
+    combine_bwd_rows<<<grid_for(s->T), kThreads, 0, stream>>>(
+        s->T, s->d / 8, s->K, reinterpret_cast<const uint4 *>(dy),
+        reinterpret_cast<const uint4 *>(y_disp), route_row, topk_gate,
+        reinterpret_cast<uint4 *>(dy_disp), dgate);
+    return launch_status();
+}
+
+MOE_API moe_status moe_dispatch_backward(const moe_shape *s, const moe_bf16 *dx_disp,
+                                         const int32_t *route_row, float *dx,
+                                         cudaStream_t stream) {
+    moe_status r = check_shape(s);
+    if (r != MOE_OK) return r;
+    if (s->T == 0) return MOE_OK;
+    if (!route_row || !dx || (s->cap > 0 && !dx_disp)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(dx_disp) || !aligned16(route_row) || !aligned16(dx)) return MOE_ERR_ALIGNMENT;
+    dispatch_bwd_rows<<<grid_for(s->T), kThreads, 0, stream>>>(
+        s->T, s->d / 8, s->K, reinterpret_cast<const uint4 *>(dx_disp), route_row,
+        reinterpret_cast<float4 *>(dx));
+    return launch_status();
+}

@@ -1,0 +1,192 @@
+/*
+ * moe.h -- C ABI of the routed-expert (MoE) layer hot path on one GPU.
+ *
+ * Path: route (router logits, top-K gates, fixed-capacity slots) -> rowwise
+ * dispatch into packed per-expert buffers -> grouped bias-free SwiGLU expert
+ * GEMMs over the valid rows -> gate-weighted combine back to token order; plus
+ * the backward of combine, experts and dispatch.
+ *
+ * Sources (page title, then section / figure / table):
+ *   OLMo-core MoE report, "Section 05: Expert Parallelism": 5.2 and Figure 14
+ *   (route, expert-contiguous layout, Linear 1 -> SwiGLU -> Linear 2, combine),
+ *   Figures 15 and 16 (router output, route map, dropped route), 5.4, 5.6 and
+ *   Table 8 (dispatch PUT, combine GET and their adjoint backward), 5.7 (dense
+ *   prefix per buffer, unwritten tail never consumed).
+ *   OLMo-core MoE report, "Section 08: Synchronization-Free Training": 8.5 and
+ *   Table 14 (route maps, counts and int32 cumulative offsets stay on the
+ *   device; capacity-shaped buffers; grouped GEMM with device offsets).
+ *   OLMo-core MoE report, "Section 04: Distributed Data Parallel": 4.1
+ *   (bias-free SwiGLU expert).
+ *   AWS Neuron "Expert Parallelism (EP)": "Router Weights" (affinities for all
+ *   experts from one router weight).
+ *
+ * Conventions shared by every call
+ *   - All pointers are DEVICE pointers unless stated otherwise, owned by the
+ *     caller; the library never allocates or frees device memory.
+ *   - Every call is asynchronous on `stream` and never synchronises the host
+ *     or reads device data back; route-dependent values (counts, offsets,
+ *     rows) are produced and consumed on the device only.
+ *   - bf16 tensors are 16-bit bfloat16 bit patterns (moe_bf16); every pointer
+ *     must be 16-byte aligned and d, h must be multiples of 8.
+ *   - Row-major layouts.  T tokens, d model width, N experts, K routes per
+ *     token, h expert hidden width, cap rows per expert, R = N * cap rows in
+ *     every capacity buffer.
+ *   - Capacity buffers hold the experts' rows packed back to back from row 0:
+ *     expert e owns rows [expert_offset[e], expert_offset[e] + expert_count[e]).
+ *     Rows from expert_offset[N] to R - 1 (the tail) are neither read nor
+ *     written by any call and may hold anything, including NaN.
+ *   - Host-side argument errors are returned before anything is enqueued.
+ *     Errors seen on the device (a wait that timed out) are recorded in the
+ *     workspace's status word; moe_read_device_error() reads it.
+ *   - Results are deterministic: no floating-point atomics anywhere.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *cudaStream_t;
+typedef uint16_t moe_bf16;
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,  /* bad shape, null pointer, K > N, ... */
+    MOE_ERR_ALIGNMENT = 2,    /* pointer not 16-byte aligned or d, h not multiples of 8 */
+    MOE_ERR_WORKSPACE = 3,    /* workspace missing or smaller than the *_workspace_bytes query */
+    MOE_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+    MOE_ERR_UNSUPPORTED = 5,  /* shape outside what the kernels handle (see each call) */
+    MOE_ERR_DEVICE_TIMEOUT = 6 /* device status word: a bounded wait inside a kernel expired */
+} moe_status;
+
+/* Layer shape.  cap is chosen by the caller before its loop, e.g.
+ * cap = ceil(cf * T * K / N) for a capacity factor cf. */
+typedef struct {
+    int32_t T, d, N, K, h, cap;
+} moe_shape;
+
+/* Limits: 1 <= K <= 16, K <= N <= 1024, 0 <= cap, T >= 0, N * cap < 2^31,
+ * T * K < 2^31, 8 <= d, h with d, h multiples of 8. */
+
+/* Human-readable name of a status code (static string). */
+const char *moe_status_string(moe_status s);
+
+/* Bytes of workspace moe_route needs for this shape (0 if the shape is invalid). */
+size_t moe_route_workspace_bytes(const moe_shape *s);
+
+/*
+ * moe_route -- steps R0-R3: router logits, top-K, gates, slots, route map.
+ * Report: Neuron "Router Weights" (logits over all N experts); Section 05
+ * Figure 15 (K indices and K weights per token, larger weight first, summing
+ * to one); 5.4 and Figure 16 (row = offset of the expert + number of earlier
+ * accepted routes to it; capacity decided before any row moves; negative =
+ * dropped); Section 08 Table 14 (counts and cumulative offsets on the device).
+ *
+ *   x            [T, d] bf16 token rows.
+ *   w_router     [N, d] fp32 router weight.
+ *   bias         [N] fp32 per-expert logit offset, or NULL.
+ *   topk_idx     out [T, K] int32: experts by logit descending, ties to the
+ *                lower index; NaN logits rank as -inf.
+ *   topk_gate    out [T, K] fp32: softmax over the K chosen logits.
+ *   route_row    out [T, K] int32: capacity-buffer row of each route, -1 if
+ *                the route was dropped.  Routes claim slots in token order.
+ *   expert_count out [N] int32: accepted routes per expert (<= cap).
+ *   expert_offset out [N + 1] int32: exclusive prefix sum of expert_count;
+ *                expert_offset[N] = accepted routes A.
+ *   expert_demand out [N] int32: routes that chose each expert (before the
+ *                capacity decision); dropped = sum(demand - count).
+ *   ws, ws_bytes device workspace of at least moe_route_workspace_bytes(s)
+ *                bytes, 256-byte aligned; word 0 is the device status word.
+ * Logits are fp32, one fused multiply-add chain over j ascending per (t, e),
+ * then + bias, so top-K decisions are reproducible bit for bit.
+ */
+moe_status moe_route(const moe_shape *s, const moe_bf16 *x, const float *w_router,
+                     const float *bias, int32_t *topk_idx, float *topk_gate, int32_t *route_row,
+                     int32_t *expert_count, int32_t *expert_offset, int32_t *expert_demand,
+                     void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * moe_dispatch -- step D.  Section 05 Table 8 "Dispatch forward PUT" and 5.6:
+ * x_disp[route_row[t, k]] = x[t] for every route with route_row >= 0; each
+ * token row is read once and written to each of its accepted rows (Figure 19,
+ * source-initiated fan-out).  Rows not named by route_row are untouched.
+ *   x [T, d] bf16;  route_row [T, K];  x_disp out [R, d] bf16 (may be NULL when
+ *   cap = 0: every route is then dropped and nothing is written).
+ */
+moe_status moe_dispatch(const moe_shape *s, const moe_bf16 *x, const int32_t *route_row,
+                        moe_bf16 *x_disp, cudaStream_t stream);
+
+/* Bytes of workspace moe_expert_ffn / moe_expert_ffn_backward need. */
+size_t moe_expert_ffn_workspace_bytes(const moe_shape *s);
+
+/*
+ * moe_expert_ffn -- steps F1, F2: grouped bias-free SwiGLU experts.
+ * Section 05 Figure 14 (Linear 1 -> SwiGLU -> Linear 2), 5.7 and Section 08
+ * 8.5 (per-expert row intervals from device offsets; the activation is applied
+ * to the valid prefix only; tails are skipped).  For each expert e and each
+ * row r of its interval:
+ *   G = x_disp[r] W_gate[e]^T,  U = x_disp[r] W_up[e]^T   (fp32 accumulation)
+ *   h_act[r] = bf16(silu(G) * U),   silu(z) = z / (1 + exp(-z))
+ *   y_disp[r] = bf16(h_act[r] W_down[e]^T)                (fp32 accumulation)
+ *   x_disp [R, d] bf16; expert_count [N]; expert_offset [N + 1] (from moe_route);
+ *   w_gate, w_up [N, h, d] bf16; w_down [N, d, h] bf16;
+ *   h_act out [R, h] bf16; g_save, u_save out [R, h] bf16 (bf16(G), bf16(U),
+ *   kept for the backward) or both NULL; y_disp out [R, d] bf16;
+ *   ws, ws_bytes: workspace of moe_expert_ffn_workspace_bytes(s) bytes.
+ * Runs on tcgen05 tensor cores; d and h must be multiples of 64
+ * (MOE_ERR_UNSUPPORTED otherwise).
+ */
+moe_status moe_expert_ffn(const moe_shape *s, const moe_bf16 *x_disp, const int32_t *expert_count,
+                          const int32_t *expert_offset, const moe_bf16 *w_gate,
+                          const moe_bf16 *w_up, const moe_bf16 *w_down, moe_bf16 *h_act,
+                          moe_bf16 *g_save, moe_bf16 *u_save, moe_bf16 *y_disp, void *ws,
+                          size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * moe_combine -- step C.  Section 05 Table 8 "Combine forward GET", 5.6 and
+ * Figure 15: y[t] = bf16( sum over k ascending of topk_gate[t, k] *
+ * y_disp[route_row[t, k]] ), fp32 fused multiply-add accumulation from 0;
+ * dropped routes contribute zero and the kept gates are not renormalised.
+ *   y_disp [R, d] bf16; route_row, topk_gate [T, K]; y out [T, d] bf16.
+ */
+moe_status moe_combine(const moe_shape *s, const moe_bf16 *y_disp, const int32_t *route_row,
+                       const float *topk_gate, moe_bf16 *y, cudaStream_t stream);
+
+/*
+ * moe_combine_backward -- step B1.  Section 05 Table 8 "Combine backward PUT"
+ * and 5.6 (router-weight gradient from the gathered expert outputs):
+ *   dy_disp[route_row[t, k]] = bf16(topk_gate[t, k] * dy[t])   (fp32 product)
+ *   dgate[t, k] = <dy[t], y_disp[route_row[t, k]]>   (fp32; 0 if dropped)
+ *   dy [T, d] bf16; y_disp [R, d] bf16; dy_disp out [R, d] bf16;
+ *   dgate out [T, K] fp32.
+ */
+moe_status moe_combine_backward(const moe_shape *s, const moe_bf16 *dy, const moe_bf16 *y_disp,
+                                const int32_t *route_row, const float *topk_gate,
+                                moe_bf16 *dy_disp, float *dgate, cudaStream_t stream);
+
+/*
+ * moe_dispatch_backward -- step B3.  Section 05 Table 8 "Dispatch backward
+ * GET": dx[t] = sum over k ascending (route_row >= 0) of dx_disp[route_row[t, k]],
+ * fp32 accumulation from 0.
+ *   dx_disp [R, d] bf16; route_row [T, K]; dx out [T, d] fp32.
+ */
+moe_status moe_dispatch_backward(const moe_shape *s, const moe_bf16 *dx_disp,
+                                 const int32_t *route_row, float *dx, cudaStream_t stream);
+
+/*
+ * moe_read_device_error -- copies the device status word of a workspace to
+ * *code_out (a moe_status value; MOE_OK if no kernel recorded an error) and
+ * clears it.  ws is a device pointer; code_out a HOST pointer.  This call
+ * synchronises `stream`: meant for tests and diagnostics, not the hot path.
+ */
+moe_status moe_read_device_error(void *ws, int32_t *code_out, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

@@ -1,0 +1,115 @@
+"""The C-ABI library: it loads, exports every entry point that include/moe.h
+declares, and rejects bad arguments on the host before anything is enqueued.
+No call here reaches the GPU (every case fails validation first)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def moe():
+    import __graft_entry__
+    __graft_entry__.build()
+    import combine_expert_gemm_gb300 as m
+    return m
+
+
+def test_header_declares_the_path(moe):
+    names = _declared()
+    for required in ["moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine",
+                     "moe_combine_backward", "moe_dispatch_backward"]:
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(moe):
+    lib = moe.lib()
+    for name in _declared():
+        assert hasattr(lib, name), name
+    assert set(moe.EXPORTED) <= set(_declared())
+
+
+def _shape(moe, **kw):
+    base = dict(T=64, d=128, N=8, K=2, h=256, cap=20)
+    base.update(kw)
+    return moe.Shape(**base)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(K=0), 1), (dict(K=17, N=32), 1), (dict(N=1025), 1), (dict(K=9, N=8), 1),
+    (dict(T=-1), 1), (dict(cap=-1), 1), (dict(d=100), 2), (dict(h=12), 2),
+    (dict(N=1024, cap=1 << 21), 1),
+])
+def test_shape_validation(moe, kw, code):
+    s = _shape(moe, **kw)
+    lib = moe.lib()
+    assert lib.moe_route_workspace_bytes(ctypes.byref(s)) == 0
+    P = ctypes.c_void_p(16)
+    assert lib.moe_dispatch(ctypes.byref(s), P, P, P, None) == code
+    assert lib.moe_combine(ctypes.byref(s), P, P, P, P, None) == code
+
+
+def test_null_and_alignment_and_workspace_errors(moe):
+    s = _shape(moe)
+    lib = moe.lib()
+    A = ctypes.c_void_p(4096)
+    mis = ctypes.c_void_p(4096 + 4)
+    assert lib.moe_dispatch(ctypes.byref(s), None, A, A, None) == 1
+    assert lib.moe_dispatch(ctypes.byref(s), mis, A, A, None) == 2
+    assert lib.moe_combine(ctypes.byref(s), A, A, A, mis, None) == 2
+    assert lib.moe_dispatch_backward(ctypes.byref(s), A, A, None, None) == 1
+    assert lib.moe_combine_backward(ctypes.byref(s), A, A, A, A, A, None, None) == 1
+    ws_need = lib.moe_route_workspace_bytes(ctypes.byref(s))
+    assert ws_need >= 256
+    args = [A] * 9
+    assert lib.moe_route(ctypes.byref(s), *args, A, ws_need - 1, None) == 3
+    assert lib.moe_route(ctypes.byref(s), *args, ctypes.c_void_p(4096 + 16), ws_need, None) == 3
+    assert lib.moe_route(ctypes.byref(s), *args, None, ws_need, None) == 1
+    # expert FFN: tensor-core tiles need d, h multiples of 64
+    s2 = _shape(moe, d=136)
+    assert lib.moe_expert_ffn(ctypes.byref(s2), *([A] * 10), A, 256, None) == 5
+    # g_save without u_save
+    ffn = [A, A, A, A, A, A, A, A, None, A]
+    assert lib.moe_expert_ffn(ctypes.byref(s), *ffn, A, 256, None) == 1
+    assert lib.moe_read_device_error(None, None, None) == 1
+
+
+def test_status_strings(moe):
+    lib = moe.lib()
+    for c in range(7):
+        assert lib.moe_status_string(c).decode().startswith("MOE_")
+    with pytest.raises(moe.MoEError, match="MOE_ERR_ALIGNMENT"):
+        moe._check(2, "x")
+
+
+def test_capacity_formula(moe):
+    import synth
+    for cfg in synth.CONFIGS.values():
+        assert moe.capacity(cfg.T, cfg.K, cfg.N, cfg.cf_num, cfg.cf_den) == cfg.cap
+    assert synth.CONFIGS["tiny"].cap == 80 and synth.CONFIGS["olmoe"].cap == 1280
+    assert synth.CONFIGS["fine_zipf"].cap == 1024 and synth.CONFIGS["wide"].cap == 6144
+
+
+def test_product_path_refuses_to_run_without_library(tmp_path):
+    """A copy of the binding without its built library raises on import
+    instead of falling back to anything."""
+    import shutil
+    import subprocess
+    import sys
+    pkg = tmp_path / "combine_expert_gemm_gb300"
+    pkg.mkdir()
+    for f in ("__init__.py", "build.py"):
+        shutil.copy(os.path.join(ROOT, "combine_expert_gemm_gb300", f), pkg / f)
+    r = subprocess.run([sys.executable, "-c", "import combine_expert_gemm_gb300"],
+                       capture_output=True, text=True, cwd=tmp_path)
+    assert r.returncode != 0 and "no CPU fallback" in r.stderr

@@ -1,0 +1,220 @@
+"""GPU path versus the CPU oracle, through the C ABI.
+
+Bit-exact: top-K indices, route map, counts, offsets, demand, dispatched rows,
+and the movement kernels given identical inputs (combine, combine backward
+payload, dispatch backward).  Within tolerance (rel 2e-2 / abs 1e-2, plus the
+same bound with the absolute term scaled to the data): gates (rel 1e-5),
+expert outputs, the layer output and the router-weight gradient.
+
+Small cases span several tiles with ragged tails and the degenerate shapes;
+the full-size workloads are checked on sampled outputs the oracle computes
+one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from synth import MoEConfig
+
+from _gpu_util import DEV, as64, assert_close_bf16, bf, bits, f32, i32
+
+pytestmark = pytest.mark.gpu
+
+SENT = 0x7FC1  # a NaN pattern used to poison unwritten rows (fits int16)
+
+SMALL = {
+    "tiny": synth.CONFIGS["tiny"],
+    "ragged": MoEConfig("ragged", T=1000, d=256, N=16, K=4, h=192, cf_num=5, cf_den=4, seed=11),
+    "zipf_drops": MoEConfig("zipf_drops", T=777, d=128, N=32, K=8, h=128, cf_num=1, cf_den=1,
+                            seed=12, zipf_s=1.2),
+    "wide_ragged": MoEConfig("wide_ragged", T=513, d=320, N=4, K=2, h=256, cf_num=3, cf_den=2,
+                             seed=13, router_std=0.01),
+    "dense_N1": MoEConfig("dense_N1", T=300, d=128, N=1, K=1, h=128, cf_num=1, cf_den=1, seed=14),
+    "K_eq_N": MoEConfig("K_eq_N", T=200, d=64, N=4, K=4, h=64, cf_num=1, cf_den=1, seed=15),
+    "cap0": MoEConfig("cap0", T=100, d=64, N=8, K=2, h=64, cf_num=0, cf_den=1, seed=16),
+    "N1024": MoEConfig("N1024", T=300, d=64, N=1024, K=16, h=64, cf_num=1, cf_den=1, seed=17),
+    "N200": MoEConfig("N200", T=600, d=192, N=200, K=6, h=64, cf_num=2, cf_den=1, seed=18),
+}
+
+
+@pytest.fixture(scope="module")
+def moe():
+    import __graft_entry__
+    __graft_entry__.build()
+    import combine_expert_gemm_gb300 as m
+    assert torch.cuda.is_available()
+    return m
+
+
+def _inputs(cfg):
+    x = synth.gen_x(cfg)
+    wr = synth.gen_router(cfg)
+    bias = synth.gen_bias(cfg)
+    wg, wu, wd = synth.gen_expert_weights(cfg)
+    return x, wr, bias, wg, wu, wd
+
+
+def _shape(moe, cfg):
+    return moe.Shape(cfg.T, cfg.d, cfg.N, cfg.K, cfg.h, cfg.cap)
+
+
+def _run_chain(moe, cfg, x, wr, bias, wg, wu, wd, save=False, poison=True):
+    s = _shape(moe, cfg)
+    buf = moe.LayerBuffers(s, DEV, save_for_backward=save)
+    if poison:
+        for t in (buf.x_disp, buf.h_act, buf.y_disp):
+            t.view(torch.int16).fill_(SENT)
+    moe.layer_forward(buf, bf(x), f32(wr), None if bias is None else f32(bias), bf(wg), bf(wu),
+                      bf(wd))
+    torch.cuda.synchronize()
+    assert moe.read_device_error(buf.route_ws) == 0
+    assert moe.read_device_error(buf.ffn_ws) == 0
+    return buf
+
+
+def _check_route(buf, ref):
+    np.testing.assert_array_equal(buf.topk_idx.cpu().numpy(), ref["topk_idx"])
+    np.testing.assert_array_equal(buf.route_row.cpu().numpy(), ref["route_row"])
+    np.testing.assert_array_equal(buf.expert_count.cpu().numpy(), ref["expert_count"])
+    np.testing.assert_array_equal(buf.expert_offset.cpu().numpy(), ref["expert_offset"])
+    np.testing.assert_array_equal(buf.expert_demand.cpu().numpy(), ref["expert_demand"])
+    np.testing.assert_allclose(buf.topk_gate.cpu().numpy(), ref["topk_gate"], rtol=1e-5,
+                               atol=1e-7)
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_layer_parity_small(moe, name):
+    cfg = SMALL[name]
+    x, wr, bias, wg, wu, wd = _inputs(cfg)
+    ref = oracle.layer_forward(x, wr, bias, wg, wu, wd, cfg.K, cfg.cap, save=True)
+    buf = _run_chain(moe, cfg, x, wr, bias, wg, wu, wd, save=True)
+    _check_route(buf, ref)
+    A = int(ref["expert_offset"][-1])
+    xd, ha, yd = bits(buf.x_disp), bits(buf.h_act), bits(buf.y_disp)
+    # dispatch: valid rows are exact copies; the tail is untouched
+    np.testing.assert_array_equal(xd[:A], ref["x_disp"][:A])
+    assert np.all(xd[A:] == SENT) and np.all(ha[A:] == SENT) and np.all(yd[A:] == SENT)
+    # experts: within tolerance on every valid row
+    if A:
+        assert_close_bf16(ha[:A], ref["h_act"][:A], f"{name} h_act")
+        assert_close_bf16(bits(buf.g_save)[:A], ref["g_save"][:A], f"{name} g_save")
+        assert_close_bf16(bits(buf.u_save)[:A], ref["u_save"][:A], f"{name} u_save")
+        assert_close_bf16(yd[:A], ref["y_disp"][:A], f"{name} y_disp")
+    assert_close_bf16(bits(buf.y), ref["y"], f"{name} y")
+    if name == "zipf_drops":
+        assert (ref["route_row"] < 0).any()
+    if name == "cap0":
+        assert np.all(bits(buf.y) == 0)
+
+
+def test_movement_kernels_bit_exact(moe):
+    """Combine, combine backward (payload) and dispatch backward given identical
+    seeded inputs are bit-identical to the oracle; dgate within tolerance."""
+    cfg = MoEConfig("mv", T=3000, d=512, N=24, K=6, h=64, cf_num=1, cf_den=1, seed=21)
+    idx = synth.gen_topk_idx(cfg.seed, cfg.T, cfg.N, cfg.K)
+    row, count, offset, demand = oracle.route_slots(idx, cfg.N, cfg.cap)
+    assert (row < 0).any()
+    A = int(offset[-1])
+    gate = synth.gen_gates(cfg.seed, cfg.T, cfg.K)
+    yd = synth.gen_bf16(cfg.seed, (cfg.R, cfg.d), "y_disp")
+    dy = synth.gen_bf16(cfg.seed, (cfg.T, cfg.d), "dy")
+    s = _shape(moe, cfg)
+    y = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device=DEV)
+    moe.combine(s, bf(yd), i32(row), f32(gate), y)
+    dyd = torch.full((cfg.R, cfg.d), SENT, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+    dg = torch.empty((cfg.T, cfg.K), dtype=torch.float32, device=DEV)
+    moe.combine_backward(s, bf(dy), bf(yd), i32(row), f32(gate), dyd, dg)
+    dx = torch.empty((cfg.T, cfg.d), dtype=torch.float32, device=DEV)
+    moe.dispatch_backward(s, bf(yd), i32(row), dx)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(bits(y), oracle.combine(yd, row, gate))
+    ref_dyd, ref_dg = oracle.combine_bwd(dy, yd, row, gate, fill=SENT)
+    np.testing.assert_array_equal(bits(dyd), ref_dyd)
+    np.testing.assert_array_equal(dx.cpu().numpy(), oracle.dispatch_bwd(yd, row, cfg.T))
+    got = dg.cpu().numpy().astype(np.float64)
+    want = ref_dg.astype(np.float64)
+    rms = np.sqrt(np.mean(want ** 2))
+    assert np.all(np.abs(got - want) <= 1e-4 * np.abs(want) + 1e-5 * rms)
+    assert np.all(got[row < 0] == 0)
+
+
+def test_graph_capture_and_determinism(moe):
+    """The layer enqueues without any host synchronisation, so it captures into
+    a CUDA graph; replays and eager runs are bitwise identical."""
+    cfg = SMALL["ragged"]
+    x, wr, bias, wg, wu, wd = _inputs(cfg)
+    s = _shape(moe, cfg)
+    args = [bf(x), f32(wr), None, bf(wg), bf(wu), bf(wd)]
+    b1 = moe.LayerBuffers(s, DEV)
+    b2 = moe.LayerBuffers(s, DEV)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        moe.layer_forward(b1, *args)  # warm-up: one-time kernel attribute setup
+        torch.cuda.synchronize()
+        y_eager = b1.y.clone()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            moe.layer_forward(b2, *args)
+        for _ in range(2):
+            b2.y.zero_()
+            g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(b2.y.view(torch.int16), y_eager.view(torch.int16))
+    assert torch.equal(b2.route_row, b1.route_row)
+    moe.layer_forward(b1, *args)
+    torch.cuda.synchronize()
+    assert torch.equal(b1.y.view(torch.int16), y_eager.view(torch.int16))
+
+
+FULL = ["olmoe", "fine_zipf", "wide", "train"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled(moe, name):
+    """Full-size workloads: the whole route map bit-exact; dispatch, experts
+    and combine checked on sampled rows and tokens computed one by one."""
+    cfg = synth.CONFIGS[name]
+    x, wr, bias, wg, wu, wd = _inputs(cfg)
+    r = oracle.route(x, wr, bias, cfg.K, cfg.cap)
+    buf = _run_chain(moe, cfg, x, wr, bias, wg, wu, wd, save=cfg.backward)
+    _check_route(buf, r)
+    row, idx, gate = r["route_row"], r["topk_idx"], r["topk_gate"]
+    A = int(r["expert_offset"][-1])
+    rng = np.random.default_rng(cfg.seed)
+    # dispatch on 2048 sampled routes, and sampled tail rows stay poisoned
+    tk = np.argwhere(row >= 0)
+    pick = tk[rng.choice(len(tk), size=min(2048, len(tk)), replace=False)]
+    rows_t = torch.from_numpy(row[pick[:, 0], pick[:, 1]].astype(np.int64)).to(DEV)
+    got = bits(buf.x_disp.index_select(0, rows_t))
+    np.testing.assert_array_equal(got, x[pick[:, 0]])
+    if A < cfg.R:
+        tail = torch.from_numpy(rng.integers(A, cfg.R, size=64)).to(DEV)
+        assert np.all(bits(buf.y_disp.index_select(0, tail)) == SENT)
+    # experts and combine on 24 sampled tokens (all their routes)
+    toks = rng.choice(cfg.T, size=24, replace=False)
+    routes = [(t, k) for t in toks for k in range(cfg.K) if row[t, k] >= 0]
+    xr = np.stack([x[t] for t, _ in routes])
+    ex = np.array([idx[t, k] for t, k in routes], dtype=np.int32)
+    order = np.argsort(ex, kind="stable")
+    h_ref = np.empty((len(routes), cfg.h), np.uint16)
+    y_ref = np.empty((len(routes), cfg.d), np.uint16)
+    h_o, _, _, y_o = oracle.expert_ffn_rows(order.astype(np.int32), ex[order], xr, wg, wu, wd)
+    h_ref[order] = h_o
+    y_ref[order] = y_o
+    rr = torch.from_numpy(np.array([row[t, k] for t, k in routes], dtype=np.int64)).to(DEV)
+    assert_close_bf16(bits(buf.h_act.index_select(0, rr)), h_ref, f"{name} h_act sample")
+    assert_close_bf16(bits(buf.y_disp.index_select(0, rr)), y_ref, f"{name} y_disp sample")
+    # combine of the sampled tokens from the oracle's expert rows
+    remap = -np.ones((len(toks), cfg.K), np.int32)
+    pos = {rt: i for i, rt in enumerate(routes)}
+    for i, t in enumerate(toks):
+        for k in range(cfg.K):
+            if (t, k) in pos:
+                remap[i, k] = pos[(t, k)]
+    y_tok = oracle.combine(y_ref, remap, gate[toks])
+    got_y = bits(buf.y.index_select(0, torch.from_numpy(toks.astype(np.int64)).to(DEV)))
+    assert_close_bf16(got_y, y_tok, f"{name} y sample")
+    if name == "fine_zipf":
+        assert (r["expert_demand"] > cfg.cap).any()
