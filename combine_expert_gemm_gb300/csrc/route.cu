@@ -22,6 +22,8 @@
 //      the counts into the cumulative offsets.
 //   4. route_assign: slot = block base + rank; row = offset + slot, or -1 past
 //      capacity.
+#include <mutex>
+
 #include "moe_common.cuh"
 
 namespace moe {
@@ -356,6 +358,71 @@ MOE_API moe_status moe_route(const moe_shape *s, const moe_bf16 *x, const float 
         !aligned16(expert_demand) || (bias && !aligned16(bias)))
         return MOE_ERR_ALIGNMENT;
     int32_t *block_count = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + 256);
+    return route_enqueue(s, x, w_router, bias, topk_idx, topk_gate, route_row, expert_count,
+                         expert_offset, expert_demand, block_count, stream);
+}
+
+// ------------------------------------------------------------------------
+// moe_route_noalloc: moe_route for callers that cannot allocate device memory.
+//
+// Its scratch (the device status word and the per-block count array) lives in
+// the fixed array below instead of a caller-provided workspace.  Every GPU
+// that loads this library holds the array until the process exits.  In host
+// code `route_noalloc_scratch` names a host-side stand-in, not a device
+// address, so the address each kernel gets is looked up once per device with
+// cudaGetSymbolAddress (with that device current) on the first call there.
+// All calls on a device share the array and it keeps the last call's
+// contents; nothing in it needs clearing, because every entry a call reads
+// is written earlier in the same call.  Calls that overlap on the GPU (for
+// example on two streams) race on the array.
+namespace moe {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = MOE_ROUTE_NOALLOC_SCRATCH_BYTES;
+constexpr int kNoAllocMaxDevices = 64;
+
+static __device__ __align__(256) uint8_t route_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex noalloc_mu;
+void *noalloc_base[kNoAllocMaxDevices] = {};
+
+// Device address of the scratch array on the current device (looked up once).
+moe_status noalloc_scratch(void **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (dev < 0 || dev >= kNoAllocMaxDevices) return MOE_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(noalloc_mu);
+    if (!noalloc_base[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, route_noalloc_scratch) != cudaSuccess || !p)
+            return MOE_ERR_CUDA;
+        noalloc_base[dev] = p;
+    }
+    *out = noalloc_base[dev];
+    return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+MOE_API moe_status moe_route_noalloc(const moe_shape *s, const moe_bf16 *x, const float *w_router,
+                                     const float *bias, int32_t *topk_idx, float *topk_gate,
+                                     int32_t *route_row, int32_t *expert_count,
+                                     int32_t *expert_offset, int32_t *expert_demand,
+                                     cudaStream_t stream) {
+    moe_status r = check_shape(s);
+    if (r != MOE_OK) return r;
+    if (!expert_count || !expert_offset || !expert_demand) return MOE_ERR_INVALID_ARG;
+    if (s->T > 0 && (!x || !w_router || !topk_idx || !topk_gate || !route_row))
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w_router) || !aligned16(topk_idx) || !aligned16(topk_gate) ||
+        !aligned16(route_row) || !aligned16(expert_count) || !aligned16(expert_offset) ||
+        !aligned16(expert_demand) || (bias && !aligned16(bias)))
+        return MOE_ERR_ALIGNMENT;
+    if (route_ws_bytes(s) > kNoAllocScratchBytes) return MOE_ERR_UNSUPPORTED;
+    void *base = nullptr;
+    if ((r = noalloc_scratch(&base)) != MOE_OK) return r;
+    int32_t *block_count = reinterpret_cast<int32_t *>(static_cast<char *>(base) + 256);
     return route_enqueue(s, x, w_router, bias, topk_idx, topk_gate, route_row, expert_count,
                          expert_offset, expert_demand, block_count, stream);
 }

@@ -110,6 +110,35 @@ moe_status moe_route(const moe_shape *s, const moe_bf16 *x, const float *w_route
                      void *ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * moe_route_noalloc -- moe_route without a workspace argument, for callers
+ * that cannot allocate device memory: for example a plugin that a host
+ * framework hands only its input and output buffers (the framework owns the
+ * allocator), or a latency-critical loop in which cudaMalloc is not allowed
+ * because it can synchronise the device.  The report has no counterpart of
+ * this entry point.
+ *
+ * Same arguments, outputs and results as moe_route.  The scratch that
+ * moe_route keeps in `ws` lives instead in a fixed device array of
+ * MOE_ROUTE_NOALLOC_SCRATCH_BYTES (1 MiB) inside this library; every GPU that
+ * loads the library holds that array until the process exits.  The call
+ * allocates nothing.  Shapes whose scratch (moe_route_workspace_bytes) would
+ * exceed the array -- roughly ceil(T / 256) * N > 262,000 -- are rejected
+ * with MOE_ERR_UNSUPPORTED before anything is enqueued.
+ *
+ * The first call on a device looks up the array's device address there
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  All calls on one device share the array, which
+ * keeps the previous call's contents; nothing in it needs clearing.  Calls
+ * that overlap on the GPU (e.g. on two streams at once) race on the array.
+ * Device-side errors cannot be read back through moe_read_device_error here.
+ */
+#define MOE_ROUTE_NOALLOC_SCRATCH_BYTES ((size_t)1 << 20)
+moe_status moe_route_noalloc(const moe_shape *s, const moe_bf16 *x, const float *w_router,
+                             const float *bias, int32_t *topk_idx, float *topk_gate,
+                             int32_t *route_row, int32_t *expert_count, int32_t *expert_offset,
+                             int32_t *expert_demand, cudaStream_t stream);
+
+/*
  * moe_dispatch -- step D.  Section 05 Table 8 "Dispatch forward PUT" and 5.6:
  * x_disp[route_row[t, k]] = x[t] for every route with route_row >= 0; each
  * token row is read once and written to each of its accepted rows (Figure 19,

@@ -1,0 +1,90 @@
+"""moe_route_noalloc: routing for callers that cannot allocate device memory.
+
+Some callers cannot call cudaMalloc, for example a plugin that its host
+framework hands only input and output buffers, or a latency-critical loop
+where an allocation that may synchronise the device is not allowed.  For them
+moe_route_noalloc keeps its scratch in a fixed array inside the library.  This
+test calls it through the C ABI twice in a row, on different inputs and
+shapes (so stale scratch from the first call would show up in the second),
+and checks each result against moe_route on the same inputs.  It also checks
+that shapes whose scratch would not fit are refused before any work.
+
+The file is named so that pytest collects it last.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from synth import MoEConfig
+
+from _gpu_util import DEV, bf, f32
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    MoEConfig("noalloc_a", T=1000, d=256, N=16, K=4, h=64, cf_num=5, cf_den=4, seed=31),
+    MoEConfig("noalloc_b", T=8192, d=2048, N=64, K=8, h=64, cf_num=1, cf_den=1, seed=32,
+              zipf_s=1.2),
+]
+
+
+@pytest.fixture(scope="module")
+def moe():
+    import __graft_entry__
+    __graft_entry__.build()
+    import combine_expert_gemm_gb300 as m
+    f = m.lib().moe_route_noalloc
+    f.argtypes = [ctypes.POINTER(m.Shape)] + [ctypes.c_void_p] * 10
+    f.restype = ctypes.c_int
+    return m
+
+
+def _outputs(cfg):
+    e = dict(device=DEV)
+    return dict(topk_idx=torch.empty((cfg.T, cfg.K), dtype=torch.int32, **e),
+                topk_gate=torch.empty((cfg.T, cfg.K), dtype=torch.float32, **e),
+                route_row=torch.empty((cfg.T, cfg.K), dtype=torch.int32, **e),
+                expert_count=torch.empty(cfg.N, dtype=torch.int32, **e),
+                expert_offset=torch.empty(cfg.N + 1, dtype=torch.int32, **e),
+                expert_demand=torch.empty(cfg.N, dtype=torch.int32, **e))
+
+
+def test_route_noalloc_matches_route_on_two_calls_in_a_row(moe):
+    results = []
+    for cfg in CASES:
+        x = bf(synth.gen_x(cfg))
+        wr = f32(synth.gen_router(cfg))
+        b = synth.gen_bias(cfg)
+        bias = None if b is None else f32(b)
+        s = moe.Shape(cfg.T, cfg.d, cfg.N, cfg.K, cfg.h, cfg.cap)
+        mine = _outputs(cfg)
+        o = mine
+        stream = torch.cuda.current_stream().cuda_stream
+        rc = moe.lib().moe_route_noalloc(
+            ctypes.byref(s), x.data_ptr(), wr.data_ptr(), None if bias is None else bias.data_ptr(),
+            o["topk_idx"].data_ptr(), o["topk_gate"].data_ptr(), o["route_row"].data_ptr(),
+            o["expert_count"].data_ptr(), o["expert_offset"].data_ptr(),
+            o["expert_demand"].data_ptr(), stream)
+        assert rc == 0, moe.lib().moe_status_string(rc)
+        ref = _outputs(cfg)
+        ws = torch.zeros(moe.route_workspace_bytes(s), dtype=torch.uint8, device=DEV)
+        moe.route(s, x, wr, bias, ref["topk_idx"], ref["topk_gate"], ref["route_row"],
+                  ref["expert_count"], ref["expert_offset"], ref["expert_demand"], ws)
+        torch.cuda.synchronize()
+        results.append((mine, ref))
+    for cfg, (mine, ref) in zip(CASES, results):
+        for k in ("topk_idx", "route_row", "expert_count", "expert_offset", "expert_demand"):
+            assert torch.equal(mine[k], ref[k]), (cfg.name, k)
+        np.testing.assert_allclose(mine["topk_gate"].cpu().numpy(), ref["topk_gate"].cpu().numpy(),
+                                   rtol=1e-5, atol=1e-7)
+    assert int(results[1][0]["expert_offset"][-1]) < CASES[1].T * CASES[1].K  # drops happened
+
+
+def test_route_noalloc_refuses_shapes_past_its_scratch(moe):
+    s = moe.Shape(70000, 64, 1024, 2, 64, 1)   # ceil(70000/256) * 1024 counts > 1 MiB
+    P = ctypes.c_void_p(4096)
+    rc = moe.lib().moe_route_noalloc(ctypes.byref(s), P, P, None, P, P, P, P, P, P, None)
+    assert rc == 5  # MOE_ERR_UNSUPPORTED, before anything is enqueued
