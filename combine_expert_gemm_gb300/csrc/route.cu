@@ -29,8 +29,6 @@
 namespace moe {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kJC = 32;          // j-chunk of the logit tiles
 constexpr int kRankBlock = 256;  // tokens per block of the slot ranking
 
 __device__ __forceinline__ float canon(float v) { return isnan(v) ? -INFINITY : v; }
@@ -39,88 +37,143 @@ __device__ __forceinline__ bool beats(float a, int ia, float b, int ib) {
     return a > b || (a == b && ia < ib);
 }
 
-// TB tokens x EC experts per pass; 256 threads, each a 4 x 4 register tile.
+// Logit tile: TB tokens x EC experts per pass, 512 threads (16 warps), each
+// thread 2 tokens x 4 experts (8 independent fma chains).  A warp covers 8
+// tokens x 32 experts: lane = (tx in 0..7, ty in 0..3); the thread owns tokens
+// ty + 4a and experts tx + 8b of its warp's block.  x (bf16) and W_r (fp32)
+// stream through a 3-stage cp.async ring of j-chunks in their natural
+// row-major layouts; a thread reads 8 consecutive j of a row with one 16-byte
+// load (distinct banks across the warp), so every chain still runs over j in
+// ascending order.
+constexpr int kLogitThreads = 512;
+constexpr int kLogitStages = 3;
+
 template <int TB, int EC>
-__global__ void __launch_bounds__(kThreads)
+struct LogitTile {
+    static constexpr int JC = EC >= 128 ? 32 : 64;  // j per stage
+    static constexpr int XR = JC + 8;               // bf16 per padded x row
+    static constexpr int WR = JC + 4;               // fp32 per padded W row
+    static constexpr int STAGE = TB * XR * 2 + EC * WR * 4;  // bytes
+    static constexpr size_t smem_bytes(int N) {
+        return (size_t)kLogitStages * STAGE + sizeof(float) * (size_t)TB * N;
+    }
+};
+
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+template <int TB, int EC>
+__global__ void __launch_bounds__(kLogitThreads)
 route_logits_topk(int T, int d, int N, int K, const uint16_t *__restrict__ x,
                   const float *__restrict__ w_r, const float *__restrict__ bias,
                   int32_t *__restrict__ topk_idx, float *__restrict__ topk_gate) {
-    static_assert((TB / 4) * (EC / 4) == kThreads, "thread tile");
-    constexpr int XS = TB + 4;  // padded row of the transposed x tile
-    constexpr int WS = EC + 4;
-    extern __shared__ __align__(16) float smem[];
-    float *xs = smem;                 // [kJC][XS]
-    float *wsm = xs + kJC * XS;       // [kJC][WS]
-    float *lg = wsm + kJC * WS;       // [TB][N]
+    using L = LogitTile<TB, EC>;
+    constexpr int JC = L::JC, XR = L::XR, WR = L::WR;
+    static_assert((TB / 8) * (EC / 32) == kLogitThreads / 32, "warp tiling");
+    extern __shared__ __align__(16) uint8_t smem_l[];
+    float *lg = reinterpret_cast<float *>(smem_l + (size_t)kLogitStages * L::STAGE);  // [TB][N]
 
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tx = lane & 7, ty = lane >> 3;
+    const int tok0 = (warp % (TB / 8)) * 8 + ty;   // + 4a
+    const int exp0 = (warp / (TB / 8)) * 32 + tx;  // + 8b
     const int t0 = blockIdx.x * TB;
-    const int tx = tid % (EC / 4), ty = tid / (EC / 4);
+    const int nchunks = (d + JC - 1) / JC;
 
     for (int ec0 = 0; ec0 < N; ec0 += EC) {
-        float acc[4][4];
+        auto issue = [&](int c) {
+            if (c < nchunks) {
+                uint8_t *st = smem_l + (size_t)(c % kLogitStages) * L::STAGE;
+                uint16_t *xs = reinterpret_cast<uint16_t *>(st);
+                float *ws = reinterpret_cast<float *>(st + TB * XR * 2);
+                const int j0 = c * JC, jn = min(JC, d - j0);
+                for (int i = tid; i < TB * (JC / 8); i += kLogitThreads) {
+                    const int r = i / (JC / 8), q = (i % (JC / 8)) * 8;
+                    if (t0 + r < T && q < jn)
+                        cp_async16(xs + r * XR + q, x + (int64_t)(t0 + r) * d + j0 + q);
+                }
+                for (int i = tid; i < EC * (JC / 4); i += kLogitThreads) {
+                    const int r = i / (JC / 4), q = (i % (JC / 4)) * 4;
+                    if (ec0 + r < N && q < jn)
+                        cp_async16(ws + r * WR + q, w_r + (int64_t)(ec0 + r) * d + j0 + q);
+                }
+            }
+            cp_async_commit();
+        };
+
+        float acc[2][4];
 #pragma unroll
-        for (int a = 0; a < 4; ++a)
+        for (int a = 0; a < 2; ++a)
 #pragma unroll
             for (int b = 0; b < 4; ++b) acc[a][b] = 0.0f;
 
-        for (int j0 = 0; j0 < d; j0 += kJC) {
-            const int jn = min(kJC, d - j0);  // multiple of 8
+        __syncthreads();  // the previous pass is done with every stage
+#pragma unroll
+        for (int c = 0; c < kLogitStages - 1; ++c) issue(c);
+        for (int c = 0; c < nchunks; ++c) {
+            cp_async_wait<kLogitStages - 2>();
             __syncthreads();
-            for (int i = tid; i < TB * (kJC / 8); i += kThreads) {
-                const int tok = i / (kJC / 8), jp = (i % (kJC / 8)) * 8;
-                uint4 v = make_uint4(0, 0, 0, 0);
-                if (t0 + tok < T && jp < jn)
-                    v = *reinterpret_cast<const uint4 *>(x + (int64_t)(t0 + tok) * d + j0 + jp);
-                const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+            issue(c + kLogitStages - 1);
+            const uint8_t *st = smem_l + (size_t)(c % kLogitStages) * L::STAGE;
+            const uint16_t *xs = reinterpret_cast<const uint16_t *>(st) + tok0 * XR;
+            const float *ws = reinterpret_cast<const float *>(st + TB * XR * 2) + exp0 * WR;
+            const int jn = min(JC, d - c * JC);
+#pragma unroll 2
+            for (int j = 0; j < jn; j += 8) {
+                float xf[2][8];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    xs[(jp + 2 * q) * XS + tok] = bf16_lo(w4[q]);
-                    xs[(jp + 2 * q + 1) * XS + tok] = bf16_hi(w4[q]);
+                for (int a = 0; a < 2; ++a) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(xs + 4 * a * XR + j);
+                    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        xf[a][2 * q] = bf16_lo(w4[q]);
+                        xf[a][2 * q + 1] = bf16_hi(w4[q]);
+                    }
                 }
-            }
-            for (int i = tid; i < EC * (kJC / 8); i += kThreads) {
-                const int e = i / (kJC / 8), jp = (i % (kJC / 8)) * 8;
-                float4 a = make_float4(0, 0, 0, 0), b = a;
-                if (ec0 + e < N && jp < jn) {
-                    const float4 *src =
-                        reinterpret_cast<const float4 *>(w_r + (int64_t)(ec0 + e) * d + j0 + jp);
-                    a = src[0];
-                    b = src[1];
+                float wf[4][8];
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    const float *wrow = ws + 8 * b * WR + j;
+                    const float4 w0 = *reinterpret_cast<const float4 *>(wrow);
+                    const float4 w1 = *reinterpret_cast<const float4 *>(wrow + 4);
+                    wf[b][0] = w0.x; wf[b][1] = w0.y; wf[b][2] = w0.z; wf[b][3] = w0.w;
+                    wf[b][4] = w1.x; wf[b][5] = w1.y; wf[b][6] = w1.z; wf[b][7] = w1.w;
                 }
-                const float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
-                for (int q = 0; q < 8; ++q) wsm[(jp + q) * WS + e] = f[q];
-            }
-            __syncthreads();
-#pragma unroll 4
-            for (int jj = 0; jj < jn; ++jj) {
-                const float4 xv = *reinterpret_cast<const float4 *>(xs + jj * XS + ty * 4);
-                const float4 wv = *reinterpret_cast<const float4 *>(wsm + jj * WS + tx * 4);
-                const float xa[4] = {xv.x, xv.y, xv.z, xv.w};
-                const float wb[4] = {wv.x, wv.y, wv.z, wv.w};
+                for (int q = 0; q < 8; ++q)
 #pragma unroll
-                for (int a = 0; a < 4; ++a)
+                    for (int a = 0; a < 2; ++a)
 #pragma unroll
-                    for (int b = 0; b < 4; ++b) acc[a][b] = __fmaf_rn(xa[a], wb[b], acc[a][b]);
+                        for (int b = 0; b < 4; ++b)
+                            acc[a][b] = __fmaf_rn(xf[a][q], wf[b][q], acc[a][b]);
             }
         }
+        cp_async_wait<0>();
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
-            const int e = ec0 + tx * 4 + b;
+            const int e = ec0 + exp0 + 8 * b;
             if (e < N) {
                 const float bb = bias ? bias[e] : 0.0f;
 #pragma unroll
-                for (int a = 0; a < 4; ++a)
-                    lg[(ty * 4 + a) * N + e] = bias ? __fadd_rn(acc[a][b], bb) : acc[a][b];
+                for (int a = 0; a < 2; ++a)
+                    lg[(tok0 + 4 * a) * N + e] = bias ? __fadd_rn(acc[a][b], bb) : acc[a][b];
             }
         }
     }
     __syncthreads();
 
     // top-K and gates, one warp per token
-    const int lane = tid & 31, warp = tid >> 5;
-    for (int tt = warp; tt < TB; tt += kThreads / 32) {
+    for (int tt = warp; tt < TB; tt += kLogitThreads / 32) {
         const int t = t0 + tt;
         if (t >= T) break;
         const float *l = lg + tt * N;
@@ -266,8 +319,7 @@ __global__ void route_assign(int T, int N, int K, int cap, const int32_t *__rest
 template <int TB, int EC>
 moe_status launch_logits(const moe_shape *s, const uint16_t *x, const float *w, const float *b,
                          int32_t *idx, float *gate, cudaStream_t st) {
-    const size_t smem =
-        sizeof(float) * ((size_t)kJC * (TB + 4) + (size_t)kJC * (EC + 4) + (size_t)TB * s->N);
+    const size_t smem = LogitTile<TB, EC>::smem_bytes(s->N);
     static size_t configured = 0;
     if (smem > 48 * 1024 && smem > configured) {
         if (cudaFuncSetAttribute(route_logits_topk<TB, EC>,
@@ -277,7 +329,7 @@ moe_status launch_logits(const moe_shape *s, const uint16_t *x, const float *w, 
         configured = smem;
     }
     const int grid = (s->T + TB - 1) / TB;
-    route_logits_topk<TB, EC><<<grid, kThreads, smem, st>>>(s->T, s->d, s->N, s->K, x, w, b, idx,
+    route_logits_topk<TB, EC><<<grid, kLogitThreads, smem, st>>>(s->T, s->d, s->N, s->K, x, w, b, idx,
                                                              gate);
     return launch_status();
 }
@@ -300,9 +352,7 @@ moe_status route_enqueue(const moe_shape *s, const moe_bf16 *x, const float *w_r
     moe_status r = MOE_OK;
     if (s->T > 0) {
         const int n = s->N;
-        if (n <= 8) r = launch_logits<512, 8>(s, x, w_router, bias, topk_idx, topk_gate, st);
-        else if (n <= 16) r = launch_logits<256, 16>(s, x, w_router, bias, topk_idx, topk_gate, st);
-        else if (n <= 32) r = launch_logits<128, 32>(s, x, w_router, bias, topk_idx, topk_gate, st);
+        if (n <= 32) r = launch_logits<128, 32>(s, x, w_router, bias, topk_idx, topk_gate, st);
         else if (n <= 64) r = launch_logits<64, 64>(s, x, w_router, bias, topk_idx, topk_gate, st);
         else r = launch_logits<32, 128>(s, x, w_router, bias, topk_idx, topk_gate, st);
         if (r != MOE_OK) return r;
