@@ -40,7 +40,7 @@ def _declare(L):
         "oracle_route_slots": [_I, _I, _I, _I, _P, _P, _P, _P, _P],
         "oracle_dispatch": [_I, _I, _I, _P, _P, _P],
         "oracle_ffn_fwd_f64": [_I, _I, _I, _P, _P, _P, _P, _I, _P, _P, _P, _P],
-        "oracle_ffn_bwd_f64": [_I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P],
+        "oracle_ffn_bwd_f64": [_I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P],
         "oracle_expert_ffn_rows": [_I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P],
         "oracle_expert_ffn": [_I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P],
         "oracle_combine": [_I, _I, _I, _P, _P, _P, _P],
@@ -186,15 +186,18 @@ def ffn_fwd_f64(x, wg, wu, wd, round_a=False):
     return g, u, a, y
 
 
-def ffn_bwd_f64(x, g, u, a, dy, wg, wu, wd):
-    """fp64 backward of the SwiGLU expert: returns dx, dwg, dwu, dwd."""
+def ffn_bwd_f64(x, g, u, a, dy, wg, wu, wd, round_dgu=False):
+    """fp64 backward of the SwiGLU expert: returns dx, dwg, dwu, dwd.
+
+    round_dgu rounds dG and dU to bf16 before the products that consume them,
+    as the grouped backward does (they are bf16 payloads there)."""
     arrs = [_c(v, np.float64) for v in (x, g, u, a, dy, wg, wu, wd)]
     x, g, u, a, dy, wg, wu, wd = arrs
     n, d = x.shape
     h = wg.shape[0]
     dx = np.empty((n, d)); dwg = np.zeros((h, d)); dwu = np.zeros((h, d)); dwd = np.zeros((d, h))
     lib().oracle_ffn_bwd_f64(n, d, h, _p(x), _p(g), _p(u), _p(a), _p(dy), _p(wg), _p(wu), _p(wd),
-                             _p(dx), _p(dwg), _p(dwu), _p(dwd))
+                             int(round_dgu), _p(dx), _p(dwg), _p(dwu), _p(dwd))
     return dx, dwg, dwu, dwd
 
 

@@ -35,7 +35,7 @@
  *     experts packed back to back from row 0 at cumulative offsets;
  *   - expert FFN: separate W_gate, W_up [N,h,d] and W_down [N,d,h];
  *     silu(z) = z / (1 + exp(-z)); reductions in fp64; bf16 rounding (nearest
- *     even) only where a payload is stored (H, Y, saved G/U, dX);
+ *     even) only where a payload is stored (H, Y, saved G/U, dG/dU, dX);
  *   - combine / dispatch backward: fp32 accumulation over k ascending from 0;
  *     dropped routes add nothing and the kept gates are not renormalised.
  */
@@ -227,7 +227,9 @@ void oracle_ffn_fwd_f64(int nrows, int d, int h, const double *x, const double *
 
 /* Backward of the SwiGLU expert for rows x, given g, u (pre-activation), the
  * stored activation a, and dy (nrows x d).  Accumulates (+=) into dwg, dwu
- * (h x d) and dwd (d x h); writes dx (nrows x d).
+ * (h x d) and dwd (d x h); writes dx (nrows x d).  If round_dgu, dg and du are
+ * rounded to bf16 before they enter the two products that consume them (they
+ * are then stored operands, i.e. bf16 payloads).
  *   da = dy W_down ;  dW_down += dy^T a
  *   du = da * silu(g) ;  dg = da * u * silu'(g),
  *   silu'(z) = s(z) (1 + z (1 - s(z))), s = logistic
@@ -235,8 +237,8 @@ void oracle_ffn_fwd_f64(int nrows, int d, int h, const double *x, const double *
  */
 void oracle_ffn_bwd_f64(int nrows, int d, int h, const double *x, const double *g,
                         const double *u, const double *a, const double *dy, const double *wg,
-                        const double *wu, const double *wd, double *dx, double *dwg,
-                        double *dwu, double *dwd) {
+                        const double *wu, const double *wd, int round_dgu, double *dx,
+                        double *dwg, double *dwu, double *dwd) {
     double *dgv = (double *)malloc((size_t)h * sizeof(double));
     double *duv = (double *)malloc((size_t)h * sizeof(double));
     for (int r = 0; r < nrows; ++r) {
@@ -248,6 +250,10 @@ void oracle_ffn_bwd_f64(int nrows, int d, int h, const double *x, const double *
             double sg = 1.0 / (1.0 + exp(-z));
             duv[i] = da * z * sg;
             dgv[i] = da * u[(int64_t)r * h + i] * sg * (1.0 + z * (1.0 - sg));
+            if (round_dgu) {
+                duv[i] = (double)bf16_to_f32(bf16_from_f64(duv[i]));
+                dgv[i] = (double)bf16_to_f32(bf16_from_f64(dgv[i]));
+            }
         }
         for (int o = 0; o < d; ++o)
             for (int i = 0; i < h; ++i) dwd[(int64_t)o * h + i] += dyr[o] * a[(int64_t)r * h + i];
@@ -396,7 +402,8 @@ void oracle_dispatch_bwd(int T, int d, int K, const uint16_t *dx_disp, const int
 
 /* ------------------------------------------- B2: grouped expert backward ---
  * [EP] 5.7: expert backward and Wgrad run over the valid rows only.  Uses the
- * stored bf16 G, U and H of the forward.  dx_disp is a bf16 payload; the weight
+ * stored bf16 G, U and H of the forward; dG and dU are bf16 payloads between
+ * the two backward products.  dx_disp is a bf16 payload; the weight
  * gradients are fp32 [N,h,d], [N,h,d], [N,d,h] (fully written; experts with no
  * rows get zero).
  */
@@ -425,7 +432,7 @@ void oracle_expert_ffn_bwd(int N, int d, int h, const int32_t *count, const int3
             double *wue = widen_bf16(wu + (int64_t)e * hd, hd);
             double *wde = widen_bf16(wd + (int64_t)e * hd, hd);
             double *dx = (double *)malloc((size_t)n * d * sizeof(double));
-            oracle_ffn_bwd_f64(n, d, h, x, g, u, a, dy, wge, wue, wde, dx, dwg64, dwu64, dwd64);
+            oracle_ffn_bwd_f64(n, d, h, x, g, u, a, dy, wge, wue, wde, 1, dx, dwg64, dwu64, dwd64);
             for (int64_t i = 0; i < (int64_t)n * d; ++i) dx_disp[r0 * d + i] = bf16_from_f64(dx[i]);
             free(x); free(g); free(u); free(a); free(dy); free(wge); free(wue); free(wde); free(dx);
         }

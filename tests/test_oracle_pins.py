@@ -535,7 +535,34 @@ def test_expert_backward_grouped_matches_core_and_weight_grad_fd():
     e, r0, n = 2, int(offset[2]), int(count[2])
     cdx, cdwg, cdwu, cdwd = oracle.ffn_bwd_f64(f(x[r0:r0 + n]), f(gs[r0:r0 + n]), f(us[r0:r0 + n]),
                                                f(h[r0:r0 + n]), f(dyd[r0:r0 + n]), f(wg[e]),
-                                               f(wu[e]), f(wd[e]))
+                                               f(wu[e]), f(wd[e]), round_dgu=True)
     assert np.array_equal(dx[r0:r0 + n], oracle.bf16_from_f64(cdx))
     np.testing.assert_allclose(dwg[e], cdwg.astype(np.float32), rtol=1e-6, atol=1e-12)
     np.testing.assert_allclose(dwd[e], cdwd.astype(np.float32), rtol=1e-6, atol=1e-12)
+
+
+def test_expert_backward_bf16_intermediates_stay_within_rounding():
+    """With dG, dU rounded to bf16 the backward differs from the unrounded fp64
+    one by no more than that rounding (half an ulp, 2^-9 relative, per term);
+    dW_down, which never sees dG or dU, is unchanged."""
+    rng = np.random.default_rng(4)
+    n, d, h = 6, 16, 12
+    x = rng.standard_normal((n, d))
+    wg, wu, wd = (rng.standard_normal((h, d)) * 0.3, rng.standard_normal((h, d)) * 0.3,
+                  rng.standard_normal((d, h)) * 0.3)
+    dy = rng.standard_normal((n, d))
+    g, u, a, y = oracle.ffn_fwd_f64(x, wg, wu, wd)
+    exact = oracle.ffn_bwd_f64(x, g, u, a, dy, wg, wu, wd)
+    rounded = oracle.ffn_bwd_f64(x, g, u, a, dy, wg, wu, wd, round_dgu=True)
+    assert np.array_equal(exact[3], rounded[3])
+    # the same products evaluated by hand from the rounded intermediates
+    s = 1 / (1 + np.exp(-g))
+    da = dy @ wd
+    du = da * g * s
+    dg = da * u * s * (1 + g * (1 - s))
+    q = lambda v: oracle.bf16_to_f32(oracle.bf16_from_f64(v)).astype(np.float64)
+    for got, want in [(rounded[0], q(dg) @ wg + q(du) @ wu), (rounded[1], q(dg).T @ x),
+                      (rounded[2], q(du).T @ x)]:
+        np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+    for e_, r_ in zip(exact[:3], rounded[:3]):
+        assert np.max(np.abs(e_ - r_)) <= 2.0 ** -8 * np.max(np.abs(e_)) * max(d, h)
