@@ -67,7 +67,8 @@ def algorithmic(cfg, A):
     )
     if cfg.backward:
         out.update(combine_bwd_bytes=2.0 * T * d + 2.0 * A * d + 2.0 * A * d + 8.0 * T * K,
-                   dispatch_bwd_bytes=2.0 * A * d + 4.0 * T * d + 4.0 * T * K)
+                   dispatch_bwd_bytes=2.0 * A * d + 4.0 * T * d + 4.0 * T * K,
+                   gemm_bwd_flop=12.0 * d * h * A)
     return out
 
 
@@ -146,15 +147,12 @@ def run_ours(args, cfg, rank, world):
     dy = bf(synth.gen_dy(rcfg)) if cfg.backward else None
     shape = moe.Shape(cfg.T, cfg.d, cfg.N, cfg.K, cfg.h, cfg.cap)
     buf = moe.LayerBuffers(shape, dev, save_for_backward=cfg.backward)
-    if cfg.backward:
-        dy_disp = torch.empty((cfg.R, cfg.d), dtype=torch.bfloat16, device=dev)
-        dgate = torch.empty((cfg.T, cfg.K), dtype=torch.float32, device=dev)
-        dx = torch.empty((cfg.T, cfg.d), dtype=torch.float32, device=dev)
+    bwd = moe.BackwardBuffers(shape, dev) if cfg.backward else None
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
-    phases = ["route", "dispatch", "ffn", "combine"] + (["combine_bwd", "dispatch_bwd"]
-                                                         if cfg.backward else [])
-    launches_per_step = 8 + (2 if cfg.backward else 0)
+    phases = ["route", "dispatch", "ffn", "combine"] + (
+        ["combine_bwd", "ffn_bwd", "dispatch_bwd"] if cfg.backward else [])
+    launches_per_step = 8 + (6 if cfg.backward else 0)
 
     def step(ev=None):
         def mark(i):
@@ -172,17 +170,23 @@ def run_ours(args, cfg, rank, world):
         moe.combine(shape, buf.y_disp, buf.route_row, buf.topk_gate, buf.y)
         mark(4)
         if cfg.backward:
-            moe.combine_backward(shape, dy, buf.y_disp, buf.route_row, buf.topk_gate, dy_disp,
-                                 dgate)
+            moe.combine_backward(shape, dy, buf.y_disp, buf.route_row, buf.topk_gate,
+                                 bwd.dy_disp, bwd.dgate)
             mark(5)
-            moe.dispatch_backward(shape, dy_disp, buf.route_row, dx)
+            moe.expert_ffn_backward(shape, buf.x_disp, buf.expert_count, buf.expert_offset, wg, wu,
+                                    wd, buf.g_save, buf.u_save, buf.h_act, bwd.dy_disp,
+                                    bwd.dx_disp, bwd.dw_gate, bwd.dw_up, bwd.dw_down, bwd.ws)
             mark(6)
+            moe.dispatch_backward(shape, bwd.dx_disp, buf.route_row, bwd.dx)
+            mark(7)
 
     for _ in range(args.warmup):
         flush.zero_()
         step()
     torch.cuda.synchronize()
     assert moe.read_device_error(buf.route_ws) == 0 and moe.read_device_error(buf.ffn_ws) == 0
+    if bwd is not None:
+        assert moe.read_device_error(bwd.ws) == 0
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(phases) + 1)]
            for _ in range(args.steps)]
@@ -290,9 +294,11 @@ def run_ours(args, cfg, rank, world):
         "wall_s_timed_region": t_wall,
     }
     if cfg.backward:
+        bt = alg["gemm_bwd_flop"] / (ph_ms["ffn_bwd"] / 1e3) / 1e12
         line["backward"] = {
             "combine_bwd_gbs": alg["combine_bwd_bytes"] / (ph_ms["combine_bwd"] / 1e3) / 1e9,
-            "dispatch_bwd_gbs": alg["dispatch_bwd_bytes"] / (ph_ms["dispatch_bwd"] / 1e3) / 1e9}
+            "dispatch_bwd_gbs": alg["dispatch_bwd_bytes"] / (ph_ms["dispatch_bwd"] / 1e3) / 1e9,
+            "expert_bwd_tflops": bt, "expert_bwd_frac": bt / pk["bf16"]}
     if rank == 0 and not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(cfg, args.cpu_budget_s)
     if dist:

@@ -19,7 +19,8 @@ from .build import LIB
 __all__ = ["Shape", "MoEError", "lib", "route", "dispatch", "expert_ffn", "combine",
            "combine_backward", "dispatch_backward", "read_device_error",
            "route_workspace_bytes", "expert_ffn_workspace_bytes", "capacity", "LayerBuffers",
-           "layer_forward"]
+           "layer_forward", "expert_ffn_backward", "expert_ffn_backward_workspace_bytes",
+           "BackwardBuffers", "layer_backward"]
 
 if not os.path.exists(LIB):
     raise ImportError(f"{LIB} is missing: build it with `python combine_expert_gemm_gb300/build.py` "
@@ -58,6 +59,8 @@ _SIG = {
     "moe_combine_backward": ([_SP, _P, _P, _P, _P, _P, _P, _P], ctypes.c_int),
     "moe_dispatch_backward": ([_SP, _P, _P, _P, _P], ctypes.c_int),
     "moe_read_device_error": ([_P, ctypes.POINTER(ctypes.c_int32), _P], ctypes.c_int),
+    "moe_expert_ffn_backward_workspace_bytes": ([_SP], _SZ),
+    "moe_expert_ffn_backward": ([_SP] + [_P] * 14 + [_P, _SZ, _P], ctypes.c_int),
 }
 for _name, (_args, _res) in _SIG.items():
     _f = getattr(_lib, _name)
@@ -164,6 +167,22 @@ def dispatch_backward(shape, dx_disp, route_row, dx, stream=None):
                                       _stream(stream)), "moe_dispatch_backward")
 
 
+def expert_ffn_backward_workspace_bytes(shape):
+    return int(_lib.moe_expert_ffn_backward_workspace_bytes(ctypes.byref(shape)))
+
+
+def expert_ffn_backward(shape, x_disp, expert_count, expert_offset, w_gate, w_up, w_down, g_save,
+                        u_save, h_act, dy_disp, dx_disp, dw_gate, dw_up, dw_down, ws, stream=None):
+    _check(_lib.moe_expert_ffn_backward(
+        ctypes.byref(shape), _ptr(x_disp, _bf16, "x_disp"), _ptr(expert_count, _i32, "expert_count"),
+        _ptr(expert_offset, _i32, "expert_offset"), _ptr(w_gate, _bf16, "w_gate"),
+        _ptr(w_up, _bf16, "w_up"), _ptr(w_down, _bf16, "w_down"), _ptr(g_save, _bf16, "g_save"),
+        _ptr(u_save, _bf16, "u_save"), _ptr(h_act, _bf16, "h_act"), _ptr(dy_disp, _bf16, "dy_disp"),
+        _ptr(dx_disp, _bf16, "dx_disp"), _ptr(dw_gate, _f32, "dw_gate"), _ptr(dw_up, _f32, "dw_up"),
+        _ptr(dw_down, _f32, "dw_down"), _ptr(ws, None, "ws"), ws.numel() * ws.element_size(),
+        _stream(stream)), "moe_expert_ffn_backward")
+
+
 def read_device_error(ws, stream=None):
     code = ctypes.c_int32(0)
     _check(_lib.moe_read_device_error(_ptr(ws, None, "ws"), ctypes.byref(code), _stream(stream)),
@@ -205,3 +224,35 @@ def layer_forward(buf, x, w_router, bias, w_gate, w_up, w_down, stream=None):
                buf.h_act, buf.g_save, buf.u_save, buf.y_disp, buf.ffn_ws, stream)
     combine(s, buf.y_disp, buf.route_row, buf.topk_gate, buf.y, stream)
     return buf.y
+
+
+class BackwardBuffers:
+    """Device buffers of one layer's backward (allocated once before the loop)."""
+
+    def __init__(self, shape, device="cuda"):
+        T, d, N, K, h, R = shape.T, shape.d, shape.N, shape.K, shape.h, shape.R
+        e = dict(device=device)
+        self.shape = shape
+        self.dy_disp = torch.empty((R, d), dtype=_bf16, **e)
+        self.dgate = torch.empty((T, K), dtype=_f32, **e)
+        self.dx_disp = torch.empty((R, d), dtype=_bf16, **e)
+        self.dx = torch.empty((T, d), dtype=_f32, **e)
+        self.dw_gate = torch.empty((N, h, d), dtype=_f32, **e)
+        self.dw_up = torch.empty((N, h, d), dtype=_f32, **e)
+        self.dw_down = torch.empty((N, d, h), dtype=_f32, **e)
+        self.ws = torch.zeros(max(expert_ffn_backward_workspace_bytes(shape), 256),
+                              dtype=torch.uint8, **e)
+
+
+def layer_backward(fwd, bwd, dy, w_gate, w_up, w_down, stream=None):
+    """Combine backward -> grouped expert backward -> dispatch backward (3 C-ABI
+    calls) for the forward whose buffers are `fwd` (saved with
+    save_for_backward=True).  Fills bwd.dgate, bwd.dx, bwd.dw_*."""
+    s = fwd.shape
+    combine_backward(s, dy, fwd.y_disp, fwd.route_row, fwd.topk_gate, bwd.dy_disp, bwd.dgate,
+                     stream)
+    expert_ffn_backward(s, fwd.x_disp, fwd.expert_count, fwd.expert_offset, w_gate, w_up, w_down,
+                        fwd.g_save, fwd.u_save, fwd.h_act, bwd.dy_disp, bwd.dx_disp, bwd.dw_gate,
+                        bwd.dw_up, bwd.dw_down, bwd.ws, stream)
+    dispatch_backward(s, bwd.dx_disp, fwd.route_row, bwd.dx, stream)
+    return bwd

@@ -23,7 +23,6 @@
 // the tail) enter the MMA but are never stored; column tiles past the output
 // width are never stored either.  No host round trip, no per-expert launch.
 #include <algorithm>
-#include <mutex>
 
 #include "moe_common.cuh"
 
@@ -296,40 +295,6 @@ grouped_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
 }
 
 // ---------------------------------------------------------------- host side --
-
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    });
-    return fn;
-}
-
-// 2-D bf16 map over a row-major [rows, inner] matrix, box 64 x box_rows,
-// 128-byte swizzle (matches sw128_kmajor_desc on the device).
-bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    const cuuint64_t dims[2] = {inner, rows};
-    const cuuint64_t strides[1] = {inner * 2};
-    const cuuint32_t box[2] = {BK, box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
 
 template <int EPI>
 moe_status launch_gemm(const CUtensorMap &a, const CUtensorMap &b0, const CUtensorMap &b1, int N,

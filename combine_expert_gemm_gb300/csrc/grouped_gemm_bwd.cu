@@ -1,0 +1,515 @@
+// Grouped expert backward (step B2): data gradients and weight gradients of
+// the bias-free SwiGLU experts over the packed capacity buffers.
+//
+// OLMo-core MoE report, "Section 05: Expert Parallelism", 5.7 (expert backward
+// receives the real per-expert row offsets; the weight-gradient GEMM skips the
+// unwritten tail of the capacity buffer); Figure 14 (Linear 1 -> SwiGLU ->
+// Linear 2); "Section 08: Synchronization-Free Training", 8.5 (grouped GEMMs
+// driven by device offsets).  For expert e with rows X, saved G, U, H and
+// output gradient dY (all [rows, .]):
+//   dH = dY W_down                           (dgrad, M = rows, K = d)
+//   dU = dH * silu(G),  dG = dH * U * silu'(G)  (fused into the dH epilogue)
+//   dX = dG W_gate + dU W_up                  (dgrad, M = rows, K = 2h)
+//   dW_down = dY^T H                          (wgrad, K = rows of e)
+//   dW_gate = dG^T X,  dW_up = dU^T X         (wgrad, K = rows of e)
+//
+// Same engine as the forward kernel (persistent, one CTA per SM, TMA 4-stage
+// ring with 128-byte swizzle, one thread issuing tcgen05.mma M=128 N=256 into
+// a double-buffered TMEM accumulator, four epilogue warps).  The backward
+// operands that are transposed relative to their storage (weights in dgrad,
+// activations in wgrad) are read MN-major: a TMA box of 64 M/N elements x 64 K
+// rows lands as 64 swizzled 128-byte rows and the MMA descriptor walks it with
+// K rows 128 B apart, 8-row groups 1 KB apart and 64-element M/N blocks 8 KB
+// apart.  No transposed copy of anything is made.
+//
+// In wgrad the reduction runs over an expert's rows, so the last k-block of a
+// tile can reach into the next expert's rows or the tail (which may hold NaN).
+// The MMA warp waits for that block like any other, issues only the 16-row
+// MMA steps that hold valid rows, and first writes zeros over the invalid rows
+// inside the last of those steps (both operands), fencing them to the tensor
+// core's async proxy.
+#include <algorithm>
+
+#include "moe_common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int MMA_N = 256;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = MMA_N * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int BLK = 64 * BK * 2;  // one MN-major 64 x 64 block: 8 KB
+constexpr int ACC_COLS = 256;
+constexpr int TMEM_COLS = 512;
+
+enum { DGRAD_DH = 0, DGRAD_DX = 1, WGRAD_DOWN = 2, WGRAD_GATEUP = 3 };
+
+template <int MODE>
+struct ModeT {
+    static constexpr bool kgroup = MODE >= WGRAD_DOWN;  // K = rows of an expert
+    static constexpr int threads = 192;
+};
+
+// Shared-memory descriptor of an MN-major operand tile (128-byte swizzle):
+// each 128-byte row holds 64 M/N elements of one K index; K rows are 128 B
+// apart, 8-row groups 1024 B apart (stride-dimension offset), 64-element M/N
+// blocks 8 KB apart (leading-dimension offset).
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t smem_addr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((smem_addr >> 4) & 0x3FFFu);
+    d |= (uint64_t)(BLK >> 4) << 16;
+    d |= (uint64_t)(1024u >> 4) << 32;
+    d |= (uint64_t)1u << 46;
+    d |= (uint64_t)2u << 61;
+    return d;
+}
+
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_major(int M, int N, int a_mn, int b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+struct alignas(8) Bars {
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint32_t tmem_base;
+    int abort;
+};
+
+constexpr size_t smem_bytes(int N) {
+    return 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(Bars) + sizeof(int32_t) * (N + 1) + 16;
+}
+
+struct Params {
+    int N, d, h;
+    int ntn;       // output column tiles of 256
+    int mtn;       // wgrad: output row tiles of 128 (both halves for gate/up)
+    const int32_t *count, *offset;
+    const uint16_t *g_save, *u_save;  // DGRAD_DH epilogue inputs
+    uint16_t *out0, *out1;            // DH: dG, dU; DX: dx_disp
+    float *fout0, *fout1;             // wgrad: dW (down) or (gate, up)
+    int *status;
+};
+
+struct Tile {
+    int e, m, n;
+};
+
+__device__ __forceinline__ Tile map_tile(int MODE_kgroup, int g, const Params &p,
+                                         const int32_t *tile_start) {
+    if (MODE_kgroup) {
+        const int tpe = p.mtn * p.ntn;
+        const int e = g / tpe, l = g % tpe;
+        return Tile{e, l % p.mtn, l / p.mtn};
+    }
+    int lo = 0, hi = p.N - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (tile_start[mid] <= g) lo = mid;
+        else hi = mid - 1;
+    }
+    const int mt = (p.count[lo] + BM - 1) / BM;
+    const int l = g - tile_start[lo];
+    return Tile{lo, l % mt, l / mt};
+}
+
+template <int MODE>
+__device__ __forceinline__ int k_blocks(const Params &p, int cnt) {
+    if (MODE == DGRAD_DH) return p.d / BK;
+    if (MODE == DGRAD_DX) return 2 * p.h / BK;
+    return (cnt + BK - 1) / BK;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(ModeT<MODE>::threads, 1)
+grouped_gemm_bwd(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
+                 const __grid_constant__ CUtensorMap tm_b0, const __grid_constant__ CUtensorMap tm_b1,
+                 const Params p) {
+    constexpr bool KG = ModeT<MODE>::kgroup;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    Bars *bars = reinterpret_cast<Bars *>(smem + (size_t)STAGES * STAGE_BYTES);
+    int32_t *tile_start = reinterpret_cast<int32_t *>(bars + 1);
+    volatile int *abort = &bars->abort;
+    int *status = p.status;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_u32(&bars->full[s]), 1);
+            mbar_init(smem_u32(&bars->empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&bars->tfull[b]), 1);
+            mbar_init(smem_u32(&bars->tempty[b]), 128);
+        }
+        bars->abort = 0;
+        fence_mbar_init();
+    }
+    if (!KG && warp == 0) {
+        int carry = 0;
+        for (int base = 0; base < p.N; base += 32) {
+            const int e = base + lane;
+            const int v = e < p.N ? ((p.count[e] + BM - 1) / BM) * p.ntn : 0;
+            int incl = v;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int u = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+                if (lane >= off) incl += u;
+            }
+            if (e < p.N) tile_start[e] = carry + incl - v;
+            carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+        }
+        if (lane == 0) tile_start[p.N] = carry;
+    }
+    if (warp == 1) tmem_alloc(smem_u32(&bars->tmem_base), TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = bars->tmem_base;
+    const int total = KG ? p.N * p.mtn * p.ntn : tile_start[p.N];
+    const int hb = p.h / BK;  // k-blocks per half of the dX reduction
+    const int mt_half = (p.h + BM - 1) / BM;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_a0);
+            tma_prefetch_desc(&tm_b0);
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int g = blockIdx.x; g < total && ok; g += gridDim.x) {
+                const Tile t = map_tile(KG, g, p, tile_start);
+                const int cnt = p.count[t.e], off = p.offset[t.e];
+                const int nk = k_blocks<MODE>(p, cnt);
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!mbar_wait(smem_u32(&bars->empty[stage]), phase ^ 1, status, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t full = smem_u32(&bars->full[stage]);
+                    const uint32_t sa = smem_u32(smem + (size_t)stage * STAGE_BYTES);
+                    const uint32_t sb = sa + A_BYTES;
+                    mbar_arrive_expect_tx(full, STAGE_BYTES);
+                    const int ncol = t.n * MMA_N;
+                    if (MODE == DGRAD_DH) {
+                        tma_load_2d(sa, &tm_a0, full, kb * BK, off + t.m * BM);
+                        for (int q = 0; q < 4; ++q)
+                            tma_load_2d(sb + q * BLK, &tm_b0, full, ncol + 64 * q, t.e * p.d + kb * BK);
+                    } else if (MODE == DGRAD_DX) {
+                        const bool up = kb >= hb;
+                        const int kk = up ? kb - hb : kb;
+                        tma_load_2d(sa, up ? &tm_a1 : &tm_a0, full, kk * BK, off + t.m * BM);
+                        for (int q = 0; q < 4; ++q)
+                            tma_load_2d(sb + q * BLK, up ? &tm_b1 : &tm_b0, full, ncol + 64 * q,
+                                        t.e * p.h + kk * BK);
+                    } else {
+                        const int row = off + kb * BK;
+                        const bool up = MODE == WGRAD_GATEUP && t.m >= mt_half;
+                        const int mcol = (MODE == WGRAD_GATEUP && up ? t.m - mt_half : t.m) * BM;
+                        for (int q = 0; q < 2; ++q)
+                            tma_load_2d(sa + q * BLK, up ? &tm_a1 : &tm_a0, full, mcol + 64 * q, row);
+                        for (int q = 0; q < 4; ++q)
+                            tma_load_2d(sb + q * BLK, &tm_b0, full, ncol + 64 * q, row);
+                    }
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+            }
+            if (!ok) {
+                for (int s = 0; s < STAGES; ++s) {
+                    volatile int no_abort = 0;
+                    mbar_wait(smem_u32(&bars->full[s]), phase ^ (s >= stage ? 1 : 0), status,
+                              &no_abort);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        // the whole warp follows the ring (it zeroes ragged rows in wgrad);
+        // lane 0 issues the MMAs and commits
+        constexpr uint32_t idesc = idesc_bf16_f32_major(BM, MMA_N, KG ? 1 : 0, 1);
+        int stage = 0;
+        uint32_t phase = 0;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool ok = true;
+        for (int g = blockIdx.x; g < total && ok; g += gridDim.x) {
+            const Tile t = map_tile(KG, g, p, tile_start);
+            const int cnt = p.count[t.e];
+            const int nk = k_blocks<MODE>(p, cnt);
+            // every lane waits; the outcome is made warp-uniform
+            if (!__all_sync(0xFFFFFFFFu,
+                            mbar_wait(smem_u32(&bars->tempty[acc]), acc_phase ^ 1, status, abort)))
+                break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + (uint32_t)(acc * ACC_COLS);
+            for (int kb = 0; kb < nk; ++kb) {
+                if (!__all_sync(0xFFFFFFFFu,
+                                mbar_wait(smem_u32(&bars->full[stage]), phase, status, abort))) {
+                    ok = false;
+                    break;
+                }
+                int steps = BK / 16;
+                if (KG && kb == nk - 1) {
+                    const int rv = cnt - kb * BK;  // valid rows, 1..64
+                    steps = (rv + 15) / 16;
+                    const int r16 = steps * 16;
+                    if (rv < r16) {
+                        // zero rows rv..r16-1 of the 2 A and 4 B MN-major blocks
+                        uint8_t *base = smem + (size_t)stage * STAGE_BYTES;
+                        const int nrow = r16 - rv;
+                        for (int i = lane; i < 6 * nrow * 8; i += 32) {
+                            const int blk = i / (nrow * 8), rem = i % (nrow * 8);
+                            const int row = rv + rem / 8, chunk = rem % 8;
+                            *reinterpret_cast<uint4 *>(base + blk * BLK + row * 128 + chunk * 16) =
+                                make_uint4(0, 0, 0, 0);
+                        }
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    }
+                    __syncwarp();
+                }
+                if (lane == 0) {
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + (size_t)stage * STAGE_BYTES);
+                    const uint32_t sb = sa + A_BYTES;
+                    for (int kk = 0; kk < steps; ++kk) {
+                        const uint64_t ad = KG ? sw128_mnmajor_desc(sa + kk * 2048)
+                                               : sw128_kmajor_desc(sa + kk * 32);
+                        tc_mma_bf16(d_tmem, ad, sw128_mnmajor_desc(sb + kk * 2048), idesc,
+                                    (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    tc_commit(smem_u32(&bars->empty[stage]));
+                }
+                __syncwarp();
+                if (++stage == STAGES) { stage = 0; phase ^= 1; }
+            }
+            if (!ok) break;
+            if (lane == 0) tc_commit(smem_u32(&bars->tfull[acc]));
+            __syncwarp();
+            if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+        }
+    } else {
+        // --------------------------------------------------------- epilogue
+        const int quad = warp & 3;
+        const int rit = quad * 32 + lane;  // row of the tile = TMEM lane
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int g = blockIdx.x; g < total; g += gridDim.x) {
+            const Tile t = map_tile(KG, g, p, tile_start);
+            const int cnt = p.count[t.e], off = p.offset[t.e];
+            if (!mbar_wait(smem_u32(&bars->tfull[acc]), acc_phase, status, abort)) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * ACC_COLS;
+            if (!KG) {
+                const bool row_ok = rit < cnt - t.m * BM;
+                const int64_t row = (int64_t)off + t.m * BM + rit;
+                const int width = MODE == DGRAD_DH ? p.h : p.d;
+                for (int c = 0; c < MMA_N; c += 16) {
+                    uint32_t r[16];
+                    tmem_ld16(tbase + c, r);
+                    tmem_ld_wait();
+                    reg_fence(r);
+                    const int col = t.n * MMA_N + c;
+                    if (!row_ok || col >= width) continue;
+                    if (MODE == DGRAD_DH) {
+                        const uint4 *gp = reinterpret_cast<const uint4 *>(p.g_save + row * p.h + col);
+                        const uint4 *up = reinterpret_cast<const uint4 *>(p.u_save + row * p.h + col);
+                        const uint4 gv[2] = {gp[0], gp[1]}, uv[2] = {up[0], up[1]};
+                        const uint32_t *gw = reinterpret_cast<const uint32_t *>(gv);
+                        const uint32_t *uw = reinterpret_cast<const uint32_t *>(uv);
+                        uint32_t dg[8], du[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            float rg[2], ru[2];
+#pragma unroll
+                            for (int hf = 0; hf < 2; ++hf) {
+                                const float z = hf ? bf16_hi(gw[i]) : bf16_lo(gw[i]);
+                                const float u = hf ? bf16_hi(uw[i]) : bf16_lo(uw[i]);
+                                const float dh = __uint_as_float(r[2 * i + hf]);
+                                const float sg = 1.0f / (1.0f + __expf(-z));
+                                ru[hf] = dh * (z * sg);
+                                rg[hf] = dh * u * sg * (1.0f + z * (1.0f - sg));
+                            }
+                            dg[i] = pack_bf16x2(rg[0], rg[1]);
+                            du[i] = pack_bf16x2(ru[0], ru[1]);
+                        }
+                        uint4 *gd = reinterpret_cast<uint4 *>(p.out0 + row * p.h + col);
+                        uint4 *ud = reinterpret_cast<uint4 *>(p.out1 + row * p.h + col);
+                        gd[0] = make_uint4(dg[0], dg[1], dg[2], dg[3]);
+                        gd[1] = make_uint4(dg[4], dg[5], dg[6], dg[7]);
+                        ud[0] = make_uint4(du[0], du[1], du[2], du[3]);
+                        ud[1] = make_uint4(du[4], du[5], du[6], du[7]);
+                    } else {
+                        uint32_t pk[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]),
+                                                __uint_as_float(r[2 * i + 1]));
+                        uint4 *dst = reinterpret_cast<uint4 *>(p.out0 + row * p.d + col);
+                        dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                        dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                    }
+                }
+            } else {
+                // weight gradient, fp32; an expert without rows gets zeros
+                const bool up = MODE == WGRAD_GATEUP && t.m >= mt_half;
+                const int mrow = (up ? t.m - mt_half : t.m) * BM + rit;
+                const int mlim = MODE == WGRAD_DOWN ? p.d : p.h;
+                const int width = MODE == WGRAD_DOWN ? p.h : p.d;
+                float *out = (up ? p.fout1 : p.fout0) + (int64_t)t.e * mlim * width;
+                for (int c = 0; c < MMA_N; c += 16) {
+                    uint32_t r[16];
+                    tmem_ld16(tbase + c, r);
+                    tmem_ld_wait();
+                    reg_fence(r);
+                    const int col = t.n * MMA_N + c;
+                    if (mrow >= mlim || col >= width) continue;
+                    float4 *dst = reinterpret_cast<float4 *>(out + (int64_t)mrow * width + col);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        float4 v = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                               __uint_as_float(r[4 * i + 2]),
+                                               __uint_as_float(r[4 * i + 3]));
+                        if (cnt == 0) v = make_float4(0.f, 0.f, 0.f, 0.f);
+                        dst[i] = v;
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bars->tempty[acc]));
+            if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+template <int MODE>
+moe_status launch_bwd(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap &b0,
+                      const CUtensorMap &b1, const Params &p, int max_tiles, cudaStream_t st) {
+    static size_t configured = 0;
+    const size_t smem = smem_bytes(p.N);
+    if (smem > configured) {
+        if (cudaFuncSetAttribute(grouped_gemm_bwd<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem_bytes(kMaxN)) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        configured = smem_bytes(kMaxN);
+    }
+    const int grid = std::min(num_sms(), std::max(max_tiles, 1));
+    grouped_gemm_bwd<MODE><<<grid, ModeT<MODE>::threads, smem, st>>>(a0, a1, b0, b1, p);
+    return launch_status();
+}
+
+inline size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+MOE_API size_t moe_expert_ffn_backward_workspace_bytes(const moe_shape *s) {
+    if (check_shape(s) != MOE_OK) return 0;
+    const size_t R = (size_t)s->N * s->cap;
+    return 256 + 2 * align256(R * s->h * 2);
+}
+
+MOE_API moe_status moe_expert_ffn_backward(
+    const moe_shape *s, const moe_bf16 *x_disp, const int32_t *expert_count,
+    const int32_t *expert_offset, const moe_bf16 *w_gate, const moe_bf16 *w_up,
+    const moe_bf16 *w_down, const moe_bf16 *g_save, const moe_bf16 *u_save, const moe_bf16 *h_act,
+    const moe_bf16 *dy_disp, moe_bf16 *dx_disp, float *dw_gate, float *dw_up, float *dw_down,
+    void *ws, size_t ws_bytes, cudaStream_t stream) {
+    moe_status r = check_shape(s);
+    if (r != MOE_OK) return r;
+    if (s->d % BK != 0 || s->h % BK != 0) return MOE_ERR_UNSUPPORTED;
+    if (!expert_count || !expert_offset || !ws || !w_gate || !w_up || !w_down || !dw_gate ||
+        !dw_up || !dw_down)
+        return MOE_ERR_INVALID_ARG;
+    const int64_t R = (int64_t)s->N * s->cap;
+    if (R > 0 && (!x_disp || !g_save || !u_save || !h_act || !dy_disp || !dx_disp))
+        return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < moe_expert_ffn_backward_workspace_bytes(s) ||
+        (reinterpret_cast<uintptr_t>(ws) & 255u))
+        return MOE_ERR_WORKSPACE;
+    const void *ptrs[] = {x_disp, w_gate, w_up, w_down, g_save, u_save, h_act, dy_disp, dx_disp,
+                          dw_gate, dw_up, dw_down, expert_count, expert_offset};
+    for (const void *q : ptrs)
+        if (!aligned16(q)) return MOE_ERR_ALIGNMENT;
+
+    Params p{};
+    p.N = s->N;
+    p.d = s->d;
+    p.h = s->h;
+    p.count = expert_count;
+    p.offset = expert_offset;
+    p.status = static_cast<int *>(ws);
+    uint16_t *dG = reinterpret_cast<uint16_t *>(static_cast<char *>(ws) + 256);
+    uint16_t *dU = reinterpret_cast<uint16_t *>(static_cast<char *>(ws) + 256 +
+                                                align256((size_t)R * s->h * 2));
+    const int64_t rows = std::min<int64_t>(R, (int64_t)s->T * s->K);
+    const int row_tiles = (int)((rows + BM - 1) / BM + s->N);
+    const int wg_mt = 2 * ((s->h + BM - 1) / BM);
+
+    if (R == 0) {
+        // no rows at all: every weight gradient is zero; run the wgrad launches
+        // anyway?  They need row buffers for their maps, so clear directly.
+        const size_t hd = (size_t)s->N * s->h * s->d * sizeof(float);
+        if (cudaMemsetAsync(dw_gate, 0, hd, stream) != cudaSuccess ||
+            cudaMemsetAsync(dw_up, 0, hd, stream) != cudaSuccess ||
+            cudaMemsetAsync(dw_down, 0, hd, stream) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        return MOE_OK;
+    }
+
+    CUtensorMap dy_k, wd_mn, dg_k, du_k, wg_mn, wu_mn, dy_mn, h_mn, dg_mn, du_mn, x_mn;
+    const uint64_t Nd = (uint64_t)s->N * s->d, Nh = (uint64_t)s->N * s->h;
+    if (!make_map(&dy_k, dy_disp, s->d, R, BM) || !make_map(&wd_mn, w_down, s->h, Nd, 64) ||
+        !make_map(&dg_k, dG, s->h, R, BM) || !make_map(&du_k, dU, s->h, R, BM) ||
+        !make_map(&wg_mn, w_gate, s->d, Nh, 64) || !make_map(&wu_mn, w_up, s->d, Nh, 64) ||
+        !make_map(&dy_mn, dy_disp, s->d, R, 64) || !make_map(&h_mn, h_act, s->h, R, 64) ||
+        !make_map(&dg_mn, dG, s->h, R, 64) || !make_map(&du_mn, dU, s->h, R, 64) ||
+        !make_map(&x_mn, x_disp, s->d, R, 64))
+        return MOE_ERR_CUDA;
+
+    // dH = dY W_down, then dG, dU
+    p.ntn = (s->h + MMA_N - 1) / MMA_N;
+    p.g_save = g_save;
+    p.u_save = u_save;
+    p.out0 = dG;
+    p.out1 = dU;
+    r = launch_bwd<DGRAD_DH>(dy_k, dy_k, wd_mn, wd_mn, p, row_tiles * p.ntn, stream);
+    if (r != MOE_OK) return r;
+    // dX = dG W_gate + dU W_up
+    p.ntn = (s->d + MMA_N - 1) / MMA_N;
+    p.out0 = dx_disp;
+    p.out1 = nullptr;
+    r = launch_bwd<DGRAD_DX>(dg_k, du_k, wg_mn, wu_mn, p, row_tiles * p.ntn, stream);
+    if (r != MOE_OK) return r;
+    // dW_down = dY^T H
+    p.mtn = (s->d + BM - 1) / BM;
+    p.ntn = (s->h + MMA_N - 1) / MMA_N;
+    p.fout0 = dw_down;
+    p.fout1 = nullptr;
+    r = launch_bwd<WGRAD_DOWN>(dy_mn, dy_mn, h_mn, h_mn, p, s->N * p.mtn * p.ntn, stream);
+    if (r != MOE_OK) return r;
+    // dW_gate = dG^T X, dW_up = dU^T X
+    p.mtn = wg_mt;
+    p.ntn = (s->d + MMA_N - 1) / MMA_N;
+    p.fout0 = dw_gate;
+    p.fout1 = dw_up;
+    return launch_bwd<WGRAD_GATEUP>(dg_mn, du_mn, x_mn, x_mn, p, s->N * p.mtn * p.ntn, stream);
+}

@@ -175,6 +175,39 @@ moe_status moe_expert_ffn(const moe_shape *s, const moe_bf16 *x_disp, const int3
                           moe_bf16 *g_save, moe_bf16 *u_save, moe_bf16 *y_disp, void *ws,
                           size_t ws_bytes, cudaStream_t stream);
 
+/* Bytes of workspace moe_expert_ffn_backward needs: the device status word
+ * and the two [R, h] bf16 intermediates dG and dU. */
+size_t moe_expert_ffn_backward_workspace_bytes(const moe_shape *s);
+
+/*
+ * moe_expert_ffn_backward -- step B2: data and weight gradients of the
+ * grouped SwiGLU experts.  Section 05, 5.7 (expert backward and the weight-
+ * gradient GEMM run over each expert's valid rows, given the real offsets,
+ * and skip the unwritten tail); Figure 14 (Linear 1 -> SwiGLU -> Linear 2).
+ * For each expert e over its rows, with X = x_disp, G = g_save, U = u_save,
+ * H = h_act and dY = dy_disp (the combine backward's output):
+ *   dH = dY W_down[e];  dU = dH * silu(G);  dG = dH * U * silu'(G)
+ *   dx_disp = bf16(dG W_gate[e] + dU W_up[e])
+ *   dw_down[e] = dY^T H;  dw_gate[e] = dG^T X;  dw_up[e] = dU^T X   (fp32)
+ * with fp32 accumulation on tcgen05 tensor cores; dG and dU are rounded to
+ * bf16 (they are operands of the next products) and kept in the workspace.
+ *   x_disp, dy_disp [R, d] bf16; g_save, u_save, h_act [R, h] bf16 (from
+ *   moe_expert_ffn with saving on); counts and offsets from moe_route;
+ *   weights as in moe_expert_ffn; dx_disp out [R, d] bf16 (valid rows only);
+ *   dw_gate, dw_up out [N, h, d] fp32; dw_down out [N, d, h] fp32 (every
+ *   element written: experts without rows get zeros);
+ *   ws, ws_bytes: moe_expert_ffn_backward_workspace_bytes(s) bytes, 256-byte
+ *   aligned.  d and h must be multiples of 64 (MOE_ERR_UNSUPPORTED otherwise).
+ */
+moe_status moe_expert_ffn_backward(const moe_shape *s, const moe_bf16 *x_disp,
+                                   const int32_t *expert_count, const int32_t *expert_offset,
+                                   const moe_bf16 *w_gate, const moe_bf16 *w_up,
+                                   const moe_bf16 *w_down, const moe_bf16 *g_save,
+                                   const moe_bf16 *u_save, const moe_bf16 *h_act,
+                                   const moe_bf16 *dy_disp, moe_bf16 *dx_disp, float *dw_gate,
+                                   float *dw_up, float *dw_down, void *ws, size_t ws_bytes,
+                                   cudaStream_t stream);
+
 /*
  * moe_combine -- step C.  Section 05 Table 8 "Combine forward GET", 5.6 and
  * Figure 15: y[t] = bf16( sum over k ascending of topk_gate[t, k] *
