@@ -72,6 +72,24 @@ def algorithmic(cfg, A):
     return out
 
 
+def gemm_traffic(workload):
+    """DRAM bytes per moe_expert_ffn call from the committed ncu summary, or
+    None if that summary is for another workload or the kernel source has
+    changed since the counters were taken."""
+    import hashlib
+    src = os.path.join(ROOT, "combine_expert_gemm_gb300", "csrc", "grouped_gemm.cu")
+    prof = os.path.join(ROOT, "profiles", f"grouped_gemm_{workload}_ncu.md")
+    if not os.path.exists(prof):
+        return None
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    for line in open(prof):
+        f = line.split()
+        # "traffic-per-call: <bytes> bytes; grouped_gemm.cu sha256 <hex>"
+        if len(f) >= 6 and f[0] == "traffic-per-call:" and f[5] == sha:
+            return int(f[1])
+    return None
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle-reason samples while the timed region runs."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -249,10 +267,7 @@ def run_ours(args, cfg, rank, world):
     dc_bytes = alg["dispatch_bytes"] + alg["combine_bytes"]
     dc_s = (ph_ms["dispatch"] + ph_ms["combine"]) / 1e3
     achieved_tf = alg["gemm_flop"] / gemm_s / 1e12
-    traffic = None
-    tp = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tp):
-        traffic = json.load(open(tp)).get(cfg.name, {}).get("grouped_gemm_bytes_per_call")
+    traffic = gemm_traffic(cfg.name)
     sm_clock = clocks["sm_mhz"] if clocks else pk["sm_max_mhz"]
     fp32_peak = 2.0 * 128 * 152 * pk["sm_max_mhz"] * 1e6 / 1e12
     line = {
