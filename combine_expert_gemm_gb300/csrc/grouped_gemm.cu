@@ -8,13 +8,14 @@
 // touches only the valid prefix); "Section 04: Distributed Data Parallel", 4.1
 // (bias-free SwiGLU expert).
 //
-// One persistent kernel per GEMM, one CTA per SM, 6 warps:
+// One persistent kernel per GEMM, one CTA per SM, 10 warps:
 //   warp 0     TMA producer: 128x64 A tiles and 256x64 B tiles into a
 //              4-stage shared-memory ring (128-byte swizzle);
 //   warp 1     tcgen05.mma issuer (one thread; M=128, N=256, K=16 steps) into a
 //              double-buffered fp32 accumulator in tensor memory (2 x 256 of
 //              the SM's 512 columns), and owner of the TMEM allocation;
-//   warps 2-5  epilogue: tcgen05.ld of the accumulator, then either SwiGLU
+//   warps 2-9  epilogue (two warps per TMEM lane quadrant, each taking half
+//              of the columns): tcgen05.ld of the accumulator, then either SwiGLU
 //              (F1: columns 0-127 are the gate rows, 128-255 the up rows of the
 //              same 128 hidden units) or a plain bf16 store (F2).
 // Work list: every CTA derives, from expert_count in device memory, the tiles
@@ -38,7 +39,8 @@ constexpr int B_BYTES = MMA_N * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int ACC_COLS = 256;
 constexpr int TMEM_COLS = 512;
-constexpr int kThreads = 192;
+constexpr int kEpiThreads = 256;  // 8 epilogue warps
+constexpr int kThreads = 64 + kEpiThreads;
 
 enum { EPI_SWIGLU = 0, EPI_STORE = 1 };
 
@@ -99,7 +101,7 @@ grouped_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&bars->tfull[b]), 1);
-            mbar_init(smem_u32(&bars->tempty[b]), 128);
+            mbar_init(smem_u32(&bars->tempty[b]), kEpiThreads);
         }
         bars->abort = 0;
         fence_mbar_init();
@@ -205,6 +207,7 @@ grouped_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
     } else {
         // epilogue: warp w reads TMEM lanes 32 * (w % 4) .. + 31 = tile rows
         const int quad = warp & 3;
+        const int half = (warp - 2) >> 2;  // which half of the columns
         const int row_in_tile = quad * 32 + lane;
         int acc = 0;
         uint32_t acc_phase = 0;
@@ -217,7 +220,7 @@ grouped_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
             tc_fence_after();
             const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * ACC_COLS;
             if (EPI == EPI_SWIGLU) {
-                for (int c = 0; c < BN_OUT; c += 16) {
+                for (int c = half * (BN_OUT / 2); c < (half + 1) * (BN_OUT / 2); c += 16) {
                     uint32_t gr[16], ur[16];
                     tmem_ld16(tbase + c, gr);
                     tmem_ld16(tbase + BN_OUT + c, ur);
@@ -233,8 +236,8 @@ grouped_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
                             const float g1 = __uint_as_float(gr[2 * i + 1]);
                             const float u0 = __uint_as_float(ur[2 * i]);
                             const float u1 = __uint_as_float(ur[2 * i + 1]);
-                            const float h0 = g0 / (1.0f + __expf(-g0)) * u0;
-                            const float h1 = g1 / (1.0f + __expf(-g1)) * u1;
+                            const float h0 = __fdividef(g0, 1.0f + __expf(-g0)) * u0;
+                            const float h1 = __fdividef(g1, 1.0f + __expf(-g1)) * u1;
                             hp[i] = pack_bf16x2(h0, h1);
                             gp[i] = pack_bf16x2(g0, g1);
                             up[i] = pack_bf16x2(u0, u1);
@@ -253,7 +256,7 @@ grouped_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
                     }
                 }
             } else {
-                for (int c = 0; c < BN_OUT; c += 32) {
+                for (int c = half * (BN_OUT / 2); c < (half + 1) * (BN_OUT / 2); c += 32) {
                     uint32_t r0[16], r1[16];
                     tmem_ld16(tbase + c, r0);
                     tmem_ld16(tbase + c + 16, r1);

@@ -15,7 +15,7 @@
 //
 // Same engine as the forward kernel (persistent, one CTA per SM, TMA 4-stage
 // ring with 128-byte swizzle, one thread issuing tcgen05.mma M=128 N=256 into
-// a double-buffered TMEM accumulator, four epilogue warps).  The backward
+// a double-buffered TMEM accumulator, eight epilogue warps).  The backward
 // operands that are transposed relative to their storage (weights in dgrad,
 // activations in wgrad) are read MN-major: a TMA box of 64 M/N elements x 64 K
 // rows lands as 64 swizzled 128-byte rows and the MMA descriptor walks it with
@@ -51,7 +51,7 @@ enum { DGRAD_DH = 0, DGRAD_DX = 1, WGRAD_DOWN = 2, WGRAD_GATEUP = 3 };
 template <int MODE>
 struct ModeT {
     static constexpr bool kgroup = MODE >= WGRAD_DOWN;  // K = rows of an expert
-    static constexpr int threads = 192;
+    static constexpr int threads = 64 + 256;  // producer, MMA, 8 epilogue warps
 };
 
 // Shared-memory descriptor of an MN-major operand tile (128-byte swizzle):
@@ -82,8 +82,13 @@ struct alignas(8) Bars {
     int abort;
 };
 
+constexpr int kEpiThreads = 256;                      // 8 epilogue warps
+constexpr int STG_LD = 17;                           // padded fp32 row of a staging block
+constexpr int STG_BYTES = 8 * 32 * STG_LD * 4;       // one 32 x 16 block per epilogue warp
+
 constexpr size_t smem_bytes(int N) {
-    return 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(Bars) + sizeof(int32_t) * (N + 1) + 16;
+    return 1024 + (size_t)STAGES * STAGE_BYTES + STG_BYTES + sizeof(Bars) +
+           sizeof(int32_t) * (N + 1) + 16;
 }
 
 struct Params {
@@ -135,7 +140,8 @@ grouped_gemm_bwd(const __grid_constant__ CUtensorMap tm_a0, const __grid_constan
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    Bars *bars = reinterpret_cast<Bars *>(smem + (size_t)STAGES * STAGE_BYTES);
+    float *stage_out = reinterpret_cast<float *>(smem + (size_t)STAGES * STAGE_BYTES);
+    Bars *bars = reinterpret_cast<Bars *>(smem + (size_t)STAGES * STAGE_BYTES + STG_BYTES);
     int32_t *tile_start = reinterpret_cast<int32_t *>(bars + 1);
     volatile int *abort = &bars->abort;
     int *status = p.status;
@@ -149,7 +155,7 @@ grouped_gemm_bwd(const __grid_constant__ CUtensorMap tm_a0, const __grid_constan
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&bars->tfull[b]), 1);
-            mbar_init(smem_u32(&bars->tempty[b]), 128);
+            mbar_init(smem_u32(&bars->tempty[b]), kEpiThreads);
         }
         bars->abort = 0;
         fence_mbar_init();
@@ -300,6 +306,7 @@ grouped_gemm_bwd(const __grid_constant__ CUtensorMap tm_a0, const __grid_constan
     } else {
         // --------------------------------------------------------- epilogue
         const int quad = warp & 3;
+        const int half = (warp - 2) >> 2;  // which 128 of the 256 columns
         const int rit = quad * 32 + lane;  // row of the tile = TMEM lane
         int acc = 0;
         uint32_t acc_phase = 0;
@@ -313,7 +320,29 @@ grouped_gemm_bwd(const __grid_constant__ CUtensorMap tm_a0, const __grid_constan
                 const bool row_ok = rit < cnt - t.m * BM;
                 const int64_t row = (int64_t)off + t.m * BM + rit;
                 const int width = MODE == DGRAD_DH ? p.h : p.d;
-                for (int c = 0; c < MMA_N; c += 16) {
+                // saved G, U of this thread's row, prefetched three 16-column
+                // chunks ahead of their use (they come from DRAM)
+                constexpr int PF = 3, NCH = MMA_N / 32;  // 16-column chunks of this half
+                uint4 gq[PF + 1][2], uq[PF + 1][2];
+                auto fetch = [&](int ch, int slot) {
+                    const int col = t.n * MMA_N + half * (MMA_N / 2) + ch * 16;
+                    if (MODE == DGRAD_DH && row_ok && col < width) {
+                        const uint4 *gp = reinterpret_cast<const uint4 *>(p.g_save + row * p.h + col);
+                        const uint4 *up = reinterpret_cast<const uint4 *>(p.u_save + row * p.h + col);
+                        gq[slot][0] = __ldcs(gp);
+                        gq[slot][1] = __ldcs(gp + 1);
+                        uq[slot][0] = __ldcs(up);
+                        uq[slot][1] = __ldcs(up + 1);
+                    }
+                };
+                if (MODE == DGRAD_DH) {
+#pragma unroll
+                    for (int ch = 0; ch < PF; ++ch) fetch(ch, ch);
+                }
+#pragma unroll
+                for (int ch = 0; ch < NCH; ++ch) {
+                    const int c = half * (MMA_N / 2) + ch * 16;
+                    if (MODE == DGRAD_DH && ch + PF < NCH) fetch(ch + PF, (ch + PF) % (PF + 1));
                     uint32_t r[16];
                     tmem_ld16(tbase + c, r);
                     tmem_ld_wait();
@@ -321,11 +350,9 @@ grouped_gemm_bwd(const __grid_constant__ CUtensorMap tm_a0, const __grid_constan
                     const int col = t.n * MMA_N + c;
                     if (!row_ok || col >= width) continue;
                     if (MODE == DGRAD_DH) {
-                        const uint4 *gp = reinterpret_cast<const uint4 *>(p.g_save + row * p.h + col);
-                        const uint4 *up = reinterpret_cast<const uint4 *>(p.u_save + row * p.h + col);
-                        const uint4 gv[2] = {gp[0], gp[1]}, uv[2] = {up[0], up[1]};
-                        const uint32_t *gw = reinterpret_cast<const uint32_t *>(gv);
-                        const uint32_t *uw = reinterpret_cast<const uint32_t *>(uv);
+                        const int slot = ch % (PF + 1);
+                        const uint32_t *gw = reinterpret_cast<const uint32_t *>(gq[slot]);
+                        const uint32_t *uw = reinterpret_cast<const uint32_t *>(uq[slot]);
                         uint32_t dg[8], du[8];
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
@@ -335,7 +362,7 @@ grouped_gemm_bwd(const __grid_constant__ CUtensorMap tm_a0, const __grid_constan
                                 const float z = hf ? bf16_hi(gw[i]) : bf16_lo(gw[i]);
                                 const float u = hf ? bf16_hi(uw[i]) : bf16_lo(uw[i]);
                                 const float dh = __uint_as_float(r[2 * i + hf]);
-                                const float sg = 1.0f / (1.0f + __expf(-z));
+                                const float sg = __fdividef(1.0f, 1.0f + __expf(-z));
                                 ru[hf] = dh * (z * sg);
                                 rg[hf] = dh * u * sg * (1.0f + z * (1.0f - sg));
                             }
@@ -360,28 +387,36 @@ grouped_gemm_bwd(const __grid_constant__ CUtensorMap tm_a0, const __grid_constan
                     }
                 }
             } else {
-                // weight gradient, fp32; an expert without rows gets zeros
+                // weight gradient, fp32; an expert without rows gets zeros.
+                // Each 32 x 16 block goes through a padded shared-memory block so
+                // that a store instruction writes 64-byte row segments.
                 const bool up = MODE == WGRAD_GATEUP && t.m >= mt_half;
-                const int mrow = (up ? t.m - mt_half : t.m) * BM + rit;
+                const int mbase = (up ? t.m - mt_half : t.m) * BM + quad * 32;
                 const int mlim = MODE == WGRAD_DOWN ? p.d : p.h;
                 const int width = MODE == WGRAD_DOWN ? p.h : p.d;
                 float *out = (up ? p.fout1 : p.fout0) + (int64_t)t.e * mlim * width;
-                for (int c = 0; c < MMA_N; c += 16) {
-                    uint32_t r[16];
-                    tmem_ld16(tbase + c, r);
+                float *blk = stage_out + (warp - 2) * 32 * STG_LD;
+                for (int c = half * (MMA_N / 2); c < (half + 1) * (MMA_N / 2); c += 16) {
+                    uint32_t r0[16];
+                    tmem_ld16(tbase + c, r0);
                     tmem_ld_wait();
-                    reg_fence(r);
-                    const int col = t.n * MMA_N + c;
-                    if (mrow >= mlim || col >= width) continue;
-                    float4 *dst = reinterpret_cast<float4 *>(out + (int64_t)mrow * width + col);
+                    reg_fence(r0);
+                    const int col0 = t.n * MMA_N + c;
+                    if (col0 >= width) continue;  // warp-uniform
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        float4 v = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
-                                               __uint_as_float(r[4 * i + 2]),
-                                               __uint_as_float(r[4 * i + 3]));
-                        if (cnt == 0) v = make_float4(0.f, 0.f, 0.f, 0.f);
-                        dst[i] = v;
+                    for (int i = 0; i < 16; ++i)
+                        blk[lane * STG_LD + i] = cnt ? __uint_as_float(r0[i]) : 0.0f;
+                    __syncwarp();
+                    const int cq = (lane & 3) * 4;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int rr = j * 8 + (lane >> 2);
+                        const float *src = blk + rr * STG_LD + cq;
+                        const float4 v = make_float4(src[0], src[1], src[2], src[3]);
+                        if (mbase + rr < mlim)
+                            *reinterpret_cast<float4 *>(out + (int64_t)(mbase + rr) * width + col0 + cq) = v;
                     }
+                    __syncwarp();
                 }
             }
             tc_fence_before();
