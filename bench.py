@@ -240,20 +240,34 @@ def run_ours(args, cfg, rank, world):
     x_host = torch.from_numpy(x_np.view(np.int16)).view(torch.bfloat16).pin_memory()
     y_host = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16).pin_memory()
     x_dev_e2e = torch.empty_like(x)
-    e2e_steps = max(3, min(args.steps, 50))
-    for _ in range(2):
+    h2d = x.numel() * 2
+    d2h = cfg.T * cfg.d * 2
+    if cfg.backward:
+        dy_host = torch.from_numpy(synth.gen_dy(rcfg).view(np.int16)).view(torch.bfloat16).pin_memory()
+        dy_dev_e2e = torch.empty_like(dy)
+        dx_host = torch.empty((cfg.T, cfg.d), dtype=torch.float32).pin_memory()
+        h2d += dy.numel() * 2
+        d2h += cfg.T * cfg.d * 4
+
+    def e2e_step():
         x_dev_e2e.copy_(x_host, non_blocking=True)
         moe.layer_forward(buf, x_dev_e2e, wr, bias, wg, wu, wd)
         y_host.copy_(buf.y, non_blocking=True)
+        if cfg.backward:
+            dy_dev_e2e.copy_(dy_host, non_blocking=True)
+            moe.layer_backward(buf, bwd, dy_dev_e2e, wg, wu, wd)
+            dx_host.copy_(bwd.dx, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 50))
+    for _ in range(2):
+        e2e_step()
     torch.cuda.synchronize()
     e_ms = []
     for _ in range(e2e_steps):
         flush.zero_()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        x_dev_e2e.copy_(x_host, non_blocking=True)
-        moe.layer_forward(buf, x_dev_e2e, wr, bias, wg, wu, wd)
-        y_host.copy_(buf.y, non_blocking=True)
+        e2e_step()
         e1.record(stream)
         e1.synchronize()
         e_ms.append(e0.elapsed_time(e1))
@@ -303,8 +317,10 @@ def run_ours(args, cfg, rank, world):
         "phase_ms": ph_ms,
         "gpu_launches": launches_per_step * args.steps,
         "e2e": {"value": world * cfg.T / (e2e_ms / 1e3), "unit": "tokens/s",
-                "h2d_bytes_per_step": int(x.numel() * 2), "d2h_bytes_per_step": int(cfg.T * cfg.d * 2),
-                "ms_per_step": e2e_ms, "api": "combine_expert_gemm_gb300.layer_forward"},
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "ms_per_step": e2e_ms,
+                "api": "combine_expert_gemm_gb300.layer_forward" +
+                       (" + layer_backward" if cfg.backward else "")},
         "clocks": clocks,
         "wall_s_timed_region": t_wall,
     }
@@ -348,7 +364,10 @@ def _oracle_sample(cfg, tokens):
     if cfg.backward:
         dyd, dg = oracle.combine_bwd(inp["dy"][:tokens], out["y_disp"], out["route_row"],
                                      out["topk_gate"])
-        oracle.dispatch_bwd(dyd, out["route_row"], tokens)
+        dxd, dwg, dwu, dwd = oracle.expert_ffn_bwd(out["expert_count"], out["expert_offset"],
+                                                   out["x_disp"], out["g_save"], out["u_save"],
+                                                   out["h_act"], dyd, wg, wu, wd)
+        oracle.dispatch_bwd(dxd, out["route_row"], tokens)
     return time.perf_counter() - t0
 
 

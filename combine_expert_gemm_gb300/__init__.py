@@ -61,6 +61,7 @@ _SIG = {
     "moe_read_device_error": ([_P, ctypes.POINTER(ctypes.c_int32), _P], ctypes.c_int),
     "moe_expert_ffn_backward_workspace_bytes": ([_SP], _SZ),
     "moe_expert_ffn_backward": ([_SP] + [_P] * 14 + [_P, _SZ, _P], ctypes.c_int),
+    "moe_selftest_wait_timeout": ([_P, ctypes.c_uint64, _P], ctypes.c_int),
 }
 for _name, (_args, _res) in _SIG.items():
     _f = getattr(_lib, _name)
@@ -181,6 +182,12 @@ def expert_ffn_backward(shape, x_disp, expert_count, expert_offset, w_gate, w_up
         _ptr(dx_disp, _bf16, "dx_disp"), _ptr(dw_gate, _f32, "dw_gate"), _ptr(dw_up, _f32, "dw_up"),
         _ptr(dw_down, _f32, "dw_down"), _ptr(ws, None, "ws"), ws.numel() * ws.element_size(),
         _stream(stream)), "moe_expert_ffn_backward")
+
+
+def selftest_wait_timeout(ws, limit_ns, stream=None):
+    """Runs the bounded-wait failure path once (see include/moe.h)."""
+    _check(_lib.moe_selftest_wait_timeout(_ptr(ws, None, "ws"), int(limit_ns), _stream(stream)),
+           "moe_selftest_wait_timeout")
 
 
 def read_device_error(ws, stream=None):

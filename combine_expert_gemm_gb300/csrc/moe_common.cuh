@@ -145,16 +145,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Waits for the phase with the given parity to complete.  Returns false (and
 // records MOE_ERR_DEVICE_TIMEOUT in *status) if it has not completed within
-// kWaitLimitNs, or at once if *abort is already set.
+// limit_ns (kWaitLimitNs by default), or at once if *abort is already set.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int *status,
-                                          volatile int *abort) {
+                                          volatile int *abort,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     unsigned long long t0 = global_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 63u) == 0) {
             if (*abort) return false;
-            if (global_ns() - t0 > kWaitLimitNs) {
+            if (global_ns() - t0 > limit_ns) {
                 atomicExch(status, (int)MOE_ERR_DEVICE_TIMEOUT);
                 *abort = 1;
                 return false;

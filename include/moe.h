@@ -247,6 +247,18 @@ moe_status moe_dispatch_backward(const moe_shape *s, const moe_bf16 *dx_disp,
  */
 moe_status moe_read_device_error(void *ws, int32_t *code_out, cudaStream_t stream);
 
+/*
+ * moe_selftest_wait_timeout -- diagnostic for the device-side failure path.
+ * Launches one small kernel that waits, with the same bounded mbarrier wait
+ * every kernel of this library uses, on a barrier that nothing completes.
+ * After limit_ns (1 ns .. 100 ms) the wait gives up and records
+ * MOE_ERR_DEVICE_TIMEOUT in the workspace's status word, exactly as a stuck
+ * GEMM pipeline would, and the kernel returns; the CUDA context stays usable.
+ * ws: any 256-byte aligned workspace of this library.  No counterpart in the
+ * report (it describes no failure handling for this path).
+ */
+moe_status moe_selftest_wait_timeout(void *ws, uint64_t limit_ns, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

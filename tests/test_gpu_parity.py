@@ -218,3 +218,36 @@ def test_full_size_sampled(moe, name):
     assert_close_bf16(got_y, y_tok, f"{name} y sample")
     if name == "fine_zipf":
         assert (r["expert_demand"] > cfg.cap).any()
+
+
+def test_bounded_wait_records_timeout_and_context_survives(moe):
+    """A wait that nothing completes gives up after its limit, records
+    MOE_ERR_DEVICE_TIMEOUT in the status word (read once, then cleared), and
+    the context keeps working: a layer forward afterwards is still correct."""
+    ws = torch.zeros(256, dtype=torch.uint8, device=DEV)
+    moe.selftest_wait_timeout(ws, 2_000_000)  # 2 ms
+    assert moe.read_device_error(ws) == 6
+    assert moe.read_device_error(ws) == 0
+    cfg = SMALL["tiny"]
+    x, wr, bias, wg, wu, wd = _inputs(cfg)
+    ref = oracle.layer_forward(x, wr, bias, wg, wu, wd, cfg.K, cfg.cap)
+    buf = _run_chain(moe, cfg, x, wr, bias, wg, wu, wd)
+    _check_route(buf, ref)
+    assert_close_bf16(bits(buf.y), ref["y"], "y after a timeout")
+
+
+def test_forward_enqueues_without_host_sync(moe):
+    """No torch-visible synchronisation in the binding: the whole forward runs
+    under torch's sync debug mode set to raise."""
+    cfg = SMALL["ragged"]
+    x, wr, bias, wg, wu, wd = _inputs(cfg)
+    s = _shape(moe, cfg)
+    buf = moe.LayerBuffers(s, DEV)
+    args = [bf(x), f32(wr), None, bf(wg), bf(wu), bf(wd)]
+    torch.cuda.synchronize()
+    torch.cuda.set_sync_debug_mode("error")
+    try:
+        moe.layer_forward(buf, *args)
+    finally:
+        torch.cuda.set_sync_debug_mode("default")
+    torch.cuda.synchronize()
