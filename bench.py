@@ -77,15 +77,18 @@ def gemm_traffic(workload):
     None if that summary is for another workload or the kernel source has
     changed since the counters were taken."""
     import hashlib
-    src = os.path.join(ROOT, "combine_expert_gemm_gb300", "csrc", "grouped_gemm.cu")
+    csrc = os.path.join(ROOT, "combine_expert_gemm_gb300", "csrc")
     prof = os.path.join(ROOT, "profiles", f"grouped_gemm_{workload}_ncu.md")
     if not os.path.exists(prof):
         return None
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    h = hashlib.sha256()
+    for name in ("grouped_gemm.cu", "moe_common.cuh"):
+        h.update(open(os.path.join(csrc, name), "rb").read())
+    sha = h.hexdigest()
     for line in open(prof):
         f = line.split()
-        # "traffic-per-call: <bytes> bytes; grouped_gemm.cu sha256 <hex>"
-        if len(f) >= 6 and f[0] == "traffic-per-call:" and f[5] == sha:
+        # "traffic-per-call: <bytes> bytes; kernel source sha256 <hex>"
+        if len(f) >= 7 and f[0] == "traffic-per-call:" and f[6] == sha:
             return int(f[1])
     return None
 
