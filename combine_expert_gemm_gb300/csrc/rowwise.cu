@@ -59,7 +59,10 @@ dispatch_rows(int T, int nchunk, int K, const uint4 *__restrict__ x,
     }
 }
 
-__global__ void __launch_bounds__(kThreads)
+// MAXK (8 or 16) bounds the route count K: the K route rows of a chunk are
+// all in flight at once, and a smaller bound keeps more warps resident.
+template <int MAXK>
+__global__ void __launch_bounds__(kThreads, MAXK <= 8 ? 4 : 2)
 combine_rows(int T, int nchunk, int K, const uint4 *__restrict__ y_disp,
              const int32_t *__restrict__ route_row, const float *__restrict__ gate,
              uint4 *__restrict__ y) {
@@ -68,34 +71,39 @@ combine_rows(int T, int nchunk, int K, const uint4 *__restrict__ y_disp,
     if (t >= T) return;
     const int32_t my_row = lane < K ? route_row[(int64_t)t * K + lane] : -1;
     const float my_g = lane < K ? gate[(int64_t)t * K + lane] : 0.0f;
-    // the chunk loop is warp-uniform so that every shuffle has all 32 lanes
+    int32_t rows[MAXK];
+    float gs[MAXK];
+#pragma unroll
+    for (int k = 0; k < MAXK; ++k) {
+        rows[k] = __shfl_sync(0xFFFFFFFFu, my_row, k);
+        gs[k] = __shfl_sync(0xFFFFFFFFu, my_g, k);
+    }
+    // the chunk loop is warp-uniform; no shuffles inside
     for (int c0 = 0; c0 < nchunk; c0 += 32) {
         const int c = c0 + lane;
-        const bool on = c < nchunk;
-        uint4 v[kMaxK];
+        if (c >= nchunk) break;
+        uint4 v[MAXK];
 #pragma unroll
-        for (int k = 0; k < kMaxK; ++k) {
-            if (k >= K) break;
-            const int32_t r = __shfl_sync(0xFFFFFFFFu, my_row, k);
-            if (r >= 0 && on) v[k] = __ldcs(y_disp + (int64_t)r * nchunk + c);
-        }
+        for (int k = 0; k < MAXK; ++k)
+            if (k < K && rows[k] >= 0) v[k] = __ldcs(y_disp + (int64_t)rows[k] * nchunk + c);
         float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 #pragma unroll
-        for (int k = 0; k < kMaxK; ++k) {
-            if (k >= K) break;
-            const int32_t r = __shfl_sync(0xFFFFFFFFu, my_row, k);
-            const float g = __shfl_sync(0xFFFFFFFFu, my_g, k);
-            if (r < 0 || !on) continue;
+        for (int k = 0; k < MAXK; ++k) {
+            if (k >= K || rows[k] < 0) continue;
             float f[8];
             unpack8(v[k], f);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = __fmaf_rn(g, f[i], acc[i]);
+            for (int i = 0; i < 8; ++i) acc[i] = __fmaf_rn(gs[k], f[i], acc[i]);
         }
-        if (on) y[(int64_t)t * nchunk + c] = pack8(acc);
+        y[(int64_t)t * nchunk + c] = pack8(acc);
     }
 }
 
-__global__ void __launch_bounds__(kThreads)
+// Chunk-outer: for each 16-byte chunk of the token row, all K route rows are
+// read at once; the K partial dot products for dgate stay in registers and
+// are reduced across the warp at the end.
+template <int MAXK>
+__global__ void __launch_bounds__(kThreads, MAXK <= 8 ? 3 : 2)
 combine_bwd_rows(int T, int nchunk, int K, const uint4 *__restrict__ dy,
                  const uint4 *__restrict__ y_disp, const int32_t *__restrict__ route_row,
                  const float *__restrict__ gate, uint4 *__restrict__ dy_disp,
@@ -105,60 +113,70 @@ combine_bwd_rows(int T, int nchunk, int K, const uint4 *__restrict__ dy,
     if (t >= T) return;
     const int32_t my_row = lane < K ? route_row[(int64_t)t * K + lane] : -1;
     const float my_g = lane < K ? gate[(int64_t)t * K + lane] : 0.0f;
+    int32_t rows[MAXK];
+    float gs[MAXK], part[MAXK];
+#pragma unroll
+    for (int k = 0; k < MAXK; ++k) {
+        rows[k] = __shfl_sync(0xFFFFFFFFu, my_row, k);
+        gs[k] = __shfl_sync(0xFFFFFFFFu, my_g, k);
+        part[k] = 0.0f;
+    }
     const uint4 *src = dy + (int64_t)t * nchunk;
-    for (int k = 0; k < K; ++k) {
-        const int32_t r = __shfl_sync(0xFFFFFFFFu, my_row, k);
-        const float g = __shfl_sync(0xFFFFFFFFu, my_g, k);
-        float part = 0.0f;
-        if (r >= 0) {
-            for (int c = lane; c < nchunk; c += 32) {
-                float f[8], o[8];
-                unpack8(src[c], f);
-                unpack8(__ldcs(y_disp + (int64_t)r * nchunk + c), o);
-                float p[8];
+    for (int c = lane; c < nchunk; c += 32) {
+        float f[8];
+        unpack8(src[c], f);
+        uint4 v[MAXK];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    p[i] = __fmul_rn(g, f[i]);
-                    part = __fmaf_rn(f[i], o[i], part);
-                }
-                dy_disp[(int64_t)r * nchunk + c] = pack8(p);
+        for (int k = 0; k < MAXK; ++k)
+            if (k < K && rows[k] >= 0) v[k] = __ldcs(y_disp + (int64_t)rows[k] * nchunk + c);
+#pragma unroll
+        for (int k = 0; k < MAXK; ++k) {
+            if (k >= K || rows[k] < 0) continue;
+            float o[8], pr[8];
+            unpack8(v[k], o);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                pr[i] = __fmul_rn(gs[k], f[i]);
+                part[k] = __fmaf_rn(f[i], o[i], part[k]);
             }
+            dy_disp[(int64_t)rows[k] * nchunk + c] = pack8(pr);
         }
+    }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xFFFFFFFFu, part, off);
-        if (lane == 0) dgate[(int64_t)t * K + k] = r >= 0 ? part : 0.0f;
+    for (int k = 0; k < MAXK; ++k) {
+        if (k >= K) break;
+        float v = part[k];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
+        if (lane == 0) dgate[(int64_t)t * K + k] = rows[k] >= 0 ? v : 0.0f;
     }
 }
 
-__global__ void __launch_bounds__(kThreads)
+template <int MAXK>
+__global__ void __launch_bounds__(kThreads, MAXK <= 8 ? 4 : 2)
 dispatch_bwd_rows(int T, int nchunk, int K, const uint4 *__restrict__ dx_disp,
                   const int32_t *__restrict__ route_row, float4 *__restrict__ dx) {
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
     if (t >= T) return;
     const int32_t my_row = lane < K ? route_row[(int64_t)t * K + lane] : -1;
-    for (int c0 = 0; c0 < nchunk; c0 += 32) {  // warp-uniform (shuffles inside)
-        const int c = c0 + lane;
-        const bool on = c < nchunk;
-        uint4 v[kMaxK];
+    int32_t rows[MAXK];
 #pragma unroll
-        for (int k = 0; k < kMaxK; ++k) {
-            if (k >= K) break;
-            const int32_t r = __shfl_sync(0xFFFFFFFFu, my_row, k);
-            if (r >= 0 && on) v[k] = __ldcs(dx_disp + (int64_t)r * nchunk + c);
-        }
+    for (int k = 0; k < MAXK; ++k) rows[k] = __shfl_sync(0xFFFFFFFFu, my_row, k);
+    for (int c = lane; c < nchunk; c += 32) {
+        uint4 v[MAXK];
+#pragma unroll
+        for (int k = 0; k < MAXK; ++k)
+            if (k < K && rows[k] >= 0) v[k] = __ldcs(dx_disp + (int64_t)rows[k] * nchunk + c);
         float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 #pragma unroll
-        for (int k = 0; k < kMaxK; ++k) {
-            if (k >= K) break;
-            const int32_t r = __shfl_sync(0xFFFFFFFFu, my_row, k);
-            if (r < 0 || !on) continue;
+        for (int k = 0; k < MAXK; ++k) {
+            if (k >= K || rows[k] < 0) continue;
             float f[8];
             unpack8(v[k], f);
 #pragma unroll
             for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], f[i]);
         }
-        if (!on) continue;
         float4 *o = dx + ((int64_t)t * nchunk + c) * 2;
         __stcs(o, make_float4(acc[0], acc[1], acc[2], acc[3]));
         __stcs(o + 1, make_float4(acc[4], acc[5], acc[6], acc[7]));
@@ -194,9 +212,10 @@ MOE_API moe_status moe_combine(const moe_shape *s, const moe_bf16 *y_disp,
     if (!route_row || !topk_gate || !y || (s->cap > 0 && !y_disp)) return MOE_ERR_INVALID_ARG;
     if (!aligned16(y_disp) || !aligned16(route_row) || !aligned16(topk_gate) || !aligned16(y))
         return MOE_ERR_ALIGNMENT;
-    combine_rows<<<grid_for(s->T), kThreads, 0, stream>>>(
-        s->T, s->d / 8, s->K, reinterpret_cast<const uint4 *>(y_disp), route_row, topk_gate,
-        reinterpret_cast<uint4 *>(y));
+    auto *kern = s->K <= 8 ? combine_rows<8> : combine_rows<16>;
+    kern<<<grid_for(s->T), kThreads, 0, stream>>>(s->T, s->d / 8, s->K,
+                                                 reinterpret_cast<const uint4 *>(y_disp),
+                                                 route_row, topk_gate, reinterpret_cast<uint4 *>(y));
     return launch_status();
 }
 
@@ -212,7 +231,8 @@ MOE_API moe_status moe_combine_backward(const moe_shape *s, const moe_bf16 *dy,
     if (!aligned16(dy) || !aligned16(y_disp) || !aligned16(route_row) || !aligned16(topk_gate) ||
         !aligned16(dy_disp) || !aligned16(dgate))
         return MOE_ERR_ALIGNMENT;
-    combine_bwd_rows<<<grid_for(s->T), kThreads, 0, stream>>>(
+    auto *kern = s->K <= 8 ? combine_bwd_rows<8> : combine_bwd_rows<16>;
+    kern<<<grid_for(s->T), kThreads, 0, stream>>>(
         s->T, s->d / 8, s->K, reinterpret_cast<const uint4 *>(dy),
         reinterpret_cast<const uint4 *>(y_disp), route_row, topk_gate,
         reinterpret_cast<uint4 *>(dy_disp), dgate);
@@ -227,8 +247,9 @@ MOE_API moe_status moe_dispatch_backward(const moe_shape *s, const moe_bf16 *dx_
     if (s->T == 0) return MOE_OK;
     if (!route_row || !dx || (s->cap > 0 && !dx_disp)) return MOE_ERR_INVALID_ARG;
     if (!aligned16(dx_disp) || !aligned16(route_row) || !aligned16(dx)) return MOE_ERR_ALIGNMENT;
-    dispatch_bwd_rows<<<grid_for(s->T), kThreads, 0, stream>>>(
-        s->T, s->d / 8, s->K, reinterpret_cast<const uint4 *>(dx_disp), route_row,
-        reinterpret_cast<float4 *>(dx));
+    auto *kern = s->K <= 8 ? dispatch_bwd_rows<8> : dispatch_bwd_rows<16>;
+    kern<<<grid_for(s->T), kThreads, 0, stream>>>(s->T, s->d / 8, s->K,
+                                                 reinterpret_cast<const uint4 *>(dx_disp), route_row,
+                                                 reinterpret_cast<float4 *>(dx));
     return launch_status();
 }
