@@ -8,18 +8,20 @@
 // touches only the valid prefix); "Section 04: Distributed Data Parallel", 4.1
 // (bias-free SwiGLU expert).
 //
-// One persistent kernel per GEMM, one CTA per SM, 10 warps:
-//   warp 0     TMA producer: 128x64 A tiles and 256x64 B tiles into a
-//              4-stage shared-memory ring (128-byte swizzle);
-//   warp 1     tcgen05.mma issuer (one thread; M=128, N=256, K=16 steps) into a
-//              double-buffered fp32 accumulator in tensor memory (2 x 256 of
-//              the SM's 512 columns), and owner of the TMEM allocation;
-//   warps 2-9  epilogue (two warps per TMEM lane quadrant, each taking half
-//              of the columns): tcgen05.ld of the accumulator, then either SwiGLU
-//              (F1: columns 0-127 are the gate rows, 128-255 the up rows of the
-//              same 128 hidden units) or a plain bf16 store (F2).
+// One persistent kernel per GEMM; CTAs run in clusters of two, one CTA per SM,
+// 10 warps each:
+//   warp 0     TMA producer (both CTAs): this CTA's 128 rows of A and half of B
+//              per 64-wide k-block, 32 KB, into a 6-stage ring (128-byte swizzle);
+//   warp 1     in the pair's leader, one thread issues tcgen05.mma.cta_group::2
+//              (M = 256 across the pair, N = 256, K = 16) into a double-buffered
+//              fp32 accumulator in tensor memory (2 x 256 of 512 columns), and
+//              the warp owns the pair-wide TMEM allocation;
+//   warps 2-9  epilogue (two warps per TMEM lane quadrant, each half of the
+//              columns): tcgen05.ld of this CTA's 128 accumulator rows, then
+//              SwiGLU (F1: columns 0-127 are the gate rows, loaded by the leader,
+//              128-255 the up rows, loaded by the peer) or a bf16 store (F2).
 // Work list: every CTA derives, from expert_count in device memory, the tiles
-// of every expert (ceil(count/128) row tiles x output-column tiles) and walks
+// of every expert (ceil(count/256) row tiles x output-column tiles) and walks
 // them round-robin.  Rows past an expert's count (the next expert's rows or
 // the tail) enter the MMA but are never stored; column tiles past the output
 // width are never stored either.  No host round trip, no per-expert launch.
@@ -33,10 +35,7 @@ namespace {
 constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int MMA_N = 256;
-constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_BYTES = MMA_N * BK * 2;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int ACC_COLS = 256;
 constexpr int TMEM_COLS = 512;
 constexpr int kEpiThreads = 256;  // 8 epilogue warps
@@ -44,74 +43,156 @@ constexpr int kThreads = 64 + kEpiThreads;
 
 enum { EPI_SWIGLU = 0, EPI_STORE = 1 };
 
-struct alignas(8) Bars {
-    uint64_t full[STAGES];
-    uint64_t empty[STAGES];
+struct TileMap {
+    int e, m, n;
+};
+
+// Epilogue of one accumulator tile for one warp: its 32 TMEM lanes (rows) and
+// one half of the columns.  F1: columns [0, 128) hold G and [128, 256) hold U of
+// the same hidden units; H = silu(G) * U.  F2: a plain bf16 store.
+template <int EPI>
+__device__ __forceinline__ void epilogue_tile(uint32_t tbase, int half, bool row_ok, int64_t row,
+                                              int n, int Nout, uint16_t *__restrict__ out,
+                                              uint16_t *__restrict__ g_save,
+                                              uint16_t *__restrict__ u_save) {
+    constexpr int BN_OUT = EPI == EPI_SWIGLU ? MMA_N / 2 : MMA_N;
+    if (EPI == EPI_SWIGLU) {
+        for (int c = half * (BN_OUT / 2); c < (half + 1) * (BN_OUT / 2); c += 16) {
+            uint32_t gr[16], ur[16];
+            tmem_ld16(tbase + c, gr);
+            tmem_ld16(tbase + BN_OUT + c, ur);
+            tmem_ld_wait();
+            reg_fence(gr);
+            reg_fence(ur);
+            const int col = n * BN_OUT + c;
+            if (row_ok && col < Nout) {
+                uint32_t hp[8], gp[8], up[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float g0 = __uint_as_float(gr[2 * i]);
+                    const float g1 = __uint_as_float(gr[2 * i + 1]);
+                    const float u0 = __uint_as_float(ur[2 * i]);
+                    const float u1 = __uint_as_float(ur[2 * i + 1]);
+                    const float h0 = __fdividef(g0, 1.0f + __expf(-g0)) * u0;
+                    const float h1 = __fdividef(g1, 1.0f + __expf(-g1)) * u1;
+                    hp[i] = pack_bf16x2(h0, h1);
+                    gp[i] = pack_bf16x2(g0, g1);
+                    up[i] = pack_bf16x2(u0, u1);
+                }
+                uint4 *dst = reinterpret_cast<uint4 *>(out + row * Nout + col);
+                dst[0] = make_uint4(hp[0], hp[1], hp[2], hp[3]);
+                dst[1] = make_uint4(hp[4], hp[5], hp[6], hp[7]);
+                if (g_save) {
+                    uint4 *gd = reinterpret_cast<uint4 *>(g_save + row * Nout + col);
+                    gd[0] = make_uint4(gp[0], gp[1], gp[2], gp[3]);
+                    gd[1] = make_uint4(gp[4], gp[5], gp[6], gp[7]);
+                    uint4 *ud = reinterpret_cast<uint4 *>(u_save + row * Nout + col);
+                    ud[0] = make_uint4(up[0], up[1], up[2], up[3]);
+                    ud[1] = make_uint4(up[4], up[5], up[6], up[7]);
+                }
+            }
+        }
+    } else {
+        for (int c = half * (BN_OUT / 2); c < (half + 1) * (BN_OUT / 2); c += 32) {
+            uint32_t r0[16], r1[16];
+            tmem_ld16(tbase + c, r0);
+            tmem_ld16(tbase + c + 16, r1);
+            tmem_ld_wait();
+            reg_fence(r0);
+            reg_fence(r1);
+            const int col = n * BN_OUT + c;
+            if (row_ok && col < Nout) {
+                uint32_t p[16];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    p[i] = pack_bf16x2(__uint_as_float(r0[2 * i]),
+                                       __uint_as_float(r0[2 * i + 1]));
+                    p[8 + i] = pack_bf16x2(__uint_as_float(r1[2 * i]),
+                                           __uint_as_float(r1[2 * i + 1]));
+                }
+                uint4 *dst = reinterpret_cast<uint4 *>(out + row * Nout + col);
+                dst[0] = make_uint4(p[0], p[1], p[2], p[3]);
+                dst[1] = make_uint4(p[4], p[5], p[6], p[7]);
+                if (col + 16 < Nout) {
+                    dst[2] = make_uint4(p[8], p[9], p[10], p[11]);
+                    dst[3] = make_uint4(p[12], p[13], p[14], p[15]);
+                }
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------ CTA-pair kernel
+//
+// Two CTAs of a cluster compute one 256-row x 256-column tile with
+// tcgen05.mma.cta_group::2 (M = 256, N = 256): each CTA holds its own 128 rows
+// of A and one half of B (F1: the gate rows in the leader, the up rows in the
+// peer; F2: columns 0-127 / 128-255), so each SM stages and reads 32 KB per
+// k-block instead of 48 KB, and six stages fit.  The leader (rank 0) issues the
+// MMAs; both CTAs' TMA loads complete on the leader's full barrier; the
+// leader's commits release a stage, and announce an accumulator, in both CTAs
+// at once; both CTAs' epilogue warps release the accumulator on the leader's
+// barrier.  Each CTA's TMEM holds its own 128 accumulator rows.
+constexpr int P_STAGES = 6;
+constexpr int P_B_BYTES = (MMA_N / 2) * BK * 2;   // this CTA's half of B
+constexpr int P_STAGE_BYTES = A_BYTES + P_B_BYTES;  // 32 KB
+constexpr int P_EPI_WARPS = kEpiThreads / 32;
+
+struct alignas(8) PairBars {
+    uint64_t full[P_STAGES];
+    uint64_t empty[P_STAGES];
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint32_t tmem_base;
     int abort;
 };
 
-constexpr size_t smem_bytes(int N) {
-    return 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(Bars) + sizeof(int32_t) * (N + 1) + 16;
-}
-
-struct TileMap {
-    int e, m, n;
-};
-
-// Expert owning tile g: the last e with tile_start[e] <= g.
-__device__ __forceinline__ TileMap map_tile(int g, int N, const int32_t *tile_start,
-                                            const int32_t *count) {
-    int lo = 0, hi = N - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (tile_start[mid] <= g) lo = mid;
-        else hi = mid - 1;
-    }
-    const int mt = (count[lo] + BM - 1) / BM;
-    const int local = g - tile_start[lo];
-    return TileMap{lo, local % mt, local / mt};
+constexpr size_t smem_bytes_pair(int N) {
+    return 1024 + (size_t)P_STAGES * P_STAGE_BYTES + sizeof(PairBars) + sizeof(int32_t) * (N + 1) +
+           16;
 }
 
 template <int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
-grouped_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b0,
-             const __grid_constant__ CUtensorMap tm_b1, int N, int Kdim, int Nout,
-             const int32_t *__restrict__ count, const int32_t *__restrict__ offset,
-             uint16_t *__restrict__ out, uint16_t *__restrict__ g_save,
-             uint16_t *__restrict__ u_save, int *status) {
+grouped_gemm_pair(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b0,
+                  const __grid_constant__ CUtensorMap tm_b1, int N, int Kdim, int Nout,
+                  const int32_t *__restrict__ count, const int32_t *__restrict__ offset,
+                  uint16_t *__restrict__ out, uint16_t *__restrict__ g_save,
+                  uint16_t *__restrict__ u_save, int *status) {
     constexpr int BN_OUT = EPI == EPI_SWIGLU ? MMA_N / 2 : MMA_N;
+    constexpr int PM = 2 * BM;  // rows per pair tile
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    Bars *bars = reinterpret_cast<Bars *>(smem + (size_t)STAGES * STAGE_BYTES);
+    PairBars *bars = reinterpret_cast<PairBars *>(smem + (size_t)P_STAGES * P_STAGE_BYTES);
     int32_t *tile_start = reinterpret_cast<int32_t *>(bars + 1);
     volatile int *abort = &bars->abort;
+    const uint32_t rank = cluster_rank();
+    const bool leader = rank == 0;
+    const int unit0 = (int)blockIdx.x / 2, units = (int)gridDim.x / 2;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ntn = (Nout + BN_OUT - 1) / BN_OUT;
     const int nk = (Kdim + BK - 1) / BK;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < P_STAGES; ++s) {
             mbar_init(smem_u32(&bars->full[s]), 1);
             mbar_init(smem_u32(&bars->empty[s]), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&bars->tfull[b]), 1);
-            mbar_init(smem_u32(&bars->tempty[b]), kEpiThreads);
+            mbar_init(smem_u32(&bars->tempty[b]), 2 * P_EPI_WARPS);
         }
         bars->abort = 0;
         fence_mbar_init();
     }
     if (warp == 0) {
-        // tile_start[e] = tiles of experts < e (warp-wide scan, 32 experts per step)
+        // tile_start[e] = pair tiles of experts < e
         int carry = 0;
         for (int base = 0; base < N; base += 32) {
             const int e = base + lane;
-            const int v = e < N ? ((count[e] + BM - 1) / BM) * ntn : 0;
+            const int v = e < N ? ((count[e] + PM - 1) / PM) * ntn : 0;
             int incl = v;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
@@ -123,62 +204,83 @@ grouped_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
         }
         if (lane == 0) tile_start[N] = carry;
     }
-    if (warp == 1) tmem_alloc(smem_u32(&bars->tmem_base), TMEM_COLS);
+    if (warp == 1) tmem_alloc_pair(smem_u32(&bars->tmem_base), TMEM_COLS);
     tc_fence_before();
     __syncthreads();
+    cluster_sync_all();  // barriers of both CTAs exist before any remote arrival
     tc_fence_after();
     const uint32_t tmem_base = bars->tmem_base;
     const int total = tile_start[N];
 
+    auto map_pair = [&](int g) {
+        int lo = 0, hi = N - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (tile_start[mid] <= g) lo = mid;
+            else hi = mid - 1;
+        }
+        const int mt = (count[lo] + PM - 1) / PM;
+        const int local = g - tile_start[lo];
+        return TileMap{lo, local % mt, local / mt};
+    };
+
     if (warp == 0) {
+        // -------------------------------------------- TMA producer (both CTAs)
         if (lane == 0) {
             tma_prefetch_desc(&tm_a);
-            tma_prefetch_desc(&tm_b0);
-            if (EPI == EPI_SWIGLU) tma_prefetch_desc(&tm_b1);
+            tma_prefetch_desc(rank && EPI == EPI_SWIGLU ? &tm_b1 : &tm_b0);
             int stage = 0;
             uint32_t phase = 0;
+            int issued = 0;
             bool ok = true;
-            for (int g = blockIdx.x; g < total && ok; g += gridDim.x) {
-                const TileMap t = map_tile(g, N, tile_start, count);
-                const int a_row = offset[t.e] + t.m * BM;
-                const int b_row = t.e * Nout + t.n * BN_OUT;
+            for (int g = unit0; g < total && ok; g += units) {
+                const TileMap t = map_pair(g);
+                const int a_row = offset[t.e] + t.m * PM + (int)rank * BM;
+                const int b_row = EPI == EPI_SWIGLU ? t.e * Nout + t.n * BN_OUT
+                                                    : t.e * Nout + t.n * BN_OUT + (int)rank * (MMA_N / 2);
+                const CUtensorMap *mb = rank && EPI == EPI_SWIGLU ? &tm_b1 : &tm_b0;
                 for (int kb = 0; kb < nk; ++kb) {
                     if (!mbar_wait(smem_u32(&bars->empty[stage]), phase ^ 1, status, abort)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t full = smem_u32(&bars->full[stage]);
-                    const uint32_t sa = smem_u32(smem + (size_t)stage * STAGE_BYTES);
+                    const uint32_t own_full = smem_u32(&bars->full[stage]);
+                    const uint32_t full = cluster_map(own_full, 0);
+                    const uint32_t sa = smem_u32(smem + (size_t)stage * P_STAGE_BYTES);
                     const uint32_t sb = sa + A_BYTES;
-                    mbar_arrive_expect_tx(full, STAGE_BYTES);
-                    tma_load_2d(sa, &tm_a, full, kb * BK, a_row);
-                    if (EPI == EPI_SWIGLU) {
-                        tma_load_2d(sb, &tm_b0, full, kb * BK, b_row);
-                        tma_load_2d(sb + B_BYTES / 2, &tm_b1, full, kb * BK, b_row);
-                    } else {
-                        tma_load_2d(sb, &tm_b0, full, kb * BK, b_row);
-                    }
-                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                    if (leader) mbar_arrive_expect_tx(own_full, 2 * P_STAGE_BYTES);
+                    tma_load_2d_pair(sa, &tm_a, full, kb * BK, a_row);
+                    tma_load_2d_pair(sb, mb, full, kb * BK, b_row);
+                    ++issued;
+                    if (++stage == P_STAGES) { stage = 0; phase ^= 1; }
                 }
             }
-            if (!ok) {
-                // let copies already issued land before the CTA leaves
-                for (int s = 0; s < STAGES; ++s) {
+            if (!ok && leader) {
+                // the leader's full barriers count both CTAs' copies: let the ones
+                // already issued land before the pair leaves
+                for (int s = 0; s < P_STAGES; ++s) {
                     volatile int no_abort = 0;
                     mbar_wait(smem_u32(&bars->full[s]), phase ^ (s >= stage ? 1 : 0), status,
                               &no_abort);
                 }
             }
+            // every release of every stage (the leader's commits) has arrived
+            for (int s = 0; s < P_STAGES; ++s) {
+                const int uses = issued / P_STAGES + (s < issued % P_STAGES ? 1 : 0);
+                if (uses > 0)
+                    mbar_wait(smem_u32(&bars->empty[s]), (uint32_t)((uses - 1) & 1), status, abort);
+            }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(BM, MMA_N);
+        // --------------------------------------------- MMA issuer (leader only)
+        if (lane == 0 && leader) {
+            constexpr uint32_t idesc = idesc_bf16_f32(PM, MMA_N);
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
-            for (int g = blockIdx.x; g < total && ok; g += gridDim.x) {
+            for (int g = unit0; g < total && ok; g += units) {
                 if (!mbar_wait(smem_u32(&bars->tempty[acc]), acc_phase ^ 1, status, abort)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * ACC_COLS);
@@ -188,135 +290,87 @@ grouped_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = smem_u32(smem + (size_t)stage * STAGE_BYTES);
+                    const uint32_t sa = smem_u32(smem + (size_t)stage * P_STAGE_BYTES);
                     const uint32_t sb = sa + A_BYTES;
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
-                        tc_mma_bf16(d_tmem, sw128_kmajor_desc(sa + kk * 32),
-                                    sw128_kmajor_desc(sb + kk * 32), idesc,
-                                    (kb | kk) != 0 ? 1u : 0u);
+                        tc_mma_bf16_pair(d_tmem, sw128_kmajor_desc(sa + kk * 32),
+                                         sw128_kmajor_desc(sb + kk * 32), idesc,
+                                         (kb | kk) != 0 ? 1u : 0u);
                     }
-                    tc_commit(smem_u32(&bars->empty[stage]));
-                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                    tc_commit_pair(smem_u32(&bars->empty[stage]));
+                    if (++stage == P_STAGES) { stage = 0; phase ^= 1; }
                 }
                 if (!ok) break;
-                tc_commit(smem_u32(&bars->tfull[acc]));
+                tc_commit_pair(smem_u32(&bars->tfull[acc]));
                 if (++acc == 2) { acc = 0; acc_phase ^= 1; }
             }
         }
     } else {
-        // epilogue: warp w reads TMEM lanes 32 * (w % 4) .. + 31 = tile rows
+        // ----------------------------------------------- epilogue (both CTAs)
         const int quad = warp & 3;
-        const int half = (warp - 2) >> 2;  // which half of the columns
-        const int row_in_tile = quad * 32 + lane;
+        const int half = (warp - 2) >> 2;
+        const int row_in_tile = (int)rank * BM + quad * 32 + lane;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int g = blockIdx.x; g < total; g += gridDim.x) {
-            const TileMap t = map_tile(g, N, tile_start, count);
-            const int rows_valid = count[t.e] - t.m * BM;
+        for (int g = unit0; g < total; g += units) {
+            const TileMap t = map_pair(g);
+            const int rows_valid = count[t.e] - t.m * PM;
             const bool row_ok = row_in_tile < rows_valid;
-            const int64_t row = (int64_t)offset[t.e] + t.m * BM + row_in_tile;
+            const int64_t row = (int64_t)offset[t.e] + t.m * PM + row_in_tile;
             if (!mbar_wait(smem_u32(&bars->tfull[acc]), acc_phase, status, abort)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * ACC_COLS;
-            if (EPI == EPI_SWIGLU) {
-                for (int c = half * (BN_OUT / 2); c < (half + 1) * (BN_OUT / 2); c += 16) {
-                    uint32_t gr[16], ur[16];
-                    tmem_ld16(tbase + c, gr);
-                    tmem_ld16(tbase + BN_OUT + c, ur);
-                    tmem_ld_wait();
-                    reg_fence(gr);
-                    reg_fence(ur);
-                    const int col = t.n * BN_OUT + c;
-                    if (row_ok && col < Nout) {
-                        uint32_t hp[8], gp[8], up[8];
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const float g0 = __uint_as_float(gr[2 * i]);
-                            const float g1 = __uint_as_float(gr[2 * i + 1]);
-                            const float u0 = __uint_as_float(ur[2 * i]);
-                            const float u1 = __uint_as_float(ur[2 * i + 1]);
-                            const float h0 = __fdividef(g0, 1.0f + __expf(-g0)) * u0;
-                            const float h1 = __fdividef(g1, 1.0f + __expf(-g1)) * u1;
-                            hp[i] = pack_bf16x2(h0, h1);
-                            gp[i] = pack_bf16x2(g0, g1);
-                            up[i] = pack_bf16x2(u0, u1);
-                        }
-                        uint4 *dst = reinterpret_cast<uint4 *>(out + row * Nout + col);
-                        dst[0] = make_uint4(hp[0], hp[1], hp[2], hp[3]);
-                        dst[1] = make_uint4(hp[4], hp[5], hp[6], hp[7]);
-                        if (g_save) {
-                            uint4 *gd = reinterpret_cast<uint4 *>(g_save + row * Nout + col);
-                            gd[0] = make_uint4(gp[0], gp[1], gp[2], gp[3]);
-                            gd[1] = make_uint4(gp[4], gp[5], gp[6], gp[7]);
-                            uint4 *ud = reinterpret_cast<uint4 *>(u_save + row * Nout + col);
-                            ud[0] = make_uint4(up[0], up[1], up[2], up[3]);
-                            ud[1] = make_uint4(up[4], up[5], up[6], up[7]);
-                        }
-                    }
-                }
-            } else {
-                for (int c = half * (BN_OUT / 2); c < (half + 1) * (BN_OUT / 2); c += 32) {
-                    uint32_t r0[16], r1[16];
-                    tmem_ld16(tbase + c, r0);
-                    tmem_ld16(tbase + c + 16, r1);
-                    tmem_ld_wait();
-                    reg_fence(r0);
-                    reg_fence(r1);
-                    const int col = t.n * BN_OUT + c;
-                    if (row_ok && col < Nout) {
-                        uint32_t p[16];
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            p[i] = pack_bf16x2(__uint_as_float(r0[2 * i]),
-                                               __uint_as_float(r0[2 * i + 1]));
-                            p[8 + i] = pack_bf16x2(__uint_as_float(r1[2 * i]),
-                                                   __uint_as_float(r1[2 * i + 1]));
-                        }
-                        uint4 *dst = reinterpret_cast<uint4 *>(out + row * Nout + col);
-                        dst[0] = make_uint4(p[0], p[1], p[2], p[3]);
-                        dst[1] = make_uint4(p[4], p[5], p[6], p[7]);
-                        if (col + 16 < Nout) {
-                            dst[2] = make_uint4(p[8], p[9], p[10], p[11]);
-                            dst[3] = make_uint4(p[12], p[13], p[14], p[15]);
-                        }
-                    }
-                }
-            }
+            epilogue_tile<EPI>(tbase, half, row_ok, row, t.n, Nout, out, g_save, u_save);
             tc_fence_before();
-            mbar_arrive(smem_u32(&bars->tempty[acc]));
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(cluster_map(smem_u32(&bars->tempty[acc]), 0));
             if (++acc == 2) { acc = 0; acc_phase ^= 1; }
         }
     }
 
     tc_fence_before();
     __syncthreads();
+    cluster_sync_all();  // both CTAs are done with every barrier and every MMA
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, TMEM_COLS);
+        tmem_dealloc_pair(tmem_base, TMEM_COLS);
     }
 }
 
 // ---------------------------------------------------------------- host side --
 
 template <int EPI>
-moe_status launch_gemm(const CUtensorMap &a, const CUtensorMap &b0, const CUtensorMap &b1, int N,
-                       int Kdim, int Nout, int max_row_tiles, const int32_t *count,
-                       const int32_t *offset, uint16_t *out, uint16_t *gs, uint16_t *us,
-                       int *status, cudaStream_t st) {
-    const size_t smem = smem_bytes(N);
+moe_status launch_gemm_pair(const CUtensorMap &a, const CUtensorMap &b0, const CUtensorMap &b1,
+                            int N, int Kdim, int Nout, int max_row_tiles, const int32_t *count,
+                            const int32_t *offset, uint16_t *out, uint16_t *gs, uint16_t *us,
+                            int *status, cudaStream_t st) {
+    const size_t smem = smem_bytes_pair(N);
     static size_t configured = 0;
     if (smem > configured) {
-        if (cudaFuncSetAttribute(grouped_gemm<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem_bytes(kMaxN)) != cudaSuccess)
+        if (cudaFuncSetAttribute(grouped_gemm_pair<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem_bytes_pair(kMaxN)) != cudaSuccess)
             return MOE_ERR_CUDA;
-        configured = smem_bytes(kMaxN);
+        configured = smem_bytes_pair(kMaxN);
     }
     constexpr int BN_OUT = EPI == EPI_SWIGLU ? MMA_N / 2 : MMA_N;
-    const int64_t max_tiles = (int64_t)max_row_tiles * ((Nout + BN_OUT - 1) / BN_OUT);
-    const int grid = (int)std::min<int64_t>(num_sms(), std::max<int64_t>(max_tiles, 1));
-    grouped_gemm<EPI><<<grid, kThreads, smem, st>>>(a, b0, b1, N, Kdim, Nout, count, offset, out,
-                                                    gs, us, status);
+    const int64_t max_units = (int64_t)((max_row_tiles + 1) / 2 + N) * ((Nout + BN_OUT - 1) / BN_OUT);
+    const int64_t pairs = std::min<int64_t>(num_sms() / 2, std::max<int64_t>(max_units, 1));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(2 * pairs));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, grouped_gemm_pair<EPI>, a, b0, b1, N, Kdim, Nout, count, offset,
+                           out, gs, us, status) != cudaSuccess)
+        return MOE_ERR_CUDA;
     return launch_status();
 }
 
@@ -324,6 +378,7 @@ moe_status launch_gemm(const CUtensorMap &a, const CUtensorMap &b0, const CUtens
 }  // namespace moe
 
 using namespace moe;
+
 
 MOE_API size_t moe_expert_ffn_workspace_bytes(const moe_shape *s) {
     if (check_shape(s) != MOE_OK) return 0;
@@ -353,14 +408,14 @@ MOE_API moe_status moe_expert_ffn(const moe_shape *s, const moe_bf16 *x_disp,
     if (!make_map(&ma, x_disp, s->d, R, BM) || !make_map(&mg, w_gate, s->d, (uint64_t)s->N * s->h, 128) ||
         !make_map(&mu, w_up, s->d, (uint64_t)s->N * s->h, 128) ||
         !make_map(&mh, h_act, s->h, R, BM) ||
-        !make_map(&md, w_down, s->h, (uint64_t)s->N * s->d, MMA_N))
+        !make_map(&md, w_down, s->h, (uint64_t)s->N * s->d, MMA_N / 2))
         return MOE_ERR_CUDA;
     int *status = static_cast<int *>(ws);
     const int64_t rows = std::min<int64_t>(R, (int64_t)s->T * s->K);
     const int max_row_tiles = (int)((rows + BM - 1) / BM + s->N);
-    r = launch_gemm<EPI_SWIGLU>(ma, mg, mu, s->N, s->d, s->h, max_row_tiles, expert_count,
-                                expert_offset, h_act, g_save, u_save, status, stream);
+    r = launch_gemm_pair<EPI_SWIGLU>(ma, mg, mu, s->N, s->d, s->h, max_row_tiles, expert_count,
+                                     expert_offset, h_act, g_save, u_save, status, stream);
     if (r != MOE_OK) return r;
-    return launch_gemm<EPI_STORE>(mh, md, md, s->N, s->h, s->d, max_row_tiles, expert_count,
-                                  expert_offset, y_disp, nullptr, nullptr, status, stream);
+    return launch_gemm_pair<EPI_STORE>(mh, md, md, s->N, s->h, s->d, max_row_tiles, expert_count,
+                                       expert_offset, y_disp, nullptr, nullptr, status, stream);
 }
