@@ -13,9 +13,13 @@
 //   dW_down = dY^T H                          (wgrad, K = rows of e)
 //   dW_gate = dG^T X,  dW_up = dU^T X         (wgrad, K = rows of e)
 //
-// Same engine as the forward kernel (persistent, one CTA per SM, TMA 4-stage
-// ring with 128-byte swizzle, one thread issuing tcgen05.mma M=128 N=256 into
-// a double-buffered TMEM accumulator, eight epilogue warps).  The backward
+// dgrad (dH, dX) runs on CTA pairs like the forward kernel: M = 256 rows per
+// tcgen05.mma.cta_group::2, each CTA holding its own 128 rows of A and half of
+// B, 32 KB per k-block in a 6-stage ring.  wgrad runs one CTA per SM (a 4-stage
+// ring of 48 KB k-blocks, tcgen05.mma M = 128, N = 256), because its ragged
+// last k-block has to be repaired in the shared memory of the CTA that reads
+// it.  Both: persistent, 128-byte swizzle, one thread issuing MMAs into a
+// double-buffered TMEM accumulator, eight epilogue warps.  The backward
 // operands that are transposed relative to their storage (weights in dgrad,
 // activations in wgrad) are read MN-major: a TMA box of 64 M/N elements x 64 K
 // rows lands as 64 swizzled 128-byte rows and the MMA descriptor walks it with
@@ -50,7 +54,6 @@ enum { DGRAD_DH = 0, DGRAD_DX = 1, WGRAD_DOWN = 2, WGRAD_GATEUP = 3 };
 
 template <int MODE>
 struct ModeT {
-    static constexpr bool kgroup = MODE >= WGRAD_DOWN;  // K = rows of an expert
     static constexpr int threads = 64 + 256;  // producer, MMA, 8 epilogue warps
 };
 
@@ -86,9 +89,8 @@ constexpr int kEpiThreads = 256;                      // 8 epilogue warps
 constexpr int STG_LD = 17;                           // padded fp32 row of a staging block
 constexpr int STG_BYTES = 8 * 32 * STG_LD * 4;       // one 32 x 16 block per epilogue warp
 
-constexpr size_t smem_bytes(int N) {
-    return 1024 + (size_t)STAGES * STAGE_BYTES + STG_BYTES + sizeof(Bars) +
-           sizeof(int32_t) * (N + 1) + 16;
+constexpr size_t smem_bytes() {
+    return 1024 + (size_t)STAGES * STAGE_BYTES + STG_BYTES + sizeof(Bars) + 16;
 }
 
 struct Params {
@@ -106,22 +108,11 @@ struct Tile {
     int e, m, n;
 };
 
-__device__ __forceinline__ Tile map_tile(int MODE_kgroup, int g, const Params &p,
-                                         const int32_t *tile_start) {
-    if (MODE_kgroup) {
-        const int tpe = p.mtn * p.ntn;
-        const int e = g / tpe, l = g % tpe;
-        return Tile{e, l % p.mtn, l / p.mtn};
-    }
-    int lo = 0, hi = p.N - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (tile_start[mid] <= g) lo = mid;
-        else hi = mid - 1;
-    }
-    const int mt = (p.count[lo] + BM - 1) / BM;
-    const int l = g - tile_start[lo];
-    return Tile{lo, l % mt, l / mt};
+// wgrad work unit g: expert-major, output-row tiles fastest.
+__device__ __forceinline__ Tile map_wgrad_tile(int g, const Params &p) {
+    const int tpe = p.mtn * p.ntn;
+    const int e = g / tpe, l = g % tpe;
+    return Tile{e, l % p.mtn, l / p.mtn};
 }
 
 template <int MODE>
@@ -131,18 +122,93 @@ __device__ __forceinline__ int k_blocks(const Params &p, int cnt) {
     return (cnt + BK - 1) / BK;
 }
 
+// Epilogue of a dgrad tile for one warp: 32 rows (TMEM lanes) and one half of
+// the 256 columns.  DGRAD_DH: dU = dH * silu(G), dG = dH * U * silu'(G) from the
+// saved G, U (prefetched three 16-column chunks ahead, they come from DRAM);
+// DGRAD_DX: a bf16 store of dX.
+template <int MODE>
+__device__ __forceinline__ void dgrad_epilogue(uint32_t tbase, int half, bool row_ok, int64_t row,
+                                               int n, const Params &p) {
+    const int width = MODE == DGRAD_DH ? p.h : p.d;
+    // saved G, U of this thread's row, prefetched three 16-column
+    // chunks ahead of their use (they come from DRAM)
+    constexpr int PF = 3, NCH = MMA_N / 32;  // 16-column chunks of this half
+    uint4 gq[PF + 1][2], uq[PF + 1][2];
+    auto fetch = [&](int ch, int slot) {
+        const int col = n * MMA_N + half * (MMA_N / 2) + ch * 16;
+        if (MODE == DGRAD_DH && row_ok && col < width) {
+            const uint4 *gp = reinterpret_cast<const uint4 *>(p.g_save + row * p.h + col);
+            const uint4 *up = reinterpret_cast<const uint4 *>(p.u_save + row * p.h + col);
+            gq[slot][0] = __ldcs(gp);
+            gq[slot][1] = __ldcs(gp + 1);
+            uq[slot][0] = __ldcs(up);
+            uq[slot][1] = __ldcs(up + 1);
+        }
+    };
+    if (MODE == DGRAD_DH) {
+#pragma unroll
+        for (int ch = 0; ch < PF; ++ch) fetch(ch, ch);
+    }
+#pragma unroll
+    for (int ch = 0; ch < NCH; ++ch) {
+        const int c = half * (MMA_N / 2) + ch * 16;
+        if (MODE == DGRAD_DH && ch + PF < NCH) fetch(ch + PF, (ch + PF) % (PF + 1));
+        uint32_t r[16];
+        tmem_ld16(tbase + c, r);
+        tmem_ld_wait();
+        reg_fence(r);
+        const int col = n * MMA_N + c;
+        if (!row_ok || col >= width) continue;
+        if (MODE == DGRAD_DH) {
+            const int slot = ch % (PF + 1);
+            const uint32_t *gw = reinterpret_cast<const uint32_t *>(gq[slot]);
+            const uint32_t *uw = reinterpret_cast<const uint32_t *>(uq[slot]);
+            uint32_t dg[8], du[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                float rg[2], ru[2];
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    const float z = hf ? bf16_hi(gw[i]) : bf16_lo(gw[i]);
+                    const float u = hf ? bf16_hi(uw[i]) : bf16_lo(uw[i]);
+                    const float dh = __uint_as_float(r[2 * i + hf]);
+                    const float sg = __fdividef(1.0f, 1.0f + __expf(-z));
+                    ru[hf] = dh * (z * sg);
+                    rg[hf] = dh * u * sg * (1.0f + z * (1.0f - sg));
+                }
+                dg[i] = pack_bf16x2(rg[0], rg[1]);
+                du[i] = pack_bf16x2(ru[0], ru[1]);
+            }
+            uint4 *gd = reinterpret_cast<uint4 *>(p.out0 + row * p.h + col);
+            uint4 *ud = reinterpret_cast<uint4 *>(p.out1 + row * p.h + col);
+            gd[0] = make_uint4(dg[0], dg[1], dg[2], dg[3]);
+            gd[1] = make_uint4(dg[4], dg[5], dg[6], dg[7]);
+            ud[0] = make_uint4(du[0], du[1], du[2], du[3]);
+            ud[1] = make_uint4(du[4], du[5], du[6], du[7]);
+        } else {
+            uint32_t pk[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]),
+                                    __uint_as_float(r[2 * i + 1]));
+            uint4 *dst = reinterpret_cast<uint4 *>(p.out0 + row * p.d + col);
+            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        }
+    }
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(ModeT<MODE>::threads, 1)
-grouped_gemm_bwd(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
+grouped_wgrad(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
                  const __grid_constant__ CUtensorMap tm_b0, const __grid_constant__ CUtensorMap tm_b1,
                  const Params p) {
-    constexpr bool KG = ModeT<MODE>::kgroup;
+    static_assert(MODE == WGRAD_DOWN || MODE == WGRAD_GATEUP, "wgrad only");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     float *stage_out = reinterpret_cast<float *>(smem + (size_t)STAGES * STAGE_BYTES);
     Bars *bars = reinterpret_cast<Bars *>(smem + (size_t)STAGES * STAGE_BYTES + STG_BYTES);
-    int32_t *tile_start = reinterpret_cast<int32_t *>(bars + 1);
     volatile int *abort = &bars->abort;
     int *status = p.status;
 
@@ -160,29 +226,12 @@ grouped_gemm_bwd(const __grid_constant__ CUtensorMap tm_a0, const __grid_constan
         bars->abort = 0;
         fence_mbar_init();
     }
-    if (!KG && warp == 0) {
-        int carry = 0;
-        for (int base = 0; base < p.N; base += 32) {
-            const int e = base + lane;
-            const int v = e < p.N ? ((p.count[e] + BM - 1) / BM) * p.ntn : 0;
-            int incl = v;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const int u = __shfl_up_sync(0xFFFFFFFFu, incl, off);
-                if (lane >= off) incl += u;
-            }
-            if (e < p.N) tile_start[e] = carry + incl - v;
-            carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
-        }
-        if (lane == 0) tile_start[p.N] = carry;
-    }
     if (warp == 1) tmem_alloc(smem_u32(&bars->tmem_base), TMEM_COLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = bars->tmem_base;
-    const int total = KG ? p.N * p.mtn * p.ntn : tile_start[p.N];
-    const int hb = p.h / BK;  // k-blocks per half of the dX reduction
+    const int total = p.N * p.mtn * p.ntn;
     const int mt_half = (p.h + BM - 1) / BM;
 
     if (warp == 0) {
@@ -194,7 +243,7 @@ grouped_gemm_bwd(const __grid_constant__ CUtensorMap tm_a0, const __grid_constan
             uint32_t phase = 0;
             bool ok = true;
             for (int g = blockIdx.x; g < total && ok; g += gridDim.x) {
-                const Tile t = map_tile(KG, g, p, tile_start);
+                const Tile t = map_wgrad_tile(g, p);
                 const int cnt = p.count[t.e], off = p.offset[t.e];
                 const int nk = k_blocks<MODE>(p, cnt);
                 for (int kb = 0; kb < nk; ++kb) {
@@ -207,26 +256,13 @@ grouped_gemm_bwd(const __grid_constant__ CUtensorMap tm_a0, const __grid_constan
                     const uint32_t sb = sa + A_BYTES;
                     mbar_arrive_expect_tx(full, STAGE_BYTES);
                     const int ncol = t.n * MMA_N;
-                    if (MODE == DGRAD_DH) {
-                        tma_load_2d(sa, &tm_a0, full, kb * BK, off + t.m * BM);
-                        for (int q = 0; q < 4; ++q)
-                            tma_load_2d(sb + q * BLK, &tm_b0, full, ncol + 64 * q, t.e * p.d + kb * BK);
-                    } else if (MODE == DGRAD_DX) {
-                        const bool up = kb >= hb;
-                        const int kk = up ? kb - hb : kb;
-                        tma_load_2d(sa, up ? &tm_a1 : &tm_a0, full, kk * BK, off + t.m * BM);
-                        for (int q = 0; q < 4; ++q)
-                            tma_load_2d(sb + q * BLK, up ? &tm_b1 : &tm_b0, full, ncol + 64 * q,
-                                        t.e * p.h + kk * BK);
-                    } else {
-                        const int row = off + kb * BK;
-                        const bool up = MODE == WGRAD_GATEUP && t.m >= mt_half;
-                        const int mcol = (MODE == WGRAD_GATEUP && up ? t.m - mt_half : t.m) * BM;
-                        for (int q = 0; q < 2; ++q)
-                            tma_load_2d(sa + q * BLK, up ? &tm_a1 : &tm_a0, full, mcol + 64 * q, row);
-                        for (int q = 0; q < 4; ++q)
-                            tma_load_2d(sb + q * BLK, &tm_b0, full, ncol + 64 * q, row);
-                    }
+                    const int row = off + kb * BK;
+                    const bool up = MODE == WGRAD_GATEUP && t.m >= mt_half;
+                    const int mcol = (up ? t.m - mt_half : t.m) * BM;
+                    for (int q = 0; q < 2; ++q)
+                        tma_load_2d(sa + q * BLK, up ? &tm_a1 : &tm_a0, full, mcol + 64 * q, row);
+                    for (int q = 0; q < 4; ++q)
+                        tma_load_2d(sb + q * BLK, &tm_b0, full, ncol + 64 * q, row);
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
             }
@@ -242,14 +278,14 @@ grouped_gemm_bwd(const __grid_constant__ CUtensorMap tm_a0, const __grid_constan
         // ------------------------------------------------------- MMA issuer
         // the whole warp follows the ring (it zeroes ragged rows in wgrad);
         // lane 0 issues the MMAs and commits
-        constexpr uint32_t idesc = idesc_bf16_f32_major(BM, MMA_N, KG ? 1 : 0, 1);
+        constexpr uint32_t idesc = idesc_bf16_f32_major(BM, MMA_N, 1, 1);
         int stage = 0;
         uint32_t phase = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
         bool ok = true;
         for (int g = blockIdx.x; g < total && ok; g += gridDim.x) {
-            const Tile t = map_tile(KG, g, p, tile_start);
+            const Tile t = map_wgrad_tile(g, p);
             const int cnt = p.count[t.e];
             const int nk = k_blocks<MODE>(p, cnt);
             // every lane waits; the outcome is made warp-uniform
@@ -265,7 +301,7 @@ grouped_gemm_bwd(const __grid_constant__ CUtensorMap tm_a0, const __grid_constan
                     break;
                 }
                 int steps = BK / 16;
-                if (KG && kb == nk - 1) {
+                if (kb == nk - 1) {
                     const int rv = cnt - kb * BK;  // valid rows, 1..64
                     steps = (rv + 15) / 16;
                     const int r16 = steps * 16;
@@ -288,9 +324,8 @@ grouped_gemm_bwd(const __grid_constant__ CUtensorMap tm_a0, const __grid_constan
                     const uint32_t sa = smem_u32(smem + (size_t)stage * STAGE_BYTES);
                     const uint32_t sb = sa + A_BYTES;
                     for (int kk = 0; kk < steps; ++kk) {
-                        const uint64_t ad = KG ? sw128_mnmajor_desc(sa + kk * 2048)
-                                               : sw128_kmajor_desc(sa + kk * 32);
-                        tc_mma_bf16(d_tmem, ad, sw128_mnmajor_desc(sb + kk * 2048), idesc,
+                        tc_mma_bf16(d_tmem, sw128_mnmajor_desc(sa + kk * 2048),
+                                    sw128_mnmajor_desc(sb + kk * 2048), idesc,
                                     (kb | kk) != 0 ? 1u : 0u);
                     }
                     tc_commit(smem_u32(&bars->empty[stage]));
@@ -307,86 +342,15 @@ grouped_gemm_bwd(const __grid_constant__ CUtensorMap tm_a0, const __grid_constan
         // --------------------------------------------------------- epilogue
         const int quad = warp & 3;
         const int half = (warp - 2) >> 2;  // which 128 of the 256 columns
-        const int rit = quad * 32 + lane;  // row of the tile = TMEM lane
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int g = blockIdx.x; g < total; g += gridDim.x) {
-            const Tile t = map_tile(KG, g, p, tile_start);
-            const int cnt = p.count[t.e], off = p.offset[t.e];
+            const Tile t = map_wgrad_tile(g, p);
+            const int cnt = p.count[t.e];
             if (!mbar_wait(smem_u32(&bars->tfull[acc]), acc_phase, status, abort)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * ACC_COLS;
-            if (!KG) {
-                const bool row_ok = rit < cnt - t.m * BM;
-                const int64_t row = (int64_t)off + t.m * BM + rit;
-                const int width = MODE == DGRAD_DH ? p.h : p.d;
-                // saved G, U of this thread's row, prefetched three 16-column
-                // chunks ahead of their use (they come from DRAM)
-                constexpr int PF = 3, NCH = MMA_N / 32;  // 16-column chunks of this half
-                uint4 gq[PF + 1][2], uq[PF + 1][2];
-                auto fetch = [&](int ch, int slot) {
-                    const int col = t.n * MMA_N + half * (MMA_N / 2) + ch * 16;
-                    if (MODE == DGRAD_DH && row_ok && col < width) {
-                        const uint4 *gp = reinterpret_cast<const uint4 *>(p.g_save + row * p.h + col);
-                        const uint4 *up = reinterpret_cast<const uint4 *>(p.u_save + row * p.h + col);
-                        gq[slot][0] = __ldcs(gp);
-                        gq[slot][1] = __ldcs(gp + 1);
-                        uq[slot][0] = __ldcs(up);
-                        uq[slot][1] = __ldcs(up + 1);
-                    }
-                };
-                if (MODE == DGRAD_DH) {
-#pragma unroll
-                    for (int ch = 0; ch < PF; ++ch) fetch(ch, ch);
-                }
-#pragma unroll
-                for (int ch = 0; ch < NCH; ++ch) {
-                    const int c = half * (MMA_N / 2) + ch * 16;
-                    if (MODE == DGRAD_DH && ch + PF < NCH) fetch(ch + PF, (ch + PF) % (PF + 1));
-                    uint32_t r[16];
-                    tmem_ld16(tbase + c, r);
-                    tmem_ld_wait();
-                    reg_fence(r);
-                    const int col = t.n * MMA_N + c;
-                    if (!row_ok || col >= width) continue;
-                    if (MODE == DGRAD_DH) {
-                        const int slot = ch % (PF + 1);
-                        const uint32_t *gw = reinterpret_cast<const uint32_t *>(gq[slot]);
-                        const uint32_t *uw = reinterpret_cast<const uint32_t *>(uq[slot]);
-                        uint32_t dg[8], du[8];
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            float rg[2], ru[2];
-#pragma unroll
-                            for (int hf = 0; hf < 2; ++hf) {
-                                const float z = hf ? bf16_hi(gw[i]) : bf16_lo(gw[i]);
-                                const float u = hf ? bf16_hi(uw[i]) : bf16_lo(uw[i]);
-                                const float dh = __uint_as_float(r[2 * i + hf]);
-                                const float sg = __fdividef(1.0f, 1.0f + __expf(-z));
-                                ru[hf] = dh * (z * sg);
-                                rg[hf] = dh * u * sg * (1.0f + z * (1.0f - sg));
-                            }
-                            dg[i] = pack_bf16x2(rg[0], rg[1]);
-                            du[i] = pack_bf16x2(ru[0], ru[1]);
-                        }
-                        uint4 *gd = reinterpret_cast<uint4 *>(p.out0 + row * p.h + col);
-                        uint4 *ud = reinterpret_cast<uint4 *>(p.out1 + row * p.h + col);
-                        gd[0] = make_uint4(dg[0], dg[1], dg[2], dg[3]);
-                        gd[1] = make_uint4(dg[4], dg[5], dg[6], dg[7]);
-                        ud[0] = make_uint4(du[0], du[1], du[2], du[3]);
-                        ud[1] = make_uint4(du[4], du[5], du[6], du[7]);
-                    } else {
-                        uint32_t pk[8];
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]),
-                                                __uint_as_float(r[2 * i + 1]));
-                        uint4 *dst = reinterpret_cast<uint4 *>(p.out0 + row * p.d + col);
-                        dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                        dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-                    }
-                }
-            } else {
+            {
                 // weight gradient, fp32; an expert without rows gets zeros.
                 // Each 32 x 16 block goes through a padded shared-memory block so
                 // that a store instruction writes 64-byte row segments.
@@ -434,18 +398,253 @@ grouped_gemm_bwd(const __grid_constant__ CUtensorMap tm_a0, const __grid_constan
 }
 
 template <int MODE>
-moe_status launch_bwd(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap &b0,
-                      const CUtensorMap &b1, const Params &p, int max_tiles, cudaStream_t st) {
-    static size_t configured = 0;
-    const size_t smem = smem_bytes(p.N);
-    if (smem > configured) {
-        if (cudaFuncSetAttribute(grouped_gemm_bwd<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem_bytes(kMaxN)) != cudaSuccess)
+moe_status launch_wgrad(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap &b0,
+                        const CUtensorMap &b1, const Params &p, int max_tiles, cudaStream_t st) {
+    static bool configured = false;
+    const size_t smem = smem_bytes();
+    if (!configured) {
+        if (cudaFuncSetAttribute(grouped_wgrad<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem) != cudaSuccess)
             return MOE_ERR_CUDA;
-        configured = smem_bytes(kMaxN);
+        configured = true;
     }
     const int grid = std::min(num_sms(), std::max(max_tiles, 1));
-    grouped_gemm_bwd<MODE><<<grid, ModeT<MODE>::threads, smem, st>>>(a0, a1, b0, b1, p);
+    grouped_wgrad<MODE><<<grid, ModeT<MODE>::threads, smem, st>>>(a0, a1, b0, b1, p);
+    return launch_status();
+}
+
+// --------------------------------------------------------- CTA-pair dgrad
+//
+// dH and dX on CTA pairs, as in the forward kernel: each 256-row x 256-column
+// tile is one tcgen05.mma.cta_group::2 per K-step; each CTA holds its own 128
+// rows of A (K-major) and half of B (two 64-column MN-major blocks of the
+// transposed weight), 32 KB per k-block in a 6-stage ring.  The leader issues
+// the MMAs; both CTAs' loads complete on the leader's full barrier; the
+// leader's commits release stages and accumulators in both CTAs.
+constexpr int P_STAGES = 6;
+constexpr int P_STAGE_BYTES = A_BYTES + B_BYTES / 2;  // 32 KB
+constexpr int P_EPI_WARPS = kEpiThreads / 32;
+
+struct alignas(8) PairBars {
+    uint64_t full[P_STAGES];
+    uint64_t empty[P_STAGES];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint32_t tmem_base;
+    int abort;
+};
+
+constexpr size_t smem_bytes_pair(int N) {
+    return 1024 + (size_t)P_STAGES * P_STAGE_BYTES + sizeof(PairBars) + sizeof(int32_t) * (N + 1) +
+           16;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(ModeT<MODE>::threads, 1)
+grouped_dgrad_pair(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
+                   const __grid_constant__ CUtensorMap tm_b0, const __grid_constant__ CUtensorMap tm_b1,
+                   const Params p) {
+    static_assert(MODE == DGRAD_DH || MODE == DGRAD_DX, "dgrad only");
+    constexpr int PM = 2 * BM;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    PairBars *bars = reinterpret_cast<PairBars *>(smem + (size_t)P_STAGES * P_STAGE_BYTES);
+    int32_t *tile_start = reinterpret_cast<int32_t *>(bars + 1);
+    volatile int *abort = &bars->abort;
+    int *status = p.status;
+    const uint32_t rank = cluster_rank();
+    const bool leader = rank == 0;
+    const int unit0 = (int)blockIdx.x / 2, units = (int)gridDim.x / 2;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < P_STAGES; ++s) {
+            mbar_init(smem_u32(&bars->full[s]), 1);
+            mbar_init(smem_u32(&bars->empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&bars->tfull[b]), 1);
+            mbar_init(smem_u32(&bars->tempty[b]), 2 * P_EPI_WARPS);
+        }
+        bars->abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        int carry = 0;
+        for (int base = 0; base < p.N; base += 32) {
+            const int e = base + lane;
+            const int v = e < p.N ? ((p.count[e] + PM - 1) / PM) * p.ntn : 0;
+            int incl = v;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int u = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+                if (lane >= off) incl += u;
+            }
+            if (e < p.N) tile_start[e] = carry + incl - v;
+            carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+        }
+        if (lane == 0) tile_start[p.N] = carry;
+    }
+    if (warp == 1) tmem_alloc_pair(smem_u32(&bars->tmem_base), TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();
+    tc_fence_after();
+    const uint32_t tmem_base = bars->tmem_base;
+    const int total = tile_start[p.N];
+    const int nk = k_blocks<MODE>(p, 0);
+    const int hb = p.h / BK;
+
+    auto map_pair = [&](int g) {
+        int lo = 0, hi = p.N - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (tile_start[mid] <= g) lo = mid;
+            else hi = mid - 1;
+        }
+        const int mt = (p.count[lo] + PM - 1) / PM;
+        const int l = g - tile_start[lo];
+        return Tile{lo, l % mt, l / mt};
+    };
+
+    if (warp == 0) {
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_a0);
+            tma_prefetch_desc(&tm_b0);
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued = 0;
+            bool ok = true;
+            for (int g = unit0; g < total && ok; g += units) {
+                const Tile t = map_pair(g);
+                const int a_row = p.offset[t.e] + t.m * PM + (int)rank * BM;
+                const int ncol = t.n * MMA_N + (int)rank * (MMA_N / 2);
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!mbar_wait(smem_u32(&bars->empty[stage]), phase ^ 1, status, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t own_full = smem_u32(&bars->full[stage]);
+                    const uint32_t full = cluster_map(own_full, 0);
+                    const uint32_t sa = smem_u32(smem + (size_t)stage * P_STAGE_BYTES);
+                    const uint32_t sb = sa + A_BYTES;
+                    if (leader) mbar_arrive_expect_tx(own_full, 2 * P_STAGE_BYTES);
+                    const bool up = MODE == DGRAD_DX && kb >= hb;
+                    const int kk = up ? kb - hb : kb;
+                    const int brow = MODE == DGRAD_DH ? t.e * p.d + kb * BK : t.e * p.h + kk * BK;
+                    tma_load_2d_pair(sa, up ? &tm_a1 : &tm_a0, full, kk * BK, a_row);
+                    for (int q = 0; q < 2; ++q)
+                        tma_load_2d_pair(sb + q * BLK, up ? &tm_b1 : &tm_b0, full, ncol + 64 * q,
+                                         brow);
+                    ++issued;
+                    if (++stage == P_STAGES) { stage = 0; phase ^= 1; }
+                }
+            }
+            if (!ok && leader) {
+                for (int s = 0; s < P_STAGES; ++s) {
+                    volatile int no_abort = 0;
+                    mbar_wait(smem_u32(&bars->full[s]), phase ^ (s >= stage ? 1 : 0), status,
+                              &no_abort);
+                }
+            }
+            for (int s = 0; s < P_STAGES; ++s) {
+                const int uses = issued / P_STAGES + (s < issued % P_STAGES ? 1 : 0);
+                if (uses > 0)
+                    mbar_wait(smem_u32(&bars->empty[s]), (uint32_t)((uses - 1) & 1), status, abort);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            constexpr uint32_t idesc = idesc_bf16_f32_major(PM, MMA_N, 0, 1);
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (int g = unit0; g < total && ok; g += units) {
+                if (!mbar_wait(smem_u32(&bars->tempty[acc]), acc_phase ^ 1, status, abort)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * ACC_COLS);
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!mbar_wait(smem_u32(&bars->full[stage]), phase, status, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + (size_t)stage * P_STAGE_BYTES);
+                    const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        tc_mma_bf16_pair(d_tmem, sw128_kmajor_desc(sa + kk * 32),
+                                         sw128_mnmajor_desc(sb + kk * 2048), idesc,
+                                         (kb | kk) != 0 ? 1u : 0u);
+                    tc_commit_pair(smem_u32(&bars->empty[stage]));
+                    if (++stage == P_STAGES) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+                tc_commit_pair(smem_u32(&bars->tfull[acc]));
+                if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+            }
+        }
+    } else {
+        const int quad = warp & 3;
+        const int half = (warp - 2) >> 2;
+        const int rit = (int)rank * BM + quad * 32 + lane;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int g = unit0; g < total; g += units) {
+            const Tile t = map_pair(g);
+            const int cnt = p.count[t.e], off = p.offset[t.e];
+            if (!mbar_wait(smem_u32(&bars->tfull[acc]), acc_phase, status, abort)) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * ACC_COLS;
+            const bool row_ok = rit < cnt - t.m * PM;
+            const int64_t row = (int64_t)off + t.m * PM + rit;
+            dgrad_epilogue<MODE>(tbase, half, row_ok, row, t.n, p);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(cluster_map(smem_u32(&bars->tempty[acc]), 0));
+            if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    }
+}
+
+template <int MODE>
+moe_status launch_dgrad_pair(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap &b0,
+                             const CUtensorMap &b1, const Params &p, int max_units, cudaStream_t st) {
+    static size_t configured = 0;
+    const size_t smem = smem_bytes_pair(p.N);
+    if (smem > configured) {
+        if (cudaFuncSetAttribute(grouped_dgrad_pair<MODE>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem_bytes_pair(kMaxN)) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        configured = smem_bytes_pair(kMaxN);
+    }
+    const int pairs = std::min(num_sms() / 2, std::max(max_units, 1));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(2 * pairs));
+    cfg.blockDim = dim3(ModeT<MODE>::threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, grouped_dgrad_pair<MODE>, a0, a1, b0, b1, p) != cudaSuccess)
+        return MOE_ERR_CUDA;
     return launch_status();
 }
 
@@ -526,25 +725,26 @@ MOE_API moe_status moe_expert_ffn_backward(
     p.u_save = u_save;
     p.out0 = dG;
     p.out1 = dU;
-    r = launch_bwd<DGRAD_DH>(dy_k, dy_k, wd_mn, wd_mn, p, row_tiles * p.ntn, stream);
+    const int pair_tiles = (row_tiles + 1) / 2 + s->N;
+    r = launch_dgrad_pair<DGRAD_DH>(dy_k, dy_k, wd_mn, wd_mn, p, pair_tiles * p.ntn, stream);
     if (r != MOE_OK) return r;
     // dX = dG W_gate + dU W_up
     p.ntn = (s->d + MMA_N - 1) / MMA_N;
     p.out0 = dx_disp;
     p.out1 = nullptr;
-    r = launch_bwd<DGRAD_DX>(dg_k, du_k, wg_mn, wu_mn, p, row_tiles * p.ntn, stream);
+    r = launch_dgrad_pair<DGRAD_DX>(dg_k, du_k, wg_mn, wu_mn, p, pair_tiles * p.ntn, stream);
     if (r != MOE_OK) return r;
     // dW_down = dY^T H
     p.mtn = (s->d + BM - 1) / BM;
     p.ntn = (s->h + MMA_N - 1) / MMA_N;
     p.fout0 = dw_down;
     p.fout1 = nullptr;
-    r = launch_bwd<WGRAD_DOWN>(dy_mn, dy_mn, h_mn, h_mn, p, s->N * p.mtn * p.ntn, stream);
+    r = launch_wgrad<WGRAD_DOWN>(dy_mn, dy_mn, h_mn, h_mn, p, s->N * p.mtn * p.ntn, stream);
     if (r != MOE_OK) return r;
     // dW_gate = dG^T X, dW_up = dU^T X
     p.mtn = wg_mt;
     p.ntn = (s->d + MMA_N - 1) / MMA_N;
     p.fout0 = dw_gate;
     p.fout1 = dw_up;
-    return launch_bwd<WGRAD_GATEUP>(dg_mn, du_mn, x_mn, x_mn, p, s->N * p.mtn * p.ntn, stream);
+    return launch_wgrad<WGRAD_GATEUP>(dg_mn, du_mn, x_mn, x_mn, p, s->N * p.mtn * p.ntn, stream);
 }
