@@ -176,6 +176,11 @@ CONFIGS = {
                       router_std=0.01),
     "train": MoEConfig("train", T=8192, d=2048, N=64, K=8, h=1024, cf_num=5, cf_den=4, seed=4,
                        backward=True),
+    # dropless: cap = T (an expert can take every token, since a token's K
+    # experts are distinct), so no route is ever dropped; the packed prefix
+    # still holds exactly the T*K routes
+    "olmoe_dropless": MoEConfig("olmoe_dropless", T=8192, d=2048, N=64, K=8, h=1024, cf_num=8,
+                                cf_den=1, seed=5),
 }
 
 

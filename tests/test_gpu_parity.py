@@ -251,3 +251,17 @@ def test_forward_enqueues_without_host_sync(moe):
     finally:
         torch.cuda.set_sync_debug_mode("default")
     torch.cuda.synchronize()
+
+
+def test_dropless_capacity(moe):
+    """Dropless variant: cap = T, so every route is accepted; expert counts
+    equal demands and the packed prefix holds all T*K routes (same kernels)."""
+    cfg = synth.CONFIGS["olmoe_dropless"].with_(T=2048, d=256, h=128)
+    assert cfg.cap == cfg.T
+    x, wr, bias, wg, wu, wd = _inputs(cfg)
+    ref = oracle.layer_forward(x, wr, bias, wg, wu, wd, cfg.K, cfg.cap)
+    buf = _run_chain(moe, cfg, x, wr, bias, wg, wu, wd)
+    _check_route(buf, ref)
+    assert (ref["route_row"] >= 0).all()
+    assert int(ref["expert_offset"][-1]) == cfg.T * cfg.K
+    assert_close_bf16(bits(buf.y), ref["y"], "dropless y")
