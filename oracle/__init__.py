@@ -48,6 +48,7 @@ def _declare(L):
         "oracle_dispatch_bwd": [_I, _I, _I, _P, _P, _P],
         "oracle_expert_ffn_bwd": [_I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                   _P, _P],
+        "oracle_router_bwd": [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P],
     }
     for name, args in sig.items():
         f = getattr(L, name)
@@ -251,6 +252,24 @@ def expert_ffn_bwd(count, offset, x_disp, g_save, u_save, h_act, dy_disp, wg, wu
                                 _p(u_save), _p(h_act), _p(dy_disp), _p(wg), _p(wu), _p(wd),
                                 _p(dx), _p(dwg), _p(dwu), _p(dwd))
     return dx, dwg, dwu, dwd
+
+
+def router_bwd(x, w_r, idx, gate, dgate, dx=None, with_bias=True):
+    """Router backward for a fixed top-K selection: returns dlogit [T,K],
+    dx (the given dx plus the router's share; zeros if None), dW_r [N,d] and
+    dbias [N] (None unless with_bias)."""
+    x = _c(x, np.uint16); w_r = _c(w_r, np.float32)
+    idx = _c(idx, np.int32); gate = _c(gate, np.float32); dgate = _c(dgate, np.float32)
+    T, d = x.shape
+    N = w_r.shape[0]
+    K = idx.shape[1]
+    dx = np.zeros((T, d), np.float32) if dx is None else np.array(dx, dtype=np.float32, copy=True)
+    dlogit = np.empty((T, K), np.float32)
+    dw = np.empty((N, d), np.float32)
+    dbias = np.empty(N, np.float32) if with_bias else None
+    lib().oracle_router_bwd(T, d, N, K, _p(x), _p(w_r), _p(idx), _p(gate), _p(dgate),
+                            _p(dlogit), _p(dx), _p(dw), _p(dbias))
+    return dlogit, dx, dw, dbias
 
 
 # ------------------------------------------------------------- whole layer --

@@ -444,3 +444,53 @@ void oracle_expert_ffn_bwd(int N, int d, int h, const int32_t *count, const int3
     }
     free(dwg64); free(dwu64); free(dwd64);
 }
+
+/* ---------------------------------------------------- router backward ---
+ * Gradient of the router for one step whose top-K selection is fixed
+ * ([EP] 5.6: the router-weight gradient comes from the gathered expert outputs
+ * through dgate; Figure 15: the gates are a softmax over the K chosen logits).
+ * With g the gates and dg = dL/dg (dgate, 0 for a dropped route):
+ *   dlogit_k = g_k * (dg_k - sum_k' g_k' dg_k')      (chosen experts; others 0)
+ *   dx[t]    = sum_k dlogit_k W_r[idx_k]              (added to dx)
+ *   dW_r[e]  = sum over routes (t, k) with idx = e of dlogit_k x_t
+ *   dbias[e] = sum over the same routes of dlogit_k    (dbias may be NULL)
+ * fp64 sums, fp32 results.
+ */
+void oracle_router_bwd(int T, int d, int N, int K, const uint16_t *x, const float *w_r,
+                       const int32_t *idx, const float *gate, const float *dgate, float *dlogit,
+                       float *dx, float *dw, float *dbias) {
+    double *acc = (double *)calloc((size_t)N * d, sizeof(double));
+    double *accb = (double *)calloc((size_t)N, sizeof(double));
+    double *dl = (double *)malloc((size_t)K * sizeof(double));
+    double *row = (double *)malloc((size_t)d * sizeof(double));
+    for (int t = 0; t < T; ++t) {
+        double dot = 0.0;
+        for (int k = 0; k < K; ++k)
+            dot += (double)gate[(int64_t)t * K + k] * (double)dgate[(int64_t)t * K + k];
+        for (int k = 0; k < K; ++k) {
+            dl[k] = (double)gate[(int64_t)t * K + k] * ((double)dgate[(int64_t)t * K + k] - dot);
+            dlogit[(int64_t)t * K + k] = (float)dl[k];
+        }
+        for (int j = 0; j < d; ++j) {
+            double sx = 0.0;
+            for (int k = 0; k < K; ++k)
+                sx += dl[k] * (double)w_r[(int64_t)idx[(int64_t)t * K + k] * d + j];
+            row[j] = sx;
+        }
+        for (int j = 0; j < d; ++j)
+            dx[(int64_t)t * d + j] = (float)((double)dx[(int64_t)t * d + j] + row[j]);
+        for (int k = 0; k < K; ++k) {
+            int e = idx[(int64_t)t * K + k];
+            accb[e] += dl[k];
+            for (int j = 0; j < d; ++j)
+                acc[(int64_t)e * d + j] += dl[k] * (double)bf16_to_f32(x[(int64_t)t * d + j]);
+        }
+    }
+    for (int64_t i = 0; i < (int64_t)N * d; ++i) dw[i] = (float)acc[i];
+    if (dbias)
+        for (int e = 0; e < N; ++e) dbias[e] = (float)accb[e];
+    free(acc);
+    free(accb);
+    free(dl);
+    free(row);
+}

@@ -566,3 +566,68 @@ def test_expert_backward_bf16_intermediates_stay_within_rounding():
         np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
     for e_, r_ in zip(exact[:3], rounded[:3]):
         assert np.max(np.abs(e_ - r_)) <= 2.0 ** -8 * np.max(np.abs(e_)) * max(d, h)
+
+
+def test_router_backward_finite_difference():
+    """Router backward against central differences of L = sum_{t,k} c[t,k] g[t,k]
+    with g the softmax over the chosen logits of x W_r^T + bias (selection held
+    fixed; the perturbation is too small to change it)."""
+    rng = np.random.default_rng(11)
+    T, d, N, K = 6, 8, 5, 3
+    x = synth.f32_to_bf16_bits(rng.standard_normal((T, d)).astype(np.float32))
+    xf = oracle.bf16_to_f32(x).astype(np.float64)
+    w = rng.standard_normal((N, d)) * 0.5
+    b = rng.standard_normal(N) * 0.3
+    c = rng.standard_normal((T, K))
+
+    def gates(xv, wv, bv):
+        l = xv @ wv.T + bv
+        idx = np.argsort(-l, axis=1, kind="stable")[:, :K]
+        sel = np.take_along_axis(l, idx, 1)
+        e = np.exp(sel - sel[:, :1])
+        return idx, e / e.sum(1, keepdims=True)
+
+    idx, g = gates(xf, w, b)
+    L = lambda xv, wv, bv: float(np.sum(c * gates(xv, wv, bv)[1]))
+    dl, dx, dw, db = oracle.router_bwd(x, w.astype(np.float32), idx.astype(np.int32),
+                                       g.astype(np.float32), c.astype(np.float32))
+    # the oracle reads W_r as fp32: evaluate with the same rounded weights
+    w = w.astype(np.float32).astype(np.float64)
+    eps = 1e-6
+    for (t, j) in [(0, 0), (3, 5), (5, 7)]:
+        e_ = np.zeros_like(xf); e_[t, j] = eps
+        fd = (L(xf + e_, w, b) - L(xf - e_, w, b)) / (2 * eps)
+        assert abs(fd - dx[t, j]) <= 1e-4 * (1 + abs(fd))
+    for (ee, j) in [(0, 1), (2, 6), (4, 0)]:
+        e_ = np.zeros_like(w); e_[ee, j] = eps
+        fd = (L(xf, w + e_, b) - L(xf, w - e_, b)) / (2 * eps)
+        assert abs(fd - dw[ee, j]) <= 1e-4 * (1 + abs(fd))
+    for ee in range(N):
+        e_ = np.zeros_like(b); e_[ee] = eps
+        fd = (L(xf, w, b + e_) - L(xf, w, b - e_)) / (2 * eps)
+        assert abs(fd - db[ee]) <= 1e-4 * (1 + abs(fd))
+
+
+def test_router_backward_closed_forms():
+    """The logit gradients of a token sum to zero (softmax is shift-invariant);
+    K = 1 gives no gradient at all; equal dgate on all routes gives none; and
+    dx is added to the dx passed in."""
+    rng = np.random.default_rng(12)
+    T, d, N, K = 20, 16, 8, 4
+    x = synth.gen_bf16(1, (T, d), "x")
+    w = rng.standard_normal((N, d)).astype(np.float32)
+    idx = synth.gen_topk_idx(3, T, N, K)
+    g = rng.random((T, K)).astype(np.float32)
+    g /= g.sum(1, keepdims=True)
+    dg = rng.standard_normal((T, K)).astype(np.float32)
+    dl, dx, dw, db = oracle.router_bwd(x, w, idx, g, dg)
+    np.testing.assert_allclose(dl.astype(np.float64).sum(1), 0, atol=1e-6)
+    np.testing.assert_allclose(db.astype(np.float64).sum(), 0, atol=1e-5)
+    dl1, dx1, dw1, db1 = oracle.router_bwd(x, w, idx[:, :1], np.ones((T, 1), np.float32), dg[:, :1])
+    assert np.all(dl1 == 0) and np.all(dx1 == 0) and np.all(dw1 == 0)
+    same = np.repeat(dg[:, :1], K, 1)
+    dl2, _, _, _ = oracle.router_bwd(x, w, idx, g, same)
+    np.testing.assert_allclose(dl2, 0, atol=1e-6)
+    base = rng.standard_normal((T, d)).astype(np.float32)
+    _, dx3, _, _ = oracle.router_bwd(x, w, idx, g, dg, dx=base)
+    np.testing.assert_allclose(dx3, base + dx, rtol=1e-6, atol=1e-6)
