@@ -2,9 +2,9 @@
 
 One step = one forward pass of the whole layer over one batch of T tokens:
 route (logits, top-K, gates, slots) -> dispatch -> grouped SwiGLU experts ->
-combine, through the C ABI (`--config train` adds the combine, expert and
-dispatch backward).  Inputs are seeded synthetic tensors resident in HBM;
-between timed steps L2 is flushed by writing a 512 MiB buffer (outside the
+combine, through the C ABI (`--config train` adds the combine, expert,
+dispatch and router backward).  Inputs are seeded synthetic tensors resident
+in HBM; between timed steps L2 is flushed by writing a 512 MiB buffer (outside the
 per-step events).  Every step is timed with CUDA events on the launching
 stream; `value` is tokens/s of the whole job (all ranks), `e2e` the same metric
 through the public Python API with the step's input copied from pinned host
@@ -68,7 +68,10 @@ def algorithmic(cfg, A):
     if cfg.backward:
         out.update(combine_bwd_bytes=2.0 * T * d + 2.0 * A * d + 2.0 * A * d + 8.0 * T * K,
                    dispatch_bwd_bytes=2.0 * A * d + 4.0 * T * d + 4.0 * T * K,
-                   gemm_bwd_flop=12.0 * d * h * A)
+                   gemm_bwd_flop=12.0 * d * h * A,
+                   # dispatch backward fused with the router's dx term and dlogit
+                   dispatch_router_bwd_bytes=2.0 * A * d + 4.0 * T * d + 24.0 * T * K + 4.0 * N * d,
+                   router_dw_bytes=2.0 * T * d + 8.0 * T * K + 4.0 * N * d)
     return out
 
 
@@ -172,8 +175,10 @@ def run_ours(args, cfg, rank, world):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
     phases = ["route", "dispatch", "ffn", "combine"] + (
-        ["combine_bwd", "ffn_bwd", "dispatch_bwd"] if cfg.backward else [])
-    launches_per_step = 8 + (6 if cfg.backward else 0)
+        ["combine_bwd", "ffn_bwd", "dispatch_router_bwd", "router_dw"] if cfg.backward else [])
+    router_dw_launches = 2 if (cfg.T + 127) // 128 > 1 else 1
+    launches_per_step = 8 + (6 + router_dw_launches if cfg.backward else 0)
+    db = None if (bias is None or bwd is None) else bwd.dbias
 
     def step(ev=None):
         def mark(i):
@@ -198,8 +203,12 @@ def run_ours(args, cfg, rank, world):
                                     wd, buf.g_save, buf.u_save, buf.h_act, bwd.dy_disp,
                                     bwd.dx_disp, bwd.dw_gate, bwd.dw_up, bwd.dw_down, bwd.ws)
             mark(6)
-            moe.dispatch_backward(shape, bwd.dx_disp, buf.route_row, bwd.dx)
+            moe.dispatch_router_backward(shape, bwd.dx_disp, buf.route_row, wr, buf.topk_idx,
+                                         buf.topk_gate, bwd.dgate, bwd.dlogit, bwd.dx)
             mark(7)
+            moe.router_weight_backward(shape, x, buf.topk_idx, bwd.dlogit, bwd.dw_router, db,
+                                       bwd.router_ws)
+            mark(8)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -258,7 +267,8 @@ def run_ours(args, cfg, rank, world):
         y_host.copy_(buf.y, non_blocking=True)
         if cfg.backward:
             dy_dev_e2e.copy_(dy_host, non_blocking=True)
-            moe.layer_backward(buf, bwd, dy_dev_e2e, wg, wu, wd)
+            moe.layer_backward(buf, bwd, dy_dev_e2e, wg, wu, wd, x=x_dev_e2e, w_router=wr,
+                               with_bias=bias is not None)
             dx_host.copy_(bwd.dx, non_blocking=True)
 
     e2e_steps = max(3, min(args.steps, 50))
@@ -331,7 +341,9 @@ def run_ours(args, cfg, rank, world):
         bt = alg["gemm_bwd_flop"] / (ph_ms["ffn_bwd"] / 1e3) / 1e12
         line["backward"] = {
             "combine_bwd_gbs": alg["combine_bwd_bytes"] / (ph_ms["combine_bwd"] / 1e3) / 1e9,
-            "dispatch_bwd_gbs": alg["dispatch_bwd_bytes"] / (ph_ms["dispatch_bwd"] / 1e3) / 1e9,
+            "dispatch_router_bwd_gbs": alg["dispatch_router_bwd_bytes"] /
+                                       (ph_ms["dispatch_router_bwd"] / 1e3) / 1e9,
+            "router_dw_gbs": alg["router_dw_bytes"] / (ph_ms["router_dw"] / 1e3) / 1e9,
             "expert_bwd_tflops": bt, "expert_bwd_frac": bt / pk["bf16"]}
     if rank == 0 and not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(cfg, args.cpu_budget_s)
@@ -370,7 +382,9 @@ def _oracle_sample(cfg, tokens):
         dxd, dwg, dwu, dwd = oracle.expert_ffn_bwd(out["expert_count"], out["expert_offset"],
                                                    out["x_disp"], out["g_save"], out["u_save"],
                                                    out["h_act"], dyd, wg, wu, wd)
-        oracle.dispatch_bwd(dxd, out["route_row"], tokens)
+        dx = oracle.dispatch_bwd(dxd, out["route_row"], tokens)
+        oracle.router_bwd(x, inp["wr"], out["topk_idx"], out["topk_gate"], dg, dx=dx,
+                          with_bias=inp["bias"] is not None)
     return time.perf_counter() - t0
 
 

@@ -42,7 +42,8 @@ class Shape(ctypes.Structure):
 
     @property
     def R(self):
-        return self.N * self.cap
+        """Rows of every capacity buffer, min(N*cap, T*K) (moe_buffer_rows)."""
+        return min(self.N * self.cap, self.T * self.K)
 
 
 _P = ctypes.c_void_p
@@ -62,6 +63,11 @@ _SIG = {
     "moe_expert_ffn_backward_workspace_bytes": ([_SP], _SZ),
     "moe_expert_ffn_backward": ([_SP] + [_P] * 14 + [_P, _SZ, _P], ctypes.c_int),
     "moe_selftest_wait_timeout": ([_P, ctypes.c_uint64, _P], ctypes.c_int),
+    "moe_router_backward_workspace_bytes": ([_SP], _SZ),
+    "moe_router_backward": ([_SP] + [_P] * 9 + [_P, _SZ, _P], ctypes.c_int),
+    "moe_buffer_rows": ([_SP], ctypes.c_int64),
+    "moe_dispatch_router_backward": ([_SP] + [_P] * 8 + [_P], ctypes.c_int),
+    "moe_router_weight_backward": ([_SP] + [_P] * 5 + [_P, _SZ, _P], ctypes.c_int),
 }
 for _name, (_args, _res) in _SIG.items():
     _f = getattr(_lib, _name)
@@ -184,6 +190,45 @@ def expert_ffn_backward(shape, x_disp, expert_count, expert_offset, w_gate, w_up
         _stream(stream)), "moe_expert_ffn_backward")
 
 
+def buffer_rows(shape):
+    """Rows of every capacity buffer, min(N*cap, T*K); -1 for an invalid shape."""
+    return int(_lib.moe_buffer_rows(ctypes.byref(shape)))
+
+
+def router_backward_workspace_bytes(shape):
+    return int(_lib.moe_router_backward_workspace_bytes(ctypes.byref(shape)))
+
+
+def router_backward(shape, x, w_router, topk_idx, topk_gate, dgate, dlogit, dx, dw_router, dbias,
+                    ws, stream=None):
+    """dlogit, dx += router term, dw_router, dbias (may be None); see include/moe.h."""
+    _check(_lib.moe_router_backward(
+        ctypes.byref(shape), _ptr(x, _bf16, "x"), _ptr(w_router, _f32, "w_router"),
+        _ptr(topk_idx, _i32, "topk_idx"), _ptr(topk_gate, _f32, "topk_gate"),
+        _ptr(dgate, _f32, "dgate"), _ptr(dlogit, _f32, "dlogit"), _ptr(dx, _f32, "dx"),
+        _ptr(dw_router, _f32, "dw_router"), _ptr(dbias, _f32, "dbias"), _ptr(ws, None, "ws"),
+        ws.numel() * ws.element_size(), _stream(stream)), "moe_router_backward")
+
+
+def dispatch_router_backward(shape, dx_disp, route_row, w_router, topk_idx, topk_gate, dgate,
+                             dlogit, dx, stream=None):
+    """dx = dispatch backward + router term, and dlogit, in one pass (include/moe.h)."""
+    _check(_lib.moe_dispatch_router_backward(
+        ctypes.byref(shape), _ptr(dx_disp, _bf16, "dx_disp"), _ptr(route_row, _i32, "route_row"),
+        _ptr(w_router, _f32, "w_router"), _ptr(topk_idx, _i32, "topk_idx"),
+        _ptr(topk_gate, _f32, "topk_gate"), _ptr(dgate, _f32, "dgate"), _ptr(dlogit, _f32, "dlogit"),
+        _ptr(dx, _f32, "dx"), _stream(stream)), "moe_dispatch_router_backward")
+
+
+def router_weight_backward(shape, x, topk_idx, dlogit, dw_router, dbias, ws, stream=None):
+    """dw_router and dbias (may be None) from dlogit (include/moe.h)."""
+    _check(_lib.moe_router_weight_backward(
+        ctypes.byref(shape), _ptr(x, _bf16, "x"), _ptr(topk_idx, _i32, "topk_idx"),
+        _ptr(dlogit, _f32, "dlogit"), _ptr(dw_router, _f32, "dw_router"),
+        _ptr(dbias, _f32, "dbias"), _ptr(ws, None, "ws"), ws.numel() * ws.element_size(),
+        _stream(stream)), "moe_router_weight_backward")
+
+
 def selftest_wait_timeout(ws, limit_ns, stream=None):
     """Runs the bounded-wait failure path once (see include/moe.h)."""
     _check(_lib.moe_selftest_wait_timeout(_ptr(ws, None, "ws"), int(limit_ns), _stream(stream)),
@@ -249,17 +294,32 @@ class BackwardBuffers:
         self.dw_down = torch.empty((N, d, h), dtype=_f32, **e)
         self.ws = torch.zeros(max(expert_ffn_backward_workspace_bytes(shape), 256),
                               dtype=torch.uint8, **e)
+        self.dlogit = torch.empty((T, K), dtype=_f32, **e)
+        self.dw_router = torch.empty((N, d), dtype=_f32, **e)
+        self.dbias = torch.empty(N, dtype=_f32, **e)
+        self.router_ws = torch.zeros(max(router_backward_workspace_bytes(shape), 256),
+                                     dtype=torch.uint8, **e)
 
 
-def layer_backward(fwd, bwd, dy, w_gate, w_up, w_down, stream=None):
+def layer_backward(fwd, bwd, dy, w_gate, w_up, w_down, stream=None, x=None, w_router=None,
+                   with_bias=False):
     """Combine backward -> grouped expert backward -> dispatch backward (3 C-ABI
     calls) for the forward whose buffers are `fwd` (saved with
-    save_for_backward=True).  Fills bwd.dgate, bwd.dx, bwd.dw_*."""
+    save_for_backward=True).  Fills bwd.dgate, bwd.dx, bwd.dw_*.  Given the
+    forward's x and w_router, the dispatch backward also adds the router term
+    to bwd.dx (one pass) and a fourth call fills bwd.dlogit, bwd.dw_router (and
+    bwd.dbias)."""
     s = fwd.shape
     combine_backward(s, dy, fwd.y_disp, fwd.route_row, fwd.topk_gate, bwd.dy_disp, bwd.dgate,
                      stream)
     expert_ffn_backward(s, fwd.x_disp, fwd.expert_count, fwd.expert_offset, w_gate, w_up, w_down,
                         fwd.g_save, fwd.u_save, fwd.h_act, bwd.dy_disp, bwd.dx_disp, bwd.dw_gate,
                         bwd.dw_up, bwd.dw_down, bwd.ws, stream)
-    dispatch_backward(s, bwd.dx_disp, fwd.route_row, bwd.dx, stream)
+    if w_router is None:
+        dispatch_backward(s, bwd.dx_disp, fwd.route_row, bwd.dx, stream)
+    else:
+        dispatch_router_backward(s, bwd.dx_disp, fwd.route_row, w_router, fwd.topk_idx,
+                                 fwd.topk_gate, bwd.dgate, bwd.dlogit, bwd.dx, stream)
+        router_weight_backward(s, x, fwd.topk_idx, bwd.dlogit, bwd.dw_router,
+                               bwd.dbias if with_bias else None, bwd.router_ws, stream)
     return bwd

@@ -17,6 +17,11 @@ MOE_API const char *moe_status_string(moe_status s) {
     return "unknown moe_status";
 }
 
+MOE_API int64_t moe_buffer_rows(const moe_shape *s) {
+    if (check_shape(s) != MOE_OK) return -1;
+    return buffer_rows(s);
+}
+
 MOE_API moe_status moe_read_device_error(void *ws, int32_t *code_out, cudaStream_t stream) {
     if (!ws || !code_out) return MOE_ERR_INVALID_ARG;
     int32_t v = 0;

@@ -397,7 +397,7 @@ MOE_API moe_status moe_expert_ffn(const moe_shape *s, const moe_bf16 *x_disp,
     if (!expert_count || !expert_offset || !ws) return MOE_ERR_INVALID_ARG;
     if ((g_save == nullptr) != (u_save == nullptr)) return MOE_ERR_INVALID_ARG;
     if (ws_bytes < 256 || (reinterpret_cast<uintptr_t>(ws) & 255u)) return MOE_ERR_WORKSPACE;
-    const int64_t R = (int64_t)s->N * s->cap;
+    const int64_t R = buffer_rows(s);
     if (R == 0 || s->T == 0) return MOE_OK;
     if (!x_disp || !w_gate || !w_up || !w_down || !h_act || !y_disp) return MOE_ERR_INVALID_ARG;
     if (!aligned16(x_disp) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) ||

@@ -657,7 +657,7 @@ using namespace moe;
 
 MOE_API size_t moe_expert_ffn_backward_workspace_bytes(const moe_shape *s) {
     if (check_shape(s) != MOE_OK) return 0;
-    const size_t R = (size_t)s->N * s->cap;
+    const size_t R = (size_t)buffer_rows(s);
     return 256 + 2 * align256(R * s->h * 2);
 }
 
@@ -673,7 +673,7 @@ MOE_API moe_status moe_expert_ffn_backward(
     if (!expert_count || !expert_offset || !ws || !w_gate || !w_up || !w_down || !dw_gate ||
         !dw_up || !dw_down)
         return MOE_ERR_INVALID_ARG;
-    const int64_t R = (int64_t)s->N * s->cap;
+    const int64_t R = buffer_rows(s);
     if (R > 0 && (!x_disp || !g_save || !u_save || !h_act || !dy_disp || !dx_disp))
         return MOE_ERR_INVALID_ARG;
     if (ws_bytes < moe_expert_ffn_backward_workspace_bytes(s) ||

@@ -30,11 +30,17 @@ inline moe_status check_shape(const moe_shape *s) {
     if (!s) return MOE_ERR_INVALID_ARG;
     if (s->T < 0 || s->cap < 0 || s->d <= 0 || s->h <= 0) return MOE_ERR_INVALID_ARG;
     if (s->K < 1 || s->K > kMaxK || s->N < s->K || s->N > kMaxN) return MOE_ERR_INVALID_ARG;
-    if ((int64_t)s->N * s->cap >= (int64_t)1 << 31) return MOE_ERR_INVALID_ARG;
     if ((int64_t)s->T * s->K >= (int64_t)1 << 31) return MOE_ERR_INVALID_ARG;
     if ((int64_t)s->T * s->d >= (int64_t)1 << 40) return MOE_ERR_INVALID_ARG;
     if (s->d % 8 != 0 || s->h % 8 != 0) return MOE_ERR_ALIGNMENT;
     return MOE_OK;
+}
+
+// Rows of every capacity buffer: the packed prefix holds at most cap rows per
+// expert and at most one row per route, so min(N * cap, T * K) rows suffice.
+inline int64_t buffer_rows(const moe_shape *s) {
+    const int64_t a = (int64_t)s->N * s->cap, b = (int64_t)s->T * s->K;
+    return a < b ? a : b;
 }
 
 inline moe_status launch_status() {
@@ -52,6 +58,13 @@ inline int num_sms() {
     }
     return n;
 }
+
+// Router term of the input gradient (rowwise.cu): dlogit and dx (+)= sum_k
+// dlogit_k W_r[e_k]; fused with the dispatch backward when add is false.
+moe_status launch_router_dx(const moe_shape *s, const moe_bf16 *dx_disp, const int32_t *route_row,
+                            const float *w_router, const int32_t *topk_idx,
+                            const float *topk_gate, const float *dgate, float *dlogit, float *dx,
+                            bool add, cudaStream_t stream);
 
 // ---- host: TMA descriptors -----------------------------------------------
 
@@ -111,6 +124,20 @@ __device__ __forceinline__ unsigned long long global_ns() {
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---- cp.async (16-byte global -> shared copies, per thread) ---------------
+
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // ---- mbarrier ------------------------------------------------------------

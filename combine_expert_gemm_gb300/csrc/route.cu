@@ -59,18 +59,6 @@ struct LogitTile {
     }
 };
 
-__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-    asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
 template <int TB, int EC>
 __global__ void __launch_bounds__(kLogitThreads)
 route_logits_topk(int T, int d, int N, int K, const uint16_t *__restrict__ x,

@@ -152,34 +152,123 @@ combine_bwd_rows(int T, int nchunk, int K, const uint4 *__restrict__ dy,
     }
 }
 
-template <int MAXK>
-__global__ void __launch_bounds__(kThreads, MAXK <= 8 ? 4 : 2)
-dispatch_bwd_rows(int T, int nchunk, int K, const uint4 *__restrict__ dx_disp,
-                  const int32_t *__restrict__ route_row, float4 *__restrict__ dx) {
+// Dispatch backward, optionally with the router's share of the input
+// gradient in the same pass over the token's row:
+//   DBWD_PLAIN       dx[t]  = sum_k dx_disp[row_k]
+//   DBWD_ROUTER      dx[t]  = sum_k dx_disp[row_k] + sum_k dlogit_k W_r[e_k]
+//   DBWD_ROUTER_ADD  dx[t] += sum_k dlogit_k W_r[e_k]
+// The router modes also compute and write dlogit (gate softmax Jacobian over
+// the K chosen experts, "Section 05" Figure 15 and 5.6):
+//   dot = fmaf chain over k ascending of g_k dgate_k;  dlogit_k = g_k (dgate_k - dot).
+// W_r rows are fp32 and read through L1/L2 (the [N, d] weight is shared by
+// every token).  Each sum runs over k ascending from 0 (deterministic); the
+// router term is summed apart and added last, so DBWD_ROUTER gives the same
+// bits as DBWD_PLAIN followed by DBWD_ROUTER_ADD.
+enum { DBWD_PLAIN = 0, DBWD_ROUTER = 1, DBWD_ROUTER_ADD = 2 };
+
+template <int MAXK, int MODE>
+__global__ void __launch_bounds__(kThreads, MODE == DBWD_PLAIN ? (MAXK <= 8 ? 4 : 2) : (MAXK <= 8 ? 2 : 1))
+dispatch_bwd_rows(int T, int nchunk, int K, int N, const uint4 *__restrict__ dx_disp,
+                  const int32_t *__restrict__ route_row, float4 *__restrict__ dx,
+                  const float4 *__restrict__ w_r, const int32_t *__restrict__ topk_idx,
+                  const float *__restrict__ gate, const float *__restrict__ dgate,
+                  float *__restrict__ dlogit) {
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
     if (t >= T) return;
-    const int32_t my_row = lane < K ? route_row[(int64_t)t * K + lane] : -1;
-    int32_t rows[MAXK];
-#pragma unroll
-    for (int k = 0; k < MAXK; ++k) rows[k] = __shfl_sync(0xFFFFFFFFu, my_row, k);
-    for (int c = lane; c < nchunk; c += 32) {
-        uint4 v[MAXK];
-#pragma unroll
-        for (int k = 0; k < MAXK; ++k)
-            if (k < K && rows[k] >= 0) v[k] = __ldcs(dx_disp + (int64_t)rows[k] * nchunk + c);
-        float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    // lane k < K holds route k's row, expert and dlogit; the chunk loop
+    // broadcasts them with shuffles (fewer live registers than arrays)
+    int32_t my_row = -1;
+    if (MODE != DBWD_ROUTER_ADD && lane < K) my_row = route_row[(int64_t)t * K + lane];
+    float my_dl = 0.f;
+    int32_t my_e = -1;
+    if (MODE != DBWD_PLAIN) {
+        float g = 0.f, dg = 0.f;
+        if (lane < K) {
+            g = gate[(int64_t)t * K + lane];
+            dg = dgate[(int64_t)t * K + lane];
+            my_e = topk_idx[(int64_t)t * K + lane];
+            if (my_e < 0 || my_e >= N) my_e = -1;
+        }
+        float dot = 0.f;
 #pragma unroll
         for (int k = 0; k < MAXK; ++k) {
-            if (k >= K || rows[k] < 0) continue;
-            float f[8];
-            unpack8(v[k], f);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], f[i]);
+            const float gk = __shfl_sync(0xFFFFFFFFu, g, k);
+            const float dk = __shfl_sync(0xFFFFFFFFu, dg, k);
+            if (k < K) dot = fmaf(gk, dk, dot);
         }
-        float4 *o = dx + ((int64_t)t * nchunk + c) * 2;
-        __stcs(o, make_float4(acc[0], acc[1], acc[2], acc[3]));
-        __stcs(o + 1, make_float4(acc[4], acc[5], acc[6], acc[7]));
+        my_dl = g * (dg - dot);
+        if (lane < K) dlogit[(int64_t)t * K + lane] = my_dl;
+    }
+    int32_t rows_h[MAXK];
+    if (MODE == DBWD_PLAIN) {
+#pragma unroll
+        for (int k = 0; k < MAXK; ++k) rows_h[k] = __shfl_sync(0xFFFFFFFFu, my_row, k);
+    }
+    // warp-uniform chunk loop: the shuffles below need every lane present
+    for (int c0 = 0; c0 < nchunk; c0 += 32) {
+        const int c = c0 + lane;
+        const bool on = c < nchunk;
+        float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        if (MODE == DBWD_ROUTER_ADD) {
+            if (on) {
+                const float4 *p = dx + ((int64_t)t * nchunk + c) * 2;
+                const float4 a = p[0], b = p[1];
+                acc[0] = a.x; acc[1] = a.y; acc[2] = a.z; acc[3] = a.w;
+                acc[4] = b.x; acc[5] = b.y; acc[6] = b.z; acc[7] = b.w;
+            }
+        } else {
+            uint4 v[MAXK];
+            int32_t rows[MAXK];
+#pragma unroll
+            for (int k = 0; k < MAXK; ++k) {
+                rows[k] = MODE == DBWD_PLAIN ? rows_h[k] : __shfl_sync(0xFFFFFFFFu, my_row, k);
+                if (on && k < K && rows[k] >= 0)
+                    v[k] = __ldcs(dx_disp + (int64_t)rows[k] * nchunk + c);
+            }
+#pragma unroll
+            for (int k = 0; k < MAXK; ++k) {
+                if (k >= K || rows[k] < 0) continue;
+                float f[8];
+                unpack8(v[k], f);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], f[i]);
+            }
+        }
+        if (MODE != DBWD_PLAIN) {
+            float r[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+            for (int k0 = 0; k0 < MAXK; k0 += 4) {
+                float4 wa[4], wb[4];
+                float dl[4];
+                int32_t e[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    e[u] = __shfl_sync(0xFFFFFFFFu, my_e, k0 + u);
+                    dl[u] = __shfl_sync(0xFFFFFFFFu, my_dl, k0 + u);
+                    if (on && k0 + u < K && e[u] >= 0) {
+                        const float4 *wp = w_r + ((int64_t)e[u] * nchunk + c) * 2;
+                        wa[u] = __ldg(wp);
+                        wb[u] = __ldg(wp + 1);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    if (k0 + u >= K || e[u] < 0) continue;
+                    r[0] = fmaf(dl[u], wa[u].x, r[0]); r[1] = fmaf(dl[u], wa[u].y, r[1]);
+                    r[2] = fmaf(dl[u], wa[u].z, r[2]); r[3] = fmaf(dl[u], wa[u].w, r[3]);
+                    r[4] = fmaf(dl[u], wb[u].x, r[4]); r[5] = fmaf(dl[u], wb[u].y, r[5]);
+                    r[6] = fmaf(dl[u], wb[u].z, r[6]); r[7] = fmaf(dl[u], wb[u].w, r[7]);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], r[i]);
+        }
+        if (on) {
+            float4 *o = dx + ((int64_t)t * nchunk + c) * 2;
+            __stcs(o, make_float4(acc[0], acc[1], acc[2], acc[3]));
+            __stcs(o + 1, make_float4(acc[4], acc[5], acc[6], acc[7]));
+        }
     }
 }
 
@@ -247,9 +336,52 @@ MOE_API moe_status moe_dispatch_backward(const moe_shape *s, const moe_bf16 *dx_
     if (s->T == 0) return MOE_OK;
     if (!route_row || !dx || (s->cap > 0 && !dx_disp)) return MOE_ERR_INVALID_ARG;
     if (!aligned16(dx_disp) || !aligned16(route_row) || !aligned16(dx)) return MOE_ERR_ALIGNMENT;
-    auto *kern = s->K <= 8 ? dispatch_bwd_rows<8> : dispatch_bwd_rows<16>;
-    kern<<<grid_for(s->T), kThreads, 0, stream>>>(s->T, s->d / 8, s->K,
+    auto *kern = s->K <= 8 ? dispatch_bwd_rows<8, DBWD_PLAIN> : dispatch_bwd_rows<16, DBWD_PLAIN>;
+    kern<<<grid_for(s->T), kThreads, 0, stream>>>(s->T, s->d / 8, s->K, s->N,
                                                  reinterpret_cast<const uint4 *>(dx_disp), route_row,
-                                                 reinterpret_cast<float4 *>(dx));
+                                                 reinterpret_cast<float4 *>(dx), nullptr, nullptr,
+                                                 nullptr, nullptr, nullptr);
     return launch_status();
+}
+
+namespace moe {
+// Router term of dx (and dlogit), alone (add = true: dx += ...) or fused into
+// the dispatch backward (dx = dispatch sum + ...).  Arguments checked by the
+// callers.
+moe_status launch_router_dx(const moe_shape *s, const moe_bf16 *dx_disp, const int32_t *route_row,
+                            const float *w_router, const int32_t *topk_idx,
+                            const float *topk_gate, const float *dgate, float *dlogit, float *dx,
+                            bool add, cudaStream_t stream) {
+    using Fn = void (*)(int, int, int, int, const uint4 *, const int32_t *, float4 *,
+                        const float4 *, const int32_t *, const float *, const float *, float *);
+    Fn kern;
+    if (add)
+        kern = s->K <= 8 ? dispatch_bwd_rows<8, DBWD_ROUTER_ADD>
+                         : dispatch_bwd_rows<16, DBWD_ROUTER_ADD>;
+    else
+        kern = s->K <= 8 ? dispatch_bwd_rows<8, DBWD_ROUTER> : dispatch_bwd_rows<16, DBWD_ROUTER>;
+    kern<<<grid_for(s->T), kThreads, 0, stream>>>(
+        s->T, s->d / 8, s->K, s->N, reinterpret_cast<const uint4 *>(dx_disp), route_row,
+        reinterpret_cast<float4 *>(dx), reinterpret_cast<const float4 *>(w_router), topk_idx,
+        topk_gate, dgate, dlogit);
+    return launch_status();
+}
+}  // namespace moe
+
+MOE_API moe_status moe_dispatch_router_backward(const moe_shape *s, const moe_bf16 *dx_disp,
+                                                const int32_t *route_row, const float *w_router,
+                                                const int32_t *topk_idx, const float *topk_gate,
+                                                const float *dgate, float *dlogit, float *dx,
+                                                cudaStream_t stream) {
+    moe_status r = check_shape(s);
+    if (r != MOE_OK) return r;
+    if (s->T == 0) return MOE_OK;
+    if (!route_row || !dx || (s->cap > 0 && !dx_disp) || !w_router || !topk_idx || !topk_gate ||
+        !dgate || !dlogit)
+        return MOE_ERR_INVALID_ARG;
+    const void *ptrs[] = {dx_disp, route_row, dx, w_router, topk_idx, topk_gate, dgate, dlogit};
+    for (const void *q : ptrs)
+        if (!aligned16(q)) return MOE_ERR_ALIGNMENT;
+    return launch_router_dx(s, dx_disp, route_row, w_router, topk_idx, topk_gate, dgate, dlogit,
+                            dx, false, stream);
 }

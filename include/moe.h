@@ -29,8 +29,10 @@
  *   - bf16 tensors are 16-bit bfloat16 bit patterns (moe_bf16); every pointer
  *     must be 16-byte aligned and d, h must be multiples of 8.
  *   - Row-major layouts.  T tokens, d model width, N experts, K routes per
- *     token, h expert hidden width, cap rows per expert, R = N * cap rows in
- *     every capacity buffer.
+ *     token, h expert hidden width, cap rows per expert, R = min(N * cap, T * K)
+ *     rows in every capacity buffer (moe_buffer_rows; the packed rows never
+ *     exceed either bound, so a dropless caller with cap = T needs T * K rows,
+ *     not N * T).  Larger buffers are accepted; the extra rows are tail.
  *   - Capacity buffers hold the experts' rows packed back to back from row 0:
  *     expert e owns rows [expert_offset[e], expert_offset[e] + expert_count[e]).
  *     Rows from expert_offset[N] to R - 1 (the tail) are neither read nor
@@ -69,8 +71,14 @@ typedef struct {
     int32_t T, d, N, K, h, cap;
 } moe_shape;
 
-/* Limits: 1 <= K <= 16, K <= N <= 1024, 0 <= cap, T >= 0, N * cap < 2^31,
- * T * K < 2^31, 8 <= d, h with d, h multiples of 8. */
+/* Limits: 1 <= K <= 16, K <= N <= 1024, 0 <= cap, T >= 0, T * K < 2^31,
+ * 8 <= d, h with d, h multiples of 8. */
+
+/* Rows R of every capacity buffer (x_disp, h_act, g_save, u_save, y_disp,
+ * dy_disp, dx_disp) for this shape: min(N * cap, T * K); -1 if the shape is
+ * invalid.  The packed layout ([EP] "Padded tiles and device offsets": experts
+ * back to back at cumulative offsets) never places a row at or past it. */
+int64_t moe_buffer_rows(const moe_shape *s);
 
 /* Human-readable name of a status code (static string). */
 const char *moe_status_string(moe_status s);
@@ -238,6 +246,77 @@ moe_status moe_combine_backward(const moe_shape *s, const moe_bf16 *dy, const mo
  */
 moe_status moe_dispatch_backward(const moe_shape *s, const moe_bf16 *dx_disp,
                                  const int32_t *route_row, float *dx, cudaStream_t stream);
+
+/* Bytes of workspace moe_router_backward and moe_router_weight_backward need
+ * (per-chunk partial sums of dW_r and dbias: at most 32 * N * (d + 1) floats;
+ * 0 if the shape is invalid). */
+size_t moe_router_backward_workspace_bytes(const moe_shape *s);
+
+/*
+ * moe_router_backward -- the router's share of the backward, with the top-K
+ * selection of the forward held fixed.  Section 05, 5.6 (the router-weight
+ * gradient starts from dgate, the gathered expert outputs against the token-
+ * output gradient) and Figure 15 (the K gates of a token are a softmax over
+ * its K chosen logits); AWS Neuron "Router Weights" (one fp32 [N, d] router
+ * weight scores every expert).  For token t with gates g and dgate dg:
+ *   dlogit[t, k] = g[t, k] * (dg[t, k] - dot),  dot = sum_k' g[t, k'] * dg[t, k']
+ *   dx[t, :]    += sum_k dlogit[t, k] * w_router[topk_idx[t, k], :]
+ *   dw_router[e, :] = sum over routes with topk_idx = e of dlogit * x[t, :]
+ *   dbias[e]        = sum over the same routes of dlogit
+ * A dropped route keeps its gate in the softmax, so its dlogit is not zero
+ * even though its dgate is.  Experts that are not selected get no gradient.
+ *   x [T, d] bf16 (the forward's input); w_router [N, d] fp32;
+ *   topk_idx, topk_gate [T, K] as moe_route wrote them (entries outside
+ *   [0, N) are skipped); dgate [T, K] fp32 as moe_combine_backward wrote it;
+ *   dlogit out [T, K] fp32; dx in/out [T, d] fp32 (the router term is ADDED:
+ *   call after moe_dispatch_backward to get the layer's whole input
+ *   gradient); dw_router out [N, d] fp32 (overwritten); dbias out [N] fp32 or
+ *   NULL.  fp32 arithmetic: dot is a fused multiply-add chain over k
+ *   ascending; the dx term is summed over k ascending and then added; dW_r is
+ *   summed per expert in token order within fixed 128-token chunks, the
+ *   chunk sums added in chunk order (deterministic, bit-identical run to run).
+ * Errors: MOE_ERR_INVALID_ARG for null required pointers; MOE_ERR_ALIGNMENT;
+ * MOE_ERR_WORKSPACE if ws is short or not 256-byte aligned;
+ * MOE_ERR_UNSUPPORTED if N and K need more than 227 KB of shared memory.
+ * Same result as moe_dispatch_router_backward (in place of
+ * moe_dispatch_backward) followed by moe_router_weight_backward, which is the
+ * faster pair: it walks each token's rows once for both dx terms.
+ */
+moe_status moe_router_backward(const moe_shape *s, const moe_bf16 *x, const float *w_router,
+                               const int32_t *topk_idx, const float *topk_gate,
+                               const float *dgate, float *dlogit, float *dx, float *dw_router,
+                               float *dbias, void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * moe_dispatch_router_backward -- steps B3 and the router's input gradient in
+ * one pass over each token (Section 05 Table 8 "Dispatch backward GET", 5.6,
+ * Figure 15):
+ *   dlogit[t, k] as in moe_router_backward (written);
+ *   dx[t] = (sum over k ascending, route_row >= 0, of dx_disp[route_row[t, k]])
+ *           + (sum over k ascending of dlogit[t, k] * w_router[topk_idx[t, k]])
+ * each sum fp32 from 0, then the two added: bit-identical to
+ * moe_dispatch_backward followed by the dx part of moe_router_backward.
+ *   dx_disp [R, d] bf16; route_row, topk_idx, topk_gate, dgate [T, K];
+ *   w_router [N, d] fp32; dlogit out [T, K] fp32; dx out [T, d] fp32.
+ * Errors: as moe_dispatch_backward, plus MOE_ERR_INVALID_ARG for a null
+ * router pointer.
+ */
+moe_status moe_dispatch_router_backward(const moe_shape *s, const moe_bf16 *dx_disp,
+                                        const int32_t *route_row, const float *w_router,
+                                        const int32_t *topk_idx, const float *topk_gate,
+                                        const float *dgate, float *dlogit, float *dx,
+                                        cudaStream_t stream);
+
+/*
+ * moe_router_weight_backward -- dw_router and dbias (NULL allowed) from the
+ * dlogit that moe_dispatch_router_backward wrote, as in moe_router_backward.
+ *   x [T, d] bf16; topk_idx [T, K]; dlogit [T, K] fp32; dw_router out [N, d]
+ *   fp32; ws of moe_router_backward_workspace_bytes bytes, 256-byte aligned.
+ */
+moe_status moe_router_weight_backward(const moe_shape *s, const moe_bf16 *x,
+                                      const int32_t *topk_idx, const float *dlogit,
+                                      float *dw_router, float *dbias, void *ws, size_t ws_bytes,
+                                      cudaStream_t stream);
 
 /*
  * moe_read_device_error -- copies the device status word of a workspace to

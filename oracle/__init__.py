@@ -278,7 +278,7 @@ def layer_forward(x, w_r, bias, wg, wu, wd, K, cap, save=False):
     """Route -> dispatch -> grouped SwiGLU experts -> combine, all on the CPU."""
     r = route(x, w_r, bias, K, cap)
     N = w_r.shape[0]
-    R = N * cap
+    R = min(N * cap, x.shape[0] * K)
     x_disp = dispatch(x, r["route_row"], R)
     h_act, gs, us, y_disp = expert_ffn(x_disp, r["expert_count"], r["expert_offset"],
                                        wg, wu, wd, save=save)

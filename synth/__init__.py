@@ -161,7 +161,8 @@ class MoEConfig:
 
     @property
     def R(self) -> int:
-        return self.N * self.cap
+        """Rows of a capacity buffer: the packed rows never exceed N*cap or T*K."""
+        return min(self.N * self.cap, self.T * self.K)
 
     def with_(self, **kw) -> "MoEConfig":
         return replace(self, **kw)
@@ -177,8 +178,8 @@ CONFIGS = {
     "train": MoEConfig("train", T=8192, d=2048, N=64, K=8, h=1024, cf_num=5, cf_den=4, seed=4,
                        backward=True),
     # dropless: cap = T (an expert can take every token, since a token's K
-    # experts are distinct), so no route is ever dropped; the packed prefix
-    # still holds exactly the T*K routes
+    # experts are distinct), so no route is ever dropped; the capacity buffers
+    # hold min(N*cap, T*K) = T*K rows
     "olmoe_dropless": MoEConfig("olmoe_dropless", T=8192, d=2048, N=64, K=8, h=1024, cf_num=8,
                                 cf_den=1, seed=5),
 }

@@ -48,7 +48,7 @@ def _shape(moe, **kw):
 @pytest.mark.parametrize("kw,code", [
     (dict(K=0), 1), (dict(K=17, N=32), 1), (dict(N=1025), 1), (dict(K=9, N=8), 1),
     (dict(T=-1), 1), (dict(cap=-1), 1), (dict(d=100), 2), (dict(h=12), 2),
-    (dict(N=1024, cap=1 << 21), 1),
+    (dict(T=1 << 28, K=8, N=16), 1),
 ])
 def test_shape_validation(moe, kw, code):
     s = _shape(moe, **kw)
@@ -57,6 +57,36 @@ def test_shape_validation(moe, kw, code):
     P = ctypes.c_void_p(16)
     assert lib.moe_dispatch(ctypes.byref(s), P, P, P, None) == code
     assert lib.moe_combine(ctypes.byref(s), P, P, P, P, None) == code
+
+
+def test_buffer_rows_is_the_smaller_bound(moe):
+    """Capacity buffers hold min(N*cap, T*K) rows: the packed prefix never
+    exceeds the per-expert caps nor one row per route."""
+    lib = moe.lib()
+    for kw, rows in [(dict(), 64 * 2), (dict(cap=10), 8 * 10), (dict(cap=0), 0),
+                     (dict(N=1024, K=2, cap=1 << 21), 128), (dict(K=0), -1)]:
+        s = _shape(moe, **kw)
+        assert lib.moe_buffer_rows(ctypes.byref(s)) == rows, kw
+        if rows >= 0:
+            assert s.R == rows
+
+
+def test_router_backward_argument_errors(moe):
+    s = _shape(moe)
+    lib = moe.lib()
+    P, Q = ctypes.c_void_p(256), ctypes.c_void_p(264)
+    ws_n = lib.moe_router_backward_workspace_bytes(ctypes.byref(s))
+    assert ws_n >= 256
+    args = [P] * 8 + [None]                            # x .. dw_router, dbias = NULL
+    bad = list(args); bad[7] = None                    # dw_router
+    assert lib.moe_router_backward(ctypes.byref(s), *bad, P, ws_n, None) == 1
+    bad = list(args); bad[5] = None                    # dlogit
+    assert lib.moe_router_backward(ctypes.byref(s), *bad, P, ws_n, None) == 1
+    bad = list(args); bad[6] = Q                       # dx misaligned
+    assert lib.moe_router_backward(ctypes.byref(s), *bad, P, ws_n, None) == 2
+    assert lib.moe_router_backward(ctypes.byref(s), *args, P, ws_n - 1, None) == 3
+    assert lib.moe_router_backward(ctypes.byref(s), *args, Q, ws_n, None) == 3
+    assert lib.moe_router_backward(ctypes.byref(_shape(moe, K=0)), *args, P, ws_n, None) == 1
 
 
 def test_null_and_alignment_and_workspace_errors(moe):
