@@ -13,13 +13,11 @@
 //   dW_down = dY^T H                          (wgrad, K = rows of e)
 //   dW_gate = dG^T X,  dW_up = dU^T X         (wgrad, K = rows of e)
 //
-// dgrad (dH, dX) runs on CTA pairs like the forward kernel: M = 256 rows per
-// tcgen05.mma.cta_group::2, each CTA holding its own 128 rows of A and half of
-// B, 32 KB per k-block in a 6-stage ring.  wgrad runs one CTA per SM (a 4-stage
-// ring of 48 KB k-blocks, tcgen05.mma M = 128, N = 256), because its ragged
-// last k-block has to be repaired in the shared memory of the CTA that reads
-// it.  Both: persistent, 128-byte swizzle, one thread issuing MMAs into a
-// double-buffered TMEM accumulator, eight epilogue warps.  The backward
+// Every kernel runs on CTA pairs like the forward kernel: 256 x 256 output
+// tiles, one tcgen05.mma.cta_group::2 per K-step, each CTA holding its own 128
+// rows of A and half of B, 32 KB per k-block in a 6-stage ring; persistent,
+// 128-byte swizzle, one thread of the leader issuing MMAs into a double-
+// buffered TMEM accumulator, eight epilogue warps per CTA.  The backward
 // operands that are transposed relative to their storage (weights in dgrad,
 // activations in wgrad) are read MN-major: a TMA box of 64 M/N elements x 64 K
 // rows lands as 64 swizzled 128-byte rows and the MMA descriptor walks it with
@@ -28,10 +26,10 @@
 //
 // In wgrad the reduction runs over an expert's rows, so the last k-block of a
 // tile can reach into the next expert's rows or the tail (which may hold NaN).
-// The MMA warp waits for that block like any other, issues only the 16-row
-// MMA steps that hold valid rows, and first writes zeros over the invalid rows
-// inside the last of those steps (both operands), fencing them to the tensor
-// core's async proxy.
+// The leader issues only the 16-row MMA steps that hold valid rows; inside the
+// last of those steps each CTA's fixer warp first writes zeros over the
+// invalid rows of its own operand blocks, fencing them to the tensor core's
+// async proxy.
 #include <algorithm>
 
 #include "moe_common.cuh"
@@ -42,10 +40,8 @@ namespace {
 constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int MMA_N = 256;
-constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = MMA_N * BK * 2;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int BLK = 64 * BK * 2;  // one MN-major 64 x 64 block: 8 KB
 constexpr int ACC_COLS = 256;
 constexpr int TMEM_COLS = 512;
@@ -76,27 +72,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32_major(int M, int N, int a_
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-struct alignas(8) Bars {
-    uint64_t full[STAGES];
-    uint64_t empty[STAGES];
-    uint64_t tfull[2];
-    uint64_t tempty[2];
-    uint32_t tmem_base;
-    int abort;
-};
-
 constexpr int kEpiThreads = 256;                      // 8 epilogue warps
 constexpr int STG_LD = 17;                           // padded fp32 row of a staging block
 constexpr int STG_BYTES = 8 * 32 * STG_LD * 4;       // one 32 x 16 block per epilogue warp
 
-constexpr size_t smem_bytes() {
-    return 1024 + (size_t)STAGES * STAGE_BYTES + STG_BYTES + sizeof(Bars) + 16;
-}
-
 struct Params {
     int N, d, h;
     int ntn;       // output column tiles of 256
-    int mtn;       // wgrad: output row tiles of 128 (both halves for gate/up)
+    int mtn;       // wgrad: output row tiles of 256 (both halves for gate/up)
     const int32_t *count, *offset;
     const uint16_t *g_save, *u_save;  // DGRAD_DH epilogue inputs
     uint16_t *out0, *out1;            // DH: dG, dU; DX: dx_disp
@@ -196,221 +179,6 @@ __device__ __forceinline__ void dgrad_epilogue(uint32_t tbase, int half, bool ro
             dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
         }
     }
-}
-
-template <int MODE>
-__global__ void __launch_bounds__(ModeT<MODE>::threads, 1)
-grouped_wgrad(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
-                 const __grid_constant__ CUtensorMap tm_b0, const __grid_constant__ CUtensorMap tm_b1,
-                 const Params p) {
-    static_assert(MODE == WGRAD_DOWN || MODE == WGRAD_GATEUP, "wgrad only");
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    float *stage_out = reinterpret_cast<float *>(smem + (size_t)STAGES * STAGE_BYTES);
-    Bars *bars = reinterpret_cast<Bars *>(smem + (size_t)STAGES * STAGE_BYTES + STG_BYTES);
-    volatile int *abort = &bars->abort;
-    int *status = p.status;
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(smem_u32(&bars->full[s]), 1);
-            mbar_init(smem_u32(&bars->empty[s]), 1);
-        }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(smem_u32(&bars->tfull[b]), 1);
-            mbar_init(smem_u32(&bars->tempty[b]), kEpiThreads);
-        }
-        bars->abort = 0;
-        fence_mbar_init();
-    }
-    if (warp == 1) tmem_alloc(smem_u32(&bars->tmem_base), TMEM_COLS);
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem_base = bars->tmem_base;
-    const int total = p.N * p.mtn * p.ntn;
-    const int mt_half = (p.h + BM - 1) / BM;
-
-    if (warp == 0) {
-        // ------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            tma_prefetch_desc(&tm_a0);
-            tma_prefetch_desc(&tm_b0);
-            int stage = 0;
-            uint32_t phase = 0;
-            bool ok = true;
-            for (int g = blockIdx.x; g < total && ok; g += gridDim.x) {
-                const Tile t = map_wgrad_tile(g, p);
-                const int cnt = p.count[t.e], off = p.offset[t.e];
-                const int nk = k_blocks<MODE>(p, cnt);
-                for (int kb = 0; kb < nk; ++kb) {
-                    if (!mbar_wait(smem_u32(&bars->empty[stage]), phase ^ 1, status, abort)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t full = smem_u32(&bars->full[stage]);
-                    const uint32_t sa = smem_u32(smem + (size_t)stage * STAGE_BYTES);
-                    const uint32_t sb = sa + A_BYTES;
-                    mbar_arrive_expect_tx(full, STAGE_BYTES);
-                    const int ncol = t.n * MMA_N;
-                    const int row = off + kb * BK;
-                    const bool up = MODE == WGRAD_GATEUP && t.m >= mt_half;
-                    const int mcol = (up ? t.m - mt_half : t.m) * BM;
-                    for (int q = 0; q < 2; ++q)
-                        tma_load_2d(sa + q * BLK, up ? &tm_a1 : &tm_a0, full, mcol + 64 * q, row);
-                    for (int q = 0; q < 4; ++q)
-                        tma_load_2d(sb + q * BLK, &tm_b0, full, ncol + 64 * q, row);
-                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
-                }
-            }
-            if (!ok) {
-                for (int s = 0; s < STAGES; ++s) {
-                    volatile int no_abort = 0;
-                    mbar_wait(smem_u32(&bars->full[s]), phase ^ (s >= stage ? 1 : 0), status,
-                              &no_abort);
-                }
-            }
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------------- MMA issuer
-        // the whole warp follows the ring (it zeroes ragged rows in wgrad);
-        // lane 0 issues the MMAs and commits
-        constexpr uint32_t idesc = idesc_bf16_f32_major(BM, MMA_N, 1, 1);
-        int stage = 0;
-        uint32_t phase = 0;
-        int acc = 0;
-        uint32_t acc_phase = 0;
-        bool ok = true;
-        for (int g = blockIdx.x; g < total && ok; g += gridDim.x) {
-            const Tile t = map_wgrad_tile(g, p);
-            const int cnt = p.count[t.e];
-            const int nk = k_blocks<MODE>(p, cnt);
-            // every lane waits; the outcome is made warp-uniform
-            if (!__all_sync(0xFFFFFFFFu,
-                            mbar_wait(smem_u32(&bars->tempty[acc]), acc_phase ^ 1, status, abort)))
-                break;
-            tc_fence_after();
-            const uint32_t d_tmem = tmem_base + (uint32_t)(acc * ACC_COLS);
-            for (int kb = 0; kb < nk; ++kb) {
-                if (!__all_sync(0xFFFFFFFFu,
-                                mbar_wait(smem_u32(&bars->full[stage]), phase, status, abort))) {
-                    ok = false;
-                    break;
-                }
-                int steps = BK / 16;
-                if (kb == nk - 1) {
-                    const int rv = cnt - kb * BK;  // valid rows, 1..64
-                    steps = (rv + 15) / 16;
-                    const int r16 = steps * 16;
-                    if (rv < r16) {
-                        // zero rows rv..r16-1 of the 2 A and 4 B MN-major blocks
-                        uint8_t *base = smem + (size_t)stage * STAGE_BYTES;
-                        const int nrow = r16 - rv;
-                        for (int i = lane; i < 6 * nrow * 8; i += 32) {
-                            const int blk = i / (nrow * 8), rem = i % (nrow * 8);
-                            const int row = rv + rem / 8, chunk = rem % 8;
-                            *reinterpret_cast<uint4 *>(base + blk * BLK + row * 128 + chunk * 16) =
-                                make_uint4(0, 0, 0, 0);
-                        }
-                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    }
-                    __syncwarp();
-                }
-                if (lane == 0) {
-                    tc_fence_after();
-                    const uint32_t sa = smem_u32(smem + (size_t)stage * STAGE_BYTES);
-                    const uint32_t sb = sa + A_BYTES;
-                    for (int kk = 0; kk < steps; ++kk) {
-                        tc_mma_bf16(d_tmem, sw128_mnmajor_desc(sa + kk * 2048),
-                                    sw128_mnmajor_desc(sb + kk * 2048), idesc,
-                                    (kb | kk) != 0 ? 1u : 0u);
-                    }
-                    tc_commit(smem_u32(&bars->empty[stage]));
-                }
-                __syncwarp();
-                if (++stage == STAGES) { stage = 0; phase ^= 1; }
-            }
-            if (!ok) break;
-            if (lane == 0) tc_commit(smem_u32(&bars->tfull[acc]));
-            __syncwarp();
-            if (++acc == 2) { acc = 0; acc_phase ^= 1; }
-        }
-    } else {
-        // --------------------------------------------------------- epilogue
-        const int quad = warp & 3;
-        const int half = (warp - 2) >> 2;  // which 128 of the 256 columns
-        int acc = 0;
-        uint32_t acc_phase = 0;
-        for (int g = blockIdx.x; g < total; g += gridDim.x) {
-            const Tile t = map_wgrad_tile(g, p);
-            const int cnt = p.count[t.e];
-            if (!mbar_wait(smem_u32(&bars->tfull[acc]), acc_phase, status, abort)) break;
-            tc_fence_after();
-            const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * ACC_COLS;
-            {
-                // weight gradient, fp32; an expert without rows gets zeros.
-                // Each 32 x 16 block goes through a padded shared-memory block so
-                // that a store instruction writes 64-byte row segments.
-                const bool up = MODE == WGRAD_GATEUP && t.m >= mt_half;
-                const int mbase = (up ? t.m - mt_half : t.m) * BM + quad * 32;
-                const int mlim = MODE == WGRAD_DOWN ? p.d : p.h;
-                const int width = MODE == WGRAD_DOWN ? p.h : p.d;
-                float *out = (up ? p.fout1 : p.fout0) + (int64_t)t.e * mlim * width;
-                float *blk = stage_out + (warp - 2) * 32 * STG_LD;
-                for (int c = half * (MMA_N / 2); c < (half + 1) * (MMA_N / 2); c += 16) {
-                    uint32_t r0[16];
-                    tmem_ld16(tbase + c, r0);
-                    tmem_ld_wait();
-                    reg_fence(r0);
-                    const int col0 = t.n * MMA_N + c;
-                    if (col0 >= width) continue;  // warp-uniform
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        blk[lane * STG_LD + i] = cnt ? __uint_as_float(r0[i]) : 0.0f;
-                    __syncwarp();
-                    const int cq = (lane & 3) * 4;
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int rr = j * 8 + (lane >> 2);
-                        const float *src = blk + rr * STG_LD + cq;
-                        const float4 v = make_float4(src[0], src[1], src[2], src[3]);
-                        if (mbase + rr < mlim)
-                            *reinterpret_cast<float4 *>(out + (int64_t)(mbase + rr) * width + col0 + cq) = v;
-                    }
-                    __syncwarp();
-                }
-            }
-            tc_fence_before();
-            mbar_arrive(smem_u32(&bars->tempty[acc]));
-            if (++acc == 2) { acc = 0; acc_phase ^= 1; }
-        }
-    }
-
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
-        tc_fence_after();
-        tmem_dealloc(tmem_base, TMEM_COLS);
-    }
-}
-
-template <int MODE>
-moe_status launch_wgrad(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap &b0,
-                        const CUtensorMap &b1, const Params &p, int max_tiles, cudaStream_t st) {
-    static bool configured = false;
-    const size_t smem = smem_bytes();
-    if (!configured) {
-        if (cudaFuncSetAttribute(grouped_wgrad<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem) != cudaSuccess)
-            return MOE_ERR_CUDA;
-        configured = true;
-    }
-    const int grid = std::min(num_sms(), std::max(max_tiles, 1));
-    grouped_wgrad<MODE><<<grid, ModeT<MODE>::threads, smem, st>>>(a0, a1, b0, b1, p);
-    return launch_status();
 }
 
 // --------------------------------------------------------- CTA-pair dgrad
@@ -648,6 +416,326 @@ moe_status launch_dgrad_pair(const CUtensorMap &a0, const CUtensorMap &a1, const
     return launch_status();
 }
 
+// --------------------------------------------------------- CTA-pair wgrad
+//
+// dW tiles of 256 output rows x 256 output columns, one tcgen05.mma
+// cta_group::2 per 16 rows of the expert: each CTA holds its own 128 output
+// rows of A and 128 output columns of B, both MN-major (two 64 x 64 blocks
+// each), 32 KB per k-block in the 6-stage ring.  Every k-block but a tile's
+// last completes on the leader's full barrier (both CTAs' copies, as in the
+// dgrad kernel).  A tile's last k-block may be ragged, so each CTA's copy of
+// it completes on that CTA's own barrier; a fixer warp in each CTA then
+// zeroes the invalid rows in its own shared memory, fences them to the async
+// proxy and reports the stage ready on the leader's barrier.  The fixers run
+// while the leader is still busy with the tile's earlier k-blocks, so the
+// repair stays off the MMA issue path.  Stage barriers alternate between the
+// two kinds of use, so each role tracks their phases per stage.
+struct alignas(8) WgradBars {
+    uint64_t full[P_STAGES];      // leader: both CTAs' copies of a k-block landed
+    uint64_t lastfull[P_STAGES];  // this CTA's copy of a tile's last k-block landed
+    uint64_t ready[P_STAGES];     // leader: both fixers repaired a last k-block
+    uint64_t empty[P_STAGES];     // the leader's MMAs are done with the stage
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint32_t tmem_base;
+    int abort;
+};
+
+constexpr int WG_THREADS = 64 + kEpiThreads + 32;  // + the fixer warp
+constexpr int WG_FIXER = 2 + P_EPI_WARPS;          // its warp index
+
+constexpr size_t smem_bytes_wgrad_pair() {
+    return 1024 + (size_t)P_STAGES * P_STAGE_BYTES + STG_BYTES + sizeof(WgradBars) + 16;
+}
+
+__device__ __forceinline__ uint32_t stage_parity(uint32_t bits, int s) { return (bits >> s) & 1u; }
+
+template <int MODE>
+__global__ void __launch_bounds__(WG_THREADS, 1)
+grouped_wgrad_pair(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
+                   const __grid_constant__ CUtensorMap tm_b0, const Params p) {
+    static_assert(MODE == WGRAD_DOWN || MODE == WGRAD_GATEUP, "wgrad only");
+    constexpr int PM = 2 * BM;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    float *stage_out = reinterpret_cast<float *>(smem + (size_t)P_STAGES * P_STAGE_BYTES);
+    WgradBars *bars =
+        reinterpret_cast<WgradBars *>(smem + (size_t)P_STAGES * P_STAGE_BYTES + STG_BYTES);
+    volatile int *abort = &bars->abort;
+    int *status = p.status;
+    const uint32_t rank = cluster_rank();
+    const bool leader = rank == 0;
+    const int unit0 = (int)blockIdx.x / 2, units = (int)gridDim.x / 2;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < P_STAGES; ++s) {
+            mbar_init(smem_u32(&bars->full[s]), 1);
+            mbar_init(smem_u32(&bars->lastfull[s]), 1);
+            mbar_init(smem_u32(&bars->ready[s]), 2);
+            mbar_init(smem_u32(&bars->empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&bars->tfull[b]), 1);
+            mbar_init(smem_u32(&bars->tempty[b]), 2 * P_EPI_WARPS);
+        }
+        bars->abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc_pair(smem_u32(&bars->tmem_base), TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();
+    tc_fence_after();
+    const uint32_t tmem_base = bars->tmem_base;
+    const int total = p.N * p.mtn * p.ntn;
+    const int mt_half = (p.h + PM - 1) / PM;  // gate/up: 256-row tiles per half
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_a0);
+            tma_prefetch_desc(&tm_b0);
+            int stage = 0;
+            uint32_t phase = 0;                    // empty barriers: every use
+            uint32_t par_full = 0, par_last = 0;   // next-use parity per stage
+            uint32_t last_kind = 0;                // stage's latest use was a last k-block
+            int issued = 0;
+            bool ok = true;
+            for (int g = unit0; g < total && ok; g += units) {
+                const Tile t = map_wgrad_tile(g, p);
+                const int cnt = p.count[t.e], off = p.offset[t.e];
+                const int nk = k_blocks<MODE>(p, cnt);
+                const bool up = MODE == WGRAD_GATEUP && t.m >= mt_half;
+                const int mcol = (up ? t.m - mt_half : t.m) * PM + (int)rank * BM;
+                const int ncol = t.n * MMA_N + (int)rank * (MMA_N / 2);
+                const CUtensorMap *ma = up ? &tm_a1 : &tm_a0;
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!mbar_wait(smem_u32(&bars->empty[stage]), phase ^ 1, status, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sa = smem_u32(smem + (size_t)stage * P_STAGE_BYTES);
+                    const uint32_t sb = sa + A_BYTES;
+                    const int row = off + kb * BK;
+                    if (kb == nk - 1) {
+                        const uint32_t bar = smem_u32(&bars->lastfull[stage]);
+                        mbar_arrive_expect_tx(bar, P_STAGE_BYTES);
+                        for (int q = 0; q < 2; ++q) tma_load_2d(sa + q * BLK, ma, bar, mcol + 64 * q, row);
+                        for (int q = 0; q < 2; ++q)
+                            tma_load_2d(sb + q * BLK, &tm_b0, bar, ncol + 64 * q, row);
+                        par_last ^= 1u << stage;
+                        last_kind |= 1u << stage;
+                    } else {
+                        const uint32_t own_full = smem_u32(&bars->full[stage]);
+                        const uint32_t full = cluster_map(own_full, 0);
+                        if (leader) mbar_arrive_expect_tx(own_full, 2 * P_STAGE_BYTES);
+                        for (int q = 0; q < 2; ++q)
+                            tma_load_2d_pair(sa + q * BLK, ma, full, mcol + 64 * q, row);
+                        for (int q = 0; q < 2; ++q)
+                            tma_load_2d_pair(sb + q * BLK, &tm_b0, full, ncol + 64 * q, row);
+                        par_full ^= 1u << stage;
+                        last_kind &= ~(1u << stage);
+                    }
+                    ++issued;
+                    if (++stage == P_STAGES) { stage = 0; phase ^= 1; }
+                }
+            }
+            if (!ok) {
+                // let the copies already issued land before the CTA leaves: the
+                // latest use of each stage completes on its own barrier (a last
+                // k-block) or on the leader's full barrier (the leader waits)
+                for (int s = 0; s < P_STAGES && s < issued; ++s) {
+                    volatile int no_abort = 0;
+                    if (last_kind >> s & 1u)
+                        mbar_wait(smem_u32(&bars->lastfull[s]), stage_parity(par_last, s) ^ 1u, status,
+                                  &no_abort);
+                    else if (leader)
+                        mbar_wait(smem_u32(&bars->full[s]), stage_parity(par_full, s) ^ 1u, status,
+                                  &no_abort);
+                }
+            }
+            // the leader's MMAs read this CTA's stages: wait until every use
+            // of every stage has been released before leaving
+            for (int s = 0; s < P_STAGES; ++s) {
+                const int uses = issued / P_STAGES + (s < issued % P_STAGES ? 1 : 0);
+                if (uses > 0)
+                    mbar_wait(smem_u32(&bars->empty[s]), (uint32_t)((uses - 1) & 1), status, abort);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------- MMA issuer (leader)
+        if (leader && lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32_major(PM, MMA_N, 1, 1);
+            int stage = 0;
+            uint32_t par_full = 0, par_ready = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (int g = unit0; g < total && ok; g += units) {
+                const Tile t = map_wgrad_tile(g, p);
+                const int cnt = p.count[t.e];
+                const int nk = k_blocks<MODE>(p, cnt);
+                if (!mbar_wait(smem_u32(&bars->tempty[acc]), acc_phase ^ 1, status, abort)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * ACC_COLS);
+                for (int kb = 0; kb < nk; ++kb) {
+                    int steps = BK / 16;
+                    bool got;
+                    if (kb == nk - 1) {
+                        steps = (cnt - kb * BK + 15) / 16;
+                        got = mbar_wait(smem_u32(&bars->ready[stage]), stage_parity(par_ready, stage),
+                                        status, abort);
+                        par_ready ^= 1u << stage;
+                    } else {
+                        got = mbar_wait(smem_u32(&bars->full[stage]), stage_parity(par_full, stage),
+                                        status, abort);
+                        par_full ^= 1u << stage;
+                    }
+                    if (!got) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + (size_t)stage * P_STAGE_BYTES);
+                    const uint32_t sb = sa + A_BYTES;
+                    for (int kk = 0; kk < steps; ++kk)
+                        tc_mma_bf16_pair(d_tmem, sw128_mnmajor_desc(sa + kk * 2048),
+                                         sw128_mnmajor_desc(sb + kk * 2048), idesc,
+                                         (kb | kk) != 0 ? 1u : 0u);
+                    tc_commit_pair(smem_u32(&bars->empty[stage]));
+                    if (++stage == P_STAGES) stage = 0;
+                }
+                if (!ok) break;
+                tc_commit_pair(smem_u32(&bars->tfull[acc]));
+                if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+            }
+        }
+    } else if (warp == WG_FIXER) {
+        // ------------------------------------- last k-block repair (both CTAs)
+        int kc = 0;  // k-blocks of the tiles before this one
+        uint32_t par_last = 0;
+        for (int g = unit0; g < total; g += units) {
+            const Tile t = map_wgrad_tile(g, p);
+            const int cnt = p.count[t.e];
+            const int nk = k_blocks<MODE>(p, cnt);
+            if (nk == 0) continue;
+            const int s = (kc + nk - 1) % P_STAGES;
+            kc += nk;
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->lastfull[s]),
+                                                   stage_parity(par_last, s), status, abort)))
+                break;
+            par_last ^= 1u << s;
+            const int rv = cnt - (nk - 1) * BK;  // valid rows, 1..64
+            const int r16 = (rv + 15) / 16 * 16;
+            if (rv < r16) {
+                // zero rows rv..r16-1 of this CTA's 4 MN-major blocks (2 of A, 2 of B)
+                uint8_t *base = smem + (size_t)s * P_STAGE_BYTES;
+                const int nrow = r16 - rv;
+                for (int i = lane; i < 4 * nrow * 8; i += 32) {
+                    const int blk = i / (nrow * 8), rr = i % (nrow * 8);
+                    const int row = rv + rr / 8, chunk = rr % 8;
+                    *reinterpret_cast<uint4 *>(base + blk * BLK + row * 128 + chunk * 16) =
+                        make_uint4(0, 0, 0, 0);
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(cluster_map(smem_u32(&bars->ready[s]), 0));
+        }
+    } else {
+        // --------------------------------------------------------- epilogue
+        const int quad = warp & 3;
+        const int half = (warp - 2) >> 2;  // which 128 of the 256 columns
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int g = unit0; g < total; g += units) {
+            const Tile t = map_wgrad_tile(g, p);
+            const int cnt = p.count[t.e];
+            if (!mbar_wait(smem_u32(&bars->tfull[acc]), acc_phase, status, abort)) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * ACC_COLS;
+            {
+                // weight gradient, fp32; an expert without rows gets zeros.
+                // Each 32 x 16 block goes through a padded shared-memory block so
+                // that a store instruction writes 64-byte row segments.
+                const bool up = MODE == WGRAD_GATEUP && t.m >= mt_half;
+                const int mbase = (up ? t.m - mt_half : t.m) * PM + (int)rank * BM + quad * 32;
+                const int mlim = MODE == WGRAD_DOWN ? p.d : p.h;
+                const int width = MODE == WGRAD_DOWN ? p.h : p.d;
+                float *out = (up ? p.fout1 : p.fout0) + (int64_t)t.e * mlim * width;
+                float *blk = stage_out + (warp - 2) * 32 * STG_LD;
+                for (int c = half * (MMA_N / 2); c < (half + 1) * (MMA_N / 2); c += 16) {
+                    uint32_t r0[16];
+                    tmem_ld16(tbase + c, r0);
+                    tmem_ld_wait();
+                    reg_fence(r0);
+                    const int col0 = t.n * MMA_N + c;
+                    if (col0 >= width) continue;  // warp-uniform
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        blk[lane * STG_LD + i] = cnt ? __uint_as_float(r0[i]) : 0.0f;
+                    __syncwarp();
+                    const int cq = (lane & 3) * 4;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int rr = j * 8 + (lane >> 2);
+                        const float *src = blk + rr * STG_LD + cq;
+                        const float4 v = make_float4(src[0], src[1], src[2], src[3]);
+                        if (mbase + rr < mlim)
+                            __stcs(reinterpret_cast<float4 *>(out + (int64_t)(mbase + rr) * width +
+                                                              col0 + cq),
+                                   v);
+                    }
+                    __syncwarp();
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(cluster_map(smem_u32(&bars->tempty[acc]), 0));
+            if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    }
+}
+
+template <int MODE>
+moe_status launch_wgrad_pair(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap &b0,
+                             const Params &p, int max_units, cudaStream_t st) {
+    static bool configured = false;
+    const size_t smem = smem_bytes_wgrad_pair();
+    if (!configured) {
+        if (cudaFuncSetAttribute(grouped_wgrad_pair<MODE>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        configured = true;
+    }
+    const int pairs = std::min(num_sms() / 2, std::max(max_units, 1));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(2 * pairs));
+    cfg.blockDim = dim3(WG_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, grouped_wgrad_pair<MODE>, a0, a1, b0, p) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return launch_status();
+}
+
 inline size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 }  // namespace
@@ -696,7 +784,7 @@ MOE_API moe_status moe_expert_ffn_backward(
                                                 align256((size_t)R * s->h * 2));
     const int64_t rows = std::min<int64_t>(R, (int64_t)s->T * s->K);
     const int row_tiles = (int)((rows + BM - 1) / BM + s->N);
-    const int wg_mt = 2 * ((s->h + BM - 1) / BM);
+    const int wg_mt = 2 * ((s->h + 2 * BM - 1) / (2 * BM));
 
     if (R == 0) {
         // no rows at all: every weight gradient is zero; run the wgrad launches
@@ -735,16 +823,16 @@ MOE_API moe_status moe_expert_ffn_backward(
     r = launch_dgrad_pair<DGRAD_DX>(dg_k, du_k, wg_mn, wu_mn, p, pair_tiles * p.ntn, stream);
     if (r != MOE_OK) return r;
     // dW_down = dY^T H
-    p.mtn = (s->d + BM - 1) / BM;
+    p.mtn = (s->d + 2 * BM - 1) / (2 * BM);
     p.ntn = (s->h + MMA_N - 1) / MMA_N;
     p.fout0 = dw_down;
     p.fout1 = nullptr;
-    r = launch_wgrad<WGRAD_DOWN>(dy_mn, dy_mn, h_mn, h_mn, p, s->N * p.mtn * p.ntn, stream);
+    r = launch_wgrad_pair<WGRAD_DOWN>(dy_mn, dy_mn, h_mn, p, s->N * p.mtn * p.ntn, stream);
     if (r != MOE_OK) return r;
     // dW_gate = dG^T X, dW_up = dU^T X
     p.mtn = wg_mt;
     p.ntn = (s->d + MMA_N - 1) / MMA_N;
     p.fout0 = dw_gate;
     p.fout1 = dw_up;
-    return launch_wgrad<WGRAD_GATEUP>(dg_mn, du_mn, x_mn, x_mn, p, s->N * p.mtn * p.ntn, stream);
+    return launch_wgrad_pair<WGRAD_GATEUP>(dg_mn, du_mn, x_mn, p, s->N * p.mtn * p.ntn, stream);
 }

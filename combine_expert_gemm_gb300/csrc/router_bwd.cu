@@ -25,7 +25,7 @@
 //                  per lane, paired fp32 FMAs).  A chunk's partial dW_r /
 //                  dbias goes to the workspace (straight to the output when
 //                  there is one chunk).
-//   router_dw_sum  sums the chunk partials in chunk order.
+//   router_dw_sum  sums the chunk partials in a fixed order.
 #include "moe_common.cuh"
 
 namespace moe {
@@ -244,33 +244,54 @@ router_dw_tile(int T, int d, int N, int K, int nchunk, const uint16_t *__restric
     }
 }
 
-// dw[e, j] = sum over chunks c ascending of pdw[c][e, j]; dbias likewise.
-__global__ void __launch_bounds__(256)
+// dw[e, j] = sum over chunks of pdw[c][e, j]; dbias likewise.  A block covers
+// 32 float4 positions; its 8 warps each sum a fixed run of chunks (c = g,
+// g + 8, ...) and warp 0 adds the 8 runs in order: a fixed order, with 8
+// times the loads in flight of a thread-per-position loop.
+constexpr int RS_GROUPS = 8;
+
+__global__ void __launch_bounds__(32 * RS_GROUPS)
 router_dw_sum(int64_t n4, int N, int nchunk, const float4 *__restrict__ pdw,
               const float *__restrict__ pdb, float4 *__restrict__ dw, float *__restrict__ dbias) {
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    __shared__ float4 part[RS_GROUPS][32];
+    __shared__ float bpart[RS_GROUPS][32];
+    const int lane = threadIdx.x & 31, g = threadIdx.x >> 5;
+    const int64_t i = (int64_t)blockIdx.x * 32 + lane;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    float b = 0.f;
     if (i < n4) {
-        float4 a = pdw[i];
-        int c = 1;
-        for (; c + 8 <= nchunk; c += 8) {
-            float4 v[8];
+        int c = g;
+        for (; c + 3 * RS_GROUPS < nchunk; c += 4 * RS_GROUPS) {
+            float4 v[4];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) v[u] = __ldcs(pdw + (int64_t)(c + u) * n4 + i);
+            for (int u = 0; u < 4; ++u) v[u] = __ldcs(pdw + (int64_t)(c + u * RS_GROUPS) * n4 + i);
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
+            for (int u = 0; u < 4; ++u) {
                 a.x += v[u].x; a.y += v[u].y; a.z += v[u].z; a.w += v[u].w;
             }
         }
-        for (; c < nchunk; ++c) {
+        for (; c < nchunk; c += RS_GROUPS) {
             const float4 v = __ldcs(pdw + (int64_t)c * n4 + i);
             a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
         }
-        dw[i] = a;
     }
-    if (dbias && i < N) {
-        float b = pdb[i];
-        for (int c = 1; c < nchunk; ++c) b += pdb[(int64_t)c * N + i];
-        dbias[i] = b;
+    const bool bias_here = dbias && i < N;
+    if (bias_here)
+        for (int c = g; c < nchunk; c += RS_GROUPS) b += pdb[(int64_t)c * N + i];
+    part[g][lane] = a;
+    bpart[g][lane] = b;
+    __syncthreads();
+    if (g == 0) {
+        float4 s4 = part[0][lane];
+        float sb = bpart[0][lane];
+#pragma unroll
+        for (int q = 1; q < RS_GROUPS; ++q) {
+            const float4 v = part[q][lane];
+            s4.x += v.x; s4.y += v.y; s4.z += v.z; s4.w += v.w;
+            sb += bpart[q][lane];
+        }
+        if (i < n4) dw[i] = s4;
+        if (bias_here) dbias[i] = sb;
     }
 }
 
@@ -301,8 +322,8 @@ moe_status launch_router_dw(const moe_shape *s, const moe_bf16 *x, const int32_t
     moe_status r = launch_status();
     if (r != MOE_OK || C == 1) return r;
     const int64_t n4 = (int64_t)s->N * s->d / 4;
-    const int64_t blocks = (std::max<int64_t>(n4, s->N) + 255) / 256;
-    router_dw_sum<<<(unsigned)blocks, 256, 0, stream>>>(n4, s->N, C,
+    const int64_t blocks = (std::max<int64_t>(n4, s->N) + 31) / 32;
+    router_dw_sum<<<(unsigned)blocks, 32 * RS_GROUPS, 0, stream>>>(n4, s->N, C,
                                                         reinterpret_cast<const float4 *>(pdw), pdb,
                                                         reinterpret_cast<float4 *>(dw_router), dbias);
     return launch_status();

@@ -76,8 +76,9 @@ typedef struct {
 
 /* Rows R of every capacity buffer (x_disp, h_act, g_save, u_save, y_disp,
  * dy_disp, dx_disp) for this shape: min(N * cap, T * K); -1 if the shape is
- * invalid.  The packed layout ([EP] "Padded tiles and device offsets": experts
- * back to back at cumulative offsets) never places a row at or past it. */
+ * invalid.  The packed layout (Section 05, 5.7: experts back to back in a
+ * dense prefix; Section 08, 8.5 and Table 14: int32 cumulative offsets on the
+ * device) never places a row at or past it. */
 int64_t moe_buffer_rows(const moe_shape *s);
 
 /* Human-readable name of a status code (static string). */
@@ -274,7 +275,7 @@ size_t moe_router_backward_workspace_bytes(const moe_shape *s);
  *   NULL.  fp32 arithmetic: dot is a fused multiply-add chain over k
  *   ascending; the dx term is summed over k ascending and then added; dW_r is
  *   summed per expert in token order within fixed 128-token chunks, the
- *   chunk sums added in chunk order (deterministic, bit-identical run to run).
+ *   chunk sums added in a fixed order (deterministic, bit-identical run to run).
  * Errors: MOE_ERR_INVALID_ARG for null required pointers; MOE_ERR_ALIGNMENT;
  * MOE_ERR_WORKSPACE if ws is short or not 256-byte aligned;
  * MOE_ERR_UNSUPPORTED if N and K need more than 227 KB of shared memory.
