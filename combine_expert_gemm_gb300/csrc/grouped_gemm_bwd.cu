@@ -430,11 +430,13 @@ moe_status launch_dgrad_pair(const CUtensorMap &a0, const CUtensorMap &a1, const
 // while the leader is still busy with the tile's earlier k-blocks, so the
 // repair stays off the MMA issue path.  Stage barriers alternate between the
 // two kinds of use, so each role tracks their phases per stage.
+constexpr int WG_STAGES = 6;
+
 struct alignas(8) WgradBars {
-    uint64_t full[P_STAGES];      // leader: both CTAs' copies of a k-block landed
-    uint64_t lastfull[P_STAGES];  // this CTA's copy of a tile's last k-block landed
-    uint64_t ready[P_STAGES];     // leader: both fixers repaired a last k-block
-    uint64_t empty[P_STAGES];     // the leader's MMAs are done with the stage
+    uint64_t full[WG_STAGES];      // leader: both CTAs' copies of a k-block landed
+    uint64_t lastfull[WG_STAGES];  // this CTA's copy of a tile's last k-block landed
+    uint64_t ready[WG_STAGES];     // leader: both fixers repaired a last k-block
+    uint64_t empty[WG_STAGES];     // the leader's MMAs are done with the stage
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint32_t tmem_base;
@@ -444,8 +446,10 @@ struct alignas(8) WgradBars {
 constexpr int WG_THREADS = 64 + kEpiThreads + 32;  // + the fixer warp
 constexpr int WG_FIXER = 2 + P_EPI_WARPS;          // its warp index
 
+constexpr int WG_STG_BYTES = P_EPI_WARPS * 32 * 32 * 4;  // one 32 x 32 fp32 block per warp
+
 constexpr size_t smem_bytes_wgrad_pair() {
-    return 1024 + (size_t)P_STAGES * P_STAGE_BYTES + STG_BYTES + sizeof(WgradBars) + 16;
+    return 1024 + (size_t)WG_STAGES * P_STAGE_BYTES + WG_STG_BYTES + sizeof(WgradBars) + 16;
 }
 
 __device__ __forceinline__ uint32_t stage_parity(uint32_t bits, int s) { return (bits >> s) & 1u; }
@@ -453,15 +457,16 @@ __device__ __forceinline__ uint32_t stage_parity(uint32_t bits, int s) { return 
 template <int MODE>
 __global__ void __launch_bounds__(WG_THREADS, 1)
 grouped_wgrad_pair(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
-                   const __grid_constant__ CUtensorMap tm_b0, const Params p) {
+                   const __grid_constant__ CUtensorMap tm_b0, const __grid_constant__ CUtensorMap tm_o0,
+                   const __grid_constant__ CUtensorMap tm_o1, const Params p) {
     static_assert(MODE == WGRAD_DOWN || MODE == WGRAD_GATEUP, "wgrad only");
     constexpr int PM = 2 * BM;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    float *stage_out = reinterpret_cast<float *>(smem + (size_t)P_STAGES * P_STAGE_BYTES);
+    uint8_t *stage_out = smem + (size_t)WG_STAGES * P_STAGE_BYTES;
     WgradBars *bars =
-        reinterpret_cast<WgradBars *>(smem + (size_t)P_STAGES * P_STAGE_BYTES + STG_BYTES);
+        reinterpret_cast<WgradBars *>(smem + (size_t)WG_STAGES * P_STAGE_BYTES + WG_STG_BYTES);
     volatile int *abort = &bars->abort;
     int *status = p.status;
     const uint32_t rank = cluster_rank();
@@ -470,7 +475,7 @@ grouped_wgrad_pair(const __grid_constant__ CUtensorMap tm_a0, const __grid_const
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < P_STAGES; ++s) {
+        for (int s = 0; s < WG_STAGES; ++s) {
             mbar_init(smem_u32(&bars->full[s]), 1);
             mbar_init(smem_u32(&bars->lastfull[s]), 1);
             mbar_init(smem_u32(&bars->ready[s]), 2);
@@ -539,14 +544,14 @@ grouped_wgrad_pair(const __grid_constant__ CUtensorMap tm_a0, const __grid_const
                         last_kind &= ~(1u << stage);
                     }
                     ++issued;
-                    if (++stage == P_STAGES) { stage = 0; phase ^= 1; }
+                    if (++stage == WG_STAGES) { stage = 0; phase ^= 1; }
                 }
             }
             if (!ok) {
                 // let the copies already issued land before the CTA leaves: the
                 // latest use of each stage completes on its own barrier (a last
                 // k-block) or on the leader's full barrier (the leader waits)
-                for (int s = 0; s < P_STAGES && s < issued; ++s) {
+                for (int s = 0; s < WG_STAGES && s < issued; ++s) {
                     volatile int no_abort = 0;
                     if (last_kind >> s & 1u)
                         mbar_wait(smem_u32(&bars->lastfull[s]), stage_parity(par_last, s) ^ 1u, status,
@@ -558,8 +563,8 @@ grouped_wgrad_pair(const __grid_constant__ CUtensorMap tm_a0, const __grid_const
             }
             // the leader's MMAs read this CTA's stages: wait until every use
             // of every stage has been released before leaving
-            for (int s = 0; s < P_STAGES; ++s) {
-                const int uses = issued / P_STAGES + (s < issued % P_STAGES ? 1 : 0);
+            for (int s = 0; s < WG_STAGES; ++s) {
+                const int uses = issued / WG_STAGES + (s < issued % WG_STAGES ? 1 : 0);
                 if (uses > 0)
                     mbar_wait(smem_u32(&bars->empty[s]), (uint32_t)((uses - 1) & 1), status, abort);
             }
@@ -605,7 +610,7 @@ grouped_wgrad_pair(const __grid_constant__ CUtensorMap tm_a0, const __grid_const
                                          sw128_mnmajor_desc(sb + kk * 2048), idesc,
                                          (kb | kk) != 0 ? 1u : 0u);
                     tc_commit_pair(smem_u32(&bars->empty[stage]));
-                    if (++stage == P_STAGES) stage = 0;
+                    if (++stage == WG_STAGES) stage = 0;
                 }
                 if (!ok) break;
                 tc_commit_pair(smem_u32(&bars->tfull[acc]));
@@ -621,7 +626,7 @@ grouped_wgrad_pair(const __grid_constant__ CUtensorMap tm_a0, const __grid_const
             const int cnt = p.count[t.e];
             const int nk = k_blocks<MODE>(p, cnt);
             if (nk == 0) continue;
-            const int s = (kc + nk - 1) % P_STAGES;
+            const int s = (kc + nk - 1) % WG_STAGES;
             kc += nk;
             if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->lastfull[s]),
                                                    stage_parity(par_last, s), status, abort)))
@@ -657,38 +662,42 @@ grouped_wgrad_pair(const __grid_constant__ CUtensorMap tm_a0, const __grid_const
             tc_fence_after();
             const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * ACC_COLS;
             {
-                // weight gradient, fp32; an expert without rows gets zeros.
-                // Each 32 x 16 block goes through a padded shared-memory block so
-                // that a store instruction writes 64-byte row segments.
+                // weight gradient, fp32; an expert without rows gets zeros.  Each
+                // 32 x 32 block is written to this warp's shared-memory block in
+                // the 128-byte swizzled layout and stored by one TMA instruction
+                // (rows past the matrix are clipped by the map).
                 const bool up = MODE == WGRAD_GATEUP && t.m >= mt_half;
                 const int mbase = (up ? t.m - mt_half : t.m) * PM + (int)rank * BM + quad * 32;
-                const int mlim = MODE == WGRAD_DOWN ? p.d : p.h;
                 const int width = MODE == WGRAD_DOWN ? p.h : p.d;
-                float *out = (up ? p.fout1 : p.fout0) + (int64_t)t.e * mlim * width;
-                float *blk = stage_out + (warp - 2) * 32 * STG_LD;
-                for (int c = half * (MMA_N / 2); c < (half + 1) * (MMA_N / 2); c += 16) {
-                    uint32_t r0[16];
+                const int mlim = MODE == WGRAD_DOWN ? p.d : p.h;
+                const CUtensorMap *om = up ? &tm_o1 : &tm_o0;
+                uint8_t *blk = stage_out + (warp - 2) * 4096;
+                const uint32_t blk_s = smem_u32(blk);
+                for (int c = half * (MMA_N / 2); c < (half + 1) * (MMA_N / 2); c += 32) {
+                    uint32_t r0[16], r1[16];
                     tmem_ld16(tbase + c, r0);
+                    tmem_ld16(tbase + c + 16, r1);
                     tmem_ld_wait();
                     reg_fence(r0);
+                    reg_fence(r1);
                     const int col0 = t.n * MMA_N + c;
-                    if (col0 >= width) continue;  // warp-uniform
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        blk[lane * STG_LD + i] = cnt ? __uint_as_float(r0[i]) : 0.0f;
+                    if (col0 >= width || mbase >= mlim) continue;  // warp-uniform
+                    // the previous store from this block has finished reading it
+                    if (lane == 0) bulk_wait_read<0>();
                     __syncwarp();
-                    const int cq = (lane & 3) * 4;
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int rr = j * 8 + (lane >> 2);
-                        const float *src = blk + rr * STG_LD + cq;
-                        const float4 v = make_float4(src[0], src[1], src[2], src[3]);
-                        if (mbase + rr < mlim)
-                            __stcs(reinterpret_cast<float4 *>(out + (int64_t)(mbase + rr) * width +
-                                                              col0 + cq),
-                                   v);
+                    for (int q = 0; q < 8; ++q) {
+                        const uint32_t *src = q < 4 ? &r0[4 * q] : &r1[4 * (q - 4)];
+                        const uint4 v = cnt ? make_uint4(src[0], src[1], src[2], src[3])
+                                            : make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4 *>(blk + lane * 128 + ((q ^ (lane & 7)) * 16)) = v;
                     }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     __syncwarp();
+                    if (lane == 0) {
+                        tma_store_3d(om, blk_s, col0, mbase, t.e);
+                        bulk_commit();
+                    }
                 }
             }
             tc_fence_before();
@@ -696,6 +705,7 @@ grouped_wgrad_pair(const __grid_constant__ CUtensorMap tm_a0, const __grid_const
             if (lane == 0) mbar_arrive_cluster(cluster_map(smem_u32(&bars->tempty[acc]), 0));
             if (++acc == 2) { acc = 0; acc_phase ^= 1; }
         }
+        if (lane == 0) bulk_wait<0>();  // stores complete before the CTA ends
     }
 
     tc_fence_before();
@@ -709,7 +719,8 @@ grouped_wgrad_pair(const __grid_constant__ CUtensorMap tm_a0, const __grid_const
 
 template <int MODE>
 moe_status launch_wgrad_pair(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap &b0,
-                             const Params &p, int max_units, cudaStream_t st) {
+                             const CUtensorMap &o0, const CUtensorMap &o1, const Params &p,
+                             int max_units, cudaStream_t st) {
     static bool configured = false;
     const size_t smem = smem_bytes_wgrad_pair();
     if (!configured) {
@@ -731,7 +742,7 @@ moe_status launch_wgrad_pair(const CUtensorMap &a0, const CUtensorMap &a1, const
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, grouped_wgrad_pair<MODE>, a0, a1, b0, p) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, grouped_wgrad_pair<MODE>, a0, a1, b0, o0, o1, p) != cudaSuccess)
         return MOE_ERR_CUDA;
     return launch_status();
 }
@@ -806,6 +817,11 @@ MOE_API moe_status moe_expert_ffn_backward(
         !make_map(&dg_mn, dG, s->h, R, 64) || !make_map(&du_mn, dU, s->h, R, 64) ||
         !make_map(&x_mn, x_disp, s->d, R, 64))
         return MOE_ERR_CUDA;
+    CUtensorMap o_down, o_gate, o_up;
+    if (!make_map_f32_3d(&o_down, dw_down, s->h, s->d, s->N) ||
+        !make_map_f32_3d(&o_gate, dw_gate, s->d, s->h, s->N) ||
+        !make_map_f32_3d(&o_up, dw_up, s->d, s->h, s->N))
+        return MOE_ERR_CUDA;
 
     // dH = dY W_down, then dG, dU
     p.ntn = (s->h + MMA_N - 1) / MMA_N;
@@ -827,12 +843,14 @@ MOE_API moe_status moe_expert_ffn_backward(
     p.ntn = (s->h + MMA_N - 1) / MMA_N;
     p.fout0 = dw_down;
     p.fout1 = nullptr;
-    r = launch_wgrad_pair<WGRAD_DOWN>(dy_mn, dy_mn, h_mn, p, s->N * p.mtn * p.ntn, stream);
+    r = launch_wgrad_pair<WGRAD_DOWN>(dy_mn, dy_mn, h_mn, o_down, o_down, p, s->N * p.mtn * p.ntn,
+                                      stream);
     if (r != MOE_OK) return r;
     // dW_gate = dG^T X, dW_up = dU^T X
     p.mtn = wg_mt;
     p.ntn = (s->d + MMA_N - 1) / MMA_N;
     p.fout0 = dw_gate;
     p.fout1 = dw_up;
-    return launch_wgrad_pair<WGRAD_GATEUP>(dg_mn, du_mn, x_mn, p, s->N * p.mtn * p.ntn, stream);
+    return launch_wgrad_pair<WGRAD_GATEUP>(dg_mn, du_mn, x_mn, o_gate, o_up, p,
+                                           s->N * p.mtn * p.ntn, stream);
 }
