@@ -185,6 +185,36 @@ def test_logits_exact_on_integers_and_error_bound():
     bound = 512 * 2.0 ** -24 * (np.abs(xf) @ np.abs(w.astype(np.float64)).T)
     assert np.all(np.abs(got - exact) <= bound)
 
+    # d = 2000 (four blocks, the last ragged): within (512 + 4) u sum|x w|
+    x = synth.normal_bf16(13, (T, 2000))
+    w = synth.normal_f32(14, (N, 2000), 0.02)
+    got = oracle.router_logits(x, w).astype(np.float64)
+    xf = oracle.bf16_to_f32(x).astype(np.float64)
+    exact = np.array([[math.fsum(xf[t] * w[e].astype(np.float64)) for e in range(N)]
+                      for t in range(T)])
+    bound = 516 * 2.0 ** -24 * (np.abs(xf) @ np.abs(w.astype(np.float64)).T)
+    assert np.all(np.abs(got - exact) <= bound)
+
+
+def test_logits_blocks_of_512():
+    """The reading of the logit order: one fp32 chain per 512-wide block of j,
+    block sums added in order.  Block 0 holds a single product 2^24 and block
+    1 holds 512 unit products: the blocked sum is the exact 2^24 + 512, which
+    one chain over all j would lose (each +1 onto 2^24 rounds back to even)."""
+    d = 1024
+    x = np.zeros((1, d), np.float32)
+    w = np.zeros((1, d), np.float32)
+    x[0, 7], w[0, 7] = 4096.0, 4096.0
+    x[0, 512:], w[0, 512:] = 1.0, 1.0
+    got = oracle.router_logits(synth.f32_to_bf16_bits(x), w)
+    assert got[0, 0] == np.float32(2.0 ** 24 + 512)
+    # the same products inside one block meet 2^24 one at a time
+    x2 = np.zeros((1, 512), np.float32)
+    w2 = np.zeros((1, 512), np.float32)
+    x2[0, 0], w2[0, 0] = 4096.0, 4096.0
+    x2[0, 1:], w2[0, 1:] = 1.0, 1.0
+    assert oracle.router_logits(synth.f32_to_bf16_bits(x2), w2)[0, 0] == np.float32(2.0 ** 24)
+
 
 def _brute_slots(idx, N, cap):
     T, K = idx.shape
