@@ -10,9 +10,10 @@
 //
 // Four launches, none of which waits on another CTA:
 //   1. route_logits_topk: per tile of tokens, fp32 logits for all experts in
-//      shared memory (one fused multiply-add chain over j ascending per
-//      logit, so the values are reproducible bit for bit), then one warp per
-//      token selects the top K and computes the gates.
+//      shared memory (per 512-wide block of j one fused multiply-add chain
+//      over j ascending, the block sums added in block order, so the values
+//      are reproducible bit for bit), then one thread per token selects the
+//      top K and computes the gates.
 //   2. route_block_rank: per block of 256 tokens, a per-warp bitmask of the
 //      tokens choosing each expert gives every route its rank among earlier
 //      routes to the same expert inside the block, and the block's count per
@@ -37,43 +38,51 @@ __device__ __forceinline__ bool beats(float a, int ia, float b, int ib) {
     return a > b || (a == b && ia < ib);
 }
 
-// Logit tile: TB tokens x EC experts per pass, 512 threads (16 warps), each
-// thread 2 tokens x 4 experts (8 independent fma chains).  A warp covers 8
-// tokens x 32 experts: lane = (tx in 0..7, ty in 0..3); the thread owns tokens
-// ty + 4a and experts tx + 8b of its warp's block.  x (bf16) and W_r (fp32)
-// stream through a 3-stage cp.async ring of j-chunks in their natural
-// row-major layouts; a thread reads 8 consecutive j of a row with one 16-byte
-// load (distinct banks across the warp), so every chain still runs over j in
-// ascending order.
-constexpr int kLogitThreads = 512;
-constexpr int kLogitStages = 3;
+// Logit tile: WT x WE warps; a warp covers 16 tokens x 32 experts, each lane
+// 4 tokens x 4 experts (16 independent fma chains, advanced in pairs by packed
+// fp32x2 fma): lane = tx + 8 ty (tx in 0..7, ty in 0..3) owns tokens ty + 4a
+// and experts tx + 8b of its warp's block.  A CTA covers TB = 16 WT tokens and
+// EC = 32 WE experts per pass (passes loop over the experts).  The dot product
+// over j is cut into 512-wide blocks: each chain restarts from 0 at a block
+// boundary and the block sums are added in block order (the order the logits
+// are defined by).  x (bf16) and W_r (fp32) stream through a 4-stage cp.async
+// ring of 32-wide j-chunks in their natural row-major layouts; per 4 j a lane
+// reads 8 bytes of each of its x rows and 16 bytes of each of its W rows (rows
+// padded so that the 8 distinct rows of a warp load hit distinct banks).
+constexpr int kLogitStages = 4;
+constexpr int kLogitJC = 32;
+constexpr int kLogitBlock = 512;  // j per block sum (a multiple of kLogitJC)
 
-template <int TB, int EC>
+template <int WT, int WE>
 struct LogitTile {
-    static constexpr int JC = EC >= 128 ? 32 : 64;  // j per stage
-    static constexpr int XR = JC + 8;               // bf16 per padded x row
-    static constexpr int WR = JC + 4;               // fp32 per padded W row
+    static constexpr int THREADS = 32 * WT * WE;
+    static constexpr int TB = 16 * WT;
+    static constexpr int EC = 32 * WE;
+    static constexpr int XR = kLogitJC + 8;  // bf16 per padded x row
+    static constexpr int WR = kLogitJC + 4;  // fp32 per padded W row
     static constexpr int STAGE = TB * XR * 2 + EC * WR * 4;  // bytes
     static constexpr size_t smem_bytes(int N) {
-        return (size_t)kLogitStages * STAGE + sizeof(float) * (size_t)TB * N;
+        return (size_t)kLogitStages * STAGE + sizeof(float) * (size_t)TB * (N + 1);
     }
 };
 
-template <int TB, int EC>
-__global__ void __launch_bounds__(kLogitThreads)
+template <int WT, int WE>
+__global__ void __launch_bounds__(LogitTile<WT, WE>::THREADS)
 route_logits_topk(int T, int d, int N, int K, const uint16_t *__restrict__ x,
                   const float *__restrict__ w_r, const float *__restrict__ bias,
                   int32_t *__restrict__ topk_idx, float *__restrict__ topk_gate) {
-    using L = LogitTile<TB, EC>;
-    constexpr int JC = L::JC, XR = L::XR, WR = L::WR;
-    static_assert((TB / 8) * (EC / 32) == kLogitThreads / 32, "warp tiling");
+    using L = LogitTile<WT, WE>;
+    constexpr int TB = L::TB, EC = L::EC, XR = L::XR, WR = L::WR, JC = kLogitJC;
+    constexpr int THREADS = L::THREADS;
+    constexpr int CPB = kLogitBlock / JC;  // chunks per block
     extern __shared__ __align__(16) uint8_t smem_l[];
-    float *lg = reinterpret_cast<float *>(smem_l + (size_t)kLogitStages * L::STAGE);  // [TB][N]
+    const int LDS = N + 1;  // padded logit row: one thread per token reads its row
+    float *lg = reinterpret_cast<float *>(smem_l + (size_t)kLogitStages * L::STAGE);  // [TB][LDS]
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int tx = lane & 7, ty = lane >> 3;
-    const int tok0 = (warp % (TB / 8)) * 8 + ty;   // + 4a
-    const int exp0 = (warp / (TB / 8)) * 32 + tx;  // + 8b
+    const int tok0 = (warp % WT) * 16 + ty;   // + 4a
+    const int exp0 = (warp / WT) * 32 + tx;   // + 8b
     const int t0 = blockIdx.x * TB;
     const int nchunks = (d + JC - 1) / JC;
 
@@ -84,12 +93,12 @@ route_logits_topk(int T, int d, int N, int K, const uint16_t *__restrict__ x,
                 uint16_t *xs = reinterpret_cast<uint16_t *>(st);
                 float *ws = reinterpret_cast<float *>(st + TB * XR * 2);
                 const int j0 = c * JC, jn = min(JC, d - j0);
-                for (int i = tid; i < TB * (JC / 8); i += kLogitThreads) {
+                for (int i = tid; i < TB * (JC / 8); i += THREADS) {
                     const int r = i / (JC / 8), q = (i % (JC / 8)) * 8;
                     if (t0 + r < T && q < jn)
                         cp_async16(xs + r * XR + q, x + (int64_t)(t0 + r) * d + j0 + q);
                 }
-                for (int i = tid; i < EC * (JC / 4); i += kLogitThreads) {
+                for (int i = tid; i < EC * (JC / 4); i += THREADS) {
                     const int r = i / (JC / 4), q = (i % (JC / 4)) * 4;
                     if (ec0 + r < N && q < jn)
                         cp_async16(ws + r * WR + q, w_r + (int64_t)(ec0 + r) * d + j0 + q);
@@ -98,101 +107,136 @@ route_logits_topk(int T, int d, int N, int K, const uint16_t *__restrict__ x,
             cp_async_commit();
         };
 
-        float acc[2][4];
+        // acc[ap][b] = the current block's chains (token 2ap, expert b) and
+        // (token 2ap + 1, expert b), advanced together by one paired fma;
+        // tot holds the sum of the finished blocks
+        float2 acc[2][4], tot[2][4];
 #pragma unroll
         for (int a = 0; a < 2; ++a)
 #pragma unroll
-            for (int b = 0; b < 4; ++b) acc[a][b] = 0.0f;
+            for (int q = 0; q < 4; ++q) {
+                acc[a][q] = make_float2(0.0f, 0.0f);
+                tot[a][q] = make_float2(0.0f, 0.0f);
+            }
+        auto fold = [&](bool first) {
+#pragma unroll
+            for (int a = 0; a < 2; ++a)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    tot[a][q] = first ? acc[a][q]
+                                      : make_float2(__fadd_rn(tot[a][q].x, acc[a][q].x),
+                                                    __fadd_rn(tot[a][q].y, acc[a][q].y));
+                    acc[a][q] = make_float2(0.0f, 0.0f);
+                }
+        };
 
         __syncthreads();  // the previous pass is done with every stage
 #pragma unroll
         for (int c = 0; c < kLogitStages - 1; ++c) issue(c);
         for (int c = 0; c < nchunks; ++c) {
+            if (c > 0 && c % CPB == 0) fold(c == CPB);  // a block boundary
             cp_async_wait<kLogitStages - 2>();
             __syncthreads();
             issue(c + kLogitStages - 1);
             const uint8_t *st = smem_l + (size_t)(c % kLogitStages) * L::STAGE;
             const uint16_t *xs = reinterpret_cast<const uint16_t *>(st) + tok0 * XR;
             const float *ws = reinterpret_cast<const float *>(st + TB * XR * 2) + exp0 * WR;
-            const int jn = min(JC, d - c * JC);
-#pragma unroll 2
-            for (int j = 0; j < jn; j += 8) {
-                float xf[2][8];
+            const int jn = min(JC, d - c * JC);  // a multiple of 8
+#pragma unroll 4
+            for (int j = 0; j < jn; j += 4) {
+                // xp[ap][q] = (x of token 2ap, x of token 2ap + 1) at j + q
+                float2 xp[2][4];
 #pragma unroll
-                for (int a = 0; a < 2; ++a) {
-                    const uint4 v = *reinterpret_cast<const uint4 *>(xs + 4 * a * XR + j);
-                    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+                for (int ap = 0; ap < 2; ++ap) {
+                    const uint2 v0 = *reinterpret_cast<const uint2 *>(xs + 8 * ap * XR + j);
+                    const uint2 v1 = *reinterpret_cast<const uint2 *>(xs + (8 * ap + 4) * XR + j);
+                    xp[ap][0] = make_float2(bf16_lo(v0.x), bf16_lo(v1.x));
+                    xp[ap][1] = make_float2(bf16_hi(v0.x), bf16_hi(v1.x));
+                    xp[ap][2] = make_float2(bf16_lo(v0.y), bf16_lo(v1.y));
+                    xp[ap][3] = make_float2(bf16_hi(v0.y), bf16_hi(v1.y));
+                }
+                float4 wf[4];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        xf[a][2 * q] = bf16_lo(w4[q]);
-                        xf[a][2 * q + 1] = bf16_hi(w4[q]);
+                for (int q = 0; q < 4; ++q)
+                    wf[q] = *reinterpret_cast<const float4 *>(ws + 8 * q * WR + j);
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+#pragma unroll
+                    for (int eb = 0; eb < 4; ++eb) {
+                        const float w = q == 0 ? wf[eb].x : q == 1 ? wf[eb].y : q == 2 ? wf[eb].z : wf[eb].w;
+                        const float2 w2 = make_float2(w, w);
+#pragma unroll
+                        for (int ap = 0; ap < 2; ++ap) acc[ap][eb] = __ffma2_rn(xp[ap][q], w2, acc[ap][eb]);
                     }
-                }
-                float wf[4][8];
-#pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                    const float *wrow = ws + 8 * b * WR + j;
-                    const float4 w0 = *reinterpret_cast<const float4 *>(wrow);
-                    const float4 w1 = *reinterpret_cast<const float4 *>(wrow + 4);
-                    wf[b][0] = w0.x; wf[b][1] = w0.y; wf[b][2] = w0.z; wf[b][3] = w0.w;
-                    wf[b][4] = w1.x; wf[b][5] = w1.y; wf[b][6] = w1.z; wf[b][7] = w1.w;
-                }
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-#pragma unroll
-                    for (int a = 0; a < 2; ++a)
-#pragma unroll
-                        for (int b = 0; b < 4; ++b)
-                            acc[a][b] = __fmaf_rn(xf[a][q], wf[b][q], acc[a][b]);
             }
         }
         cp_async_wait<0>();
+        fold(nchunks <= CPB);
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            const int e = ec0 + exp0 + 8 * b;
+        for (int eb = 0; eb < 4; ++eb) {
+            const int e = ec0 + exp0 + 8 * eb;
             if (e < N) {
                 const float bb = bias ? bias[e] : 0.0f;
 #pragma unroll
-                for (int a = 0; a < 2; ++a)
-                    lg[(tok0 + 4 * a) * N + e] = bias ? __fadd_rn(acc[a][b], bb) : acc[a][b];
+                for (int ap = 0; ap < 2; ++ap) {
+                    const float l0 = tot[ap][eb].x, l1 = tot[ap][eb].y;  // tokens 2ap, 2ap + 1
+                    lg[(tok0 + 8 * ap) * LDS + e] = bias ? __fadd_rn(l0, bb) : l0;
+                    lg[(tok0 + 8 * ap + 4) * LDS + e] = bias ? __fadd_rn(l1, bb) : l1;
+                }
             }
         }
     }
     __syncthreads();
 
-    // top-K and gates, one warp per token
-    for (int tt = warp; tt < TB; tt += kLogitThreads / 32) {
+    // top-K and gates, one thread per token: the logits stream past a
+    // sorted list of the best K so far (logit descending, lower expert first
+    // on ties, NaN as -inf); a logit that beats the K-th is swapped down into
+    // place.  The list sits at the end of a kMaxK-entry register array whose
+    // first kMaxK - K entries hold sentinels that nothing beats, so the K-th
+    // is always the last entry and every index is a constant.
+    for (int tt = tid; tt < TB; tt += THREADS) {
         const int t = t0 + tt;
         if (t >= T) break;
-        const float *l = lg + tt * N;
-        uint32_t taken = 0;  // bit q: expert lane + 32 q already chosen
-        int my_idx = 0;
-        float my_val = 0.0f, top = 0.0f, ex = 0.0f;
-        for (int k = 0; k < K; ++k) {
-            float bv = -INFINITY;
-            int bi = 0x7FFFFFFF;
-            for (int q = 0, e = lane; e < N; ++q, e += 32) {
-                if (taken & (1u << q)) continue;
-                const float v = canon(l[e]);
-                if (beats(v, e, bv, bi)) { bv = v; bi = e; }
-            }
+        const float *l = lg + tt * LDS;
+        const int first = kMaxK - K;
+        float tv[kMaxK];
+        int ti[kMaxK];
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, off);
-                const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, off);
-                if (beats(ov, oi, bv, bi)) { bv = ov; bi = oi; }
-            }
-            if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-            if (k == 0) top = bv;
-            if (lane == k) { my_idx = bi; my_val = bv; }
+        for (int q = 0; q < kMaxK; ++q) {
+            const bool real = q >= first;
+            tv[q] = real ? -INFINITY : INFINITY;
+            ti[q] = real ? 0x7FFFFFFF : -1;
         }
-        if (lane < K) ex = (my_val == top) ? 1.0f : expf(my_val - top);
-        float s = ex;
+        for (int e = 0; e < N; ++e) {
+            float v = canon(l[e]);
+            if (!beats(v, e, tv[kMaxK - 1], ti[kMaxK - 1])) continue;
+            int ie = e;
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, off);
-        if (lane < K) {
-            topk_idx[(int64_t)t * K + lane] = my_idx;
-            topk_gate[(int64_t)t * K + lane] = ex / s;
+            for (int q = 0; q < kMaxK; ++q) {
+                const bool sw = beats(v, ie, tv[q], ti[q]);
+                const float sv = tv[q];
+                const int si = ti[q];
+                tv[q] = sw ? v : sv;
+                ti[q] = sw ? ie : si;
+                v = sw ? sv : v;
+                ie = sw ? si : ie;
+            }
+        }
+        float top = 0.0f;
+#pragma unroll
+        for (int q = 0; q < kMaxK; ++q)
+            if (q == first) top = tv[q];
+        float sum = 0.0f;
+#pragma unroll
+        for (int q = 0; q < kMaxK; ++q)
+            if (q >= first) sum += (tv[q] == top) ? 1.0f : expf(tv[q] - top);
+#pragma unroll
+        for (int q = 0; q < kMaxK; ++q) {
+            if (q >= first) {
+                const float ex = (tv[q] == top) ? 1.0f : expf(tv[q] - top);
+                topk_idx[(int64_t)t * K + (q - first)] = ti[q];
+                topk_gate[(int64_t)t * K + (q - first)] = ex / sum;
+            }
         }
     }
 }
@@ -304,21 +348,22 @@ __global__ void route_assign(int T, int N, int K, int cap, const int32_t *__rest
     route_row[i] = slot < cap ? expert_offset[e] + slot : -1;
 }
 
-template <int TB, int EC>
+template <int WT, int WE>
 moe_status launch_logits(const moe_shape *s, const uint16_t *x, const float *w, const float *b,
                          int32_t *idx, float *gate, cudaStream_t st) {
-    const size_t smem = LogitTile<TB, EC>::smem_bytes(s->N);
+    using L = LogitTile<WT, WE>;
+    const size_t smem = L::smem_bytes(s->N);
     static size_t configured = 0;
     if (smem > 48 * 1024 && smem > configured) {
-        if (cudaFuncSetAttribute(route_logits_topk<TB, EC>,
+        if (cudaFuncSetAttribute(route_logits_topk<WT, WE>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem) != cudaSuccess)
             return MOE_ERR_CUDA;
         configured = smem;
     }
-    const int grid = (s->T + TB - 1) / TB;
-    route_logits_topk<TB, EC><<<grid, kLogitThreads, smem, st>>>(s->T, s->d, s->N, s->K, x, w, b, idx,
-                                                             gate);
+    const int grid = (s->T + L::TB - 1) / L::TB;
+    route_logits_topk<WT, WE><<<grid, L::THREADS, smem, st>>>(s->T, s->d, s->N, s->K, x, w, b, idx,
+                                                              gate);
     return launch_status();
 }
 
@@ -340,9 +385,9 @@ moe_status route_enqueue(const moe_shape *s, const moe_bf16 *x, const float *w_r
     moe_status r = MOE_OK;
     if (s->T > 0) {
         const int n = s->N;
-        if (n <= 32) r = launch_logits<128, 32>(s, x, w_router, bias, topk_idx, topk_gate, st);
-        else if (n <= 64) r = launch_logits<64, 64>(s, x, w_router, bias, topk_idx, topk_gate, st);
-        else r = launch_logits<32, 128>(s, x, w_router, bias, topk_idx, topk_gate, st);
+        if (n <= 32) r = launch_logits<2, 1>(s, x, w_router, bias, topk_idx, topk_gate, st);
+        else if (n <= 64) r = launch_logits<2, 2>(s, x, w_router, bias, topk_idx, topk_gate, st);
+        else r = launch_logits<2, 4>(s, x, w_router, bias, topk_idx, topk_gate, st);
         if (r != MOE_OK) return r;
         const size_t smem = sizeof(uint32_t) * 2 * (kRankBlock / 32) * (size_t)s->N;
         static bool configured = false;

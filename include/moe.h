@@ -110,8 +110,10 @@ size_t moe_route_workspace_bytes(const moe_shape *s);
  *                capacity decision); dropped = sum(demand - count).
  *   ws, ws_bytes device workspace of at least moe_route_workspace_bytes(s)
  *                bytes, 256-byte aligned; word 0 is the device status word.
- * Logits are fp32, one fused multiply-add chain over j ascending per (t, e),
- * then + bias, so top-K decisions are reproducible bit for bit.
+ * Logits are fp32: per 512-wide block of j one fused multiply-add chain over
+ * j ascending, the block sums added in block order, then + bias (the pages
+ * fix no order; this one is fixed, so top-K decisions are reproducible bit for
+ * bit).
  */
 moe_status moe_route(const moe_shape *s, const moe_bf16 *x, const float *w_router,
                      const float *bias, int32_t *topk_idx, float *topk_gate, int32_t *route_row,
