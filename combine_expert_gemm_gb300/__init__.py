@@ -68,6 +68,8 @@ _SIG = {
     "moe_buffer_rows": ([_SP], ctypes.c_int64),
     "moe_dispatch_router_backward": ([_SP] + [_P] * 8 + [_P], ctypes.c_int),
     "moe_router_weight_backward": ([_SP] + [_P] * 5 + [_P, _SZ, _P], ctypes.c_int),
+    "moe_expert_ffn_gather_workspace_bytes": ([_SP], _SZ),
+    "moe_expert_ffn_gather": ([_SP] + [_P] * 11 + [_P, _SZ, _P], ctypes.c_int),
 }
 for _name, (_args, _res) in _SIG.items():
     _f = getattr(_lib, _name)
@@ -151,6 +153,25 @@ def expert_ffn(shape, x_disp, expert_count, expert_offset, w_gate, w_up, w_down,
                                _ptr(g_save, _bf16, "g_save"), _ptr(u_save, _bf16, "u_save"),
                                _ptr(y_disp, _bf16, "y_disp"), _ptr(ws, None, "ws"),
                                ws.numel() * ws.element_size(), _stream(stream)), "moe_expert_ffn")
+
+
+def expert_ffn_gather_workspace_bytes(shape):
+    return int(_lib.moe_expert_ffn_gather_workspace_bytes(ctypes.byref(shape)))
+
+
+def expert_ffn_gather(shape, x, route_row, expert_count, expert_offset, w_gate, w_up, w_down, h_act,
+                      g_save, u_save, y_disp, ws, stream=None):
+    """Dispatch fused into the grouped SwiGLU experts: x rows are fetched by route (include/moe.h)."""
+    _check(_lib.moe_expert_ffn_gather(ctypes.byref(shape), _ptr(x, _bf16, "x"),
+                                      _ptr(route_row, _i32, "route_row"),
+                                      _ptr(expert_count, _i32, "expert_count"),
+                                      _ptr(expert_offset, _i32, "expert_offset"),
+                                      _ptr(w_gate, _bf16, "w_gate"), _ptr(w_up, _bf16, "w_up"),
+                                      _ptr(w_down, _bf16, "w_down"), _ptr(h_act, _bf16, "h_act"),
+                                      _ptr(g_save, _bf16, "g_save"), _ptr(u_save, _bf16, "u_save"),
+                                      _ptr(y_disp, _bf16, "y_disp"), _ptr(ws, None, "ws"),
+                                      ws.numel() * ws.element_size(), _stream(stream)),
+           "moe_expert_ffn_gather")
 
 
 def combine(shape, y_disp, route_row, topk_gate, y, stream=None):
@@ -258,6 +279,8 @@ class LayerBuffers:
         self.expert_demand = torch.empty(N, dtype=_i32, **e)
         self.route_ws = torch.zeros(max(route_workspace_bytes(shape), 256), dtype=torch.uint8, **e)
         self.ffn_ws = torch.zeros(max(expert_ffn_workspace_bytes(shape), 256), dtype=torch.uint8, **e)
+        self.gather_ws = torch.zeros(max(expert_ffn_gather_workspace_bytes(shape), 256),
+                                     dtype=torch.uint8, **e)
         self.x_disp = torch.empty((R, d), dtype=_bf16, **e)
         self.h_act = torch.empty((R, h), dtype=_bf16, **e)
         self.g_save = torch.empty((R, h), dtype=_bf16, **e) if save_for_backward else None
@@ -266,14 +289,21 @@ class LayerBuffers:
         self.y = torch.empty((T, d), dtype=_bf16, **e)
 
 
-def layer_forward(buf, x, w_router, bias, w_gate, w_up, w_down, stream=None):
-    """Route -> dispatch -> grouped SwiGLU experts -> combine into buf.y (4 C-ABI calls)."""
+def layer_forward(buf, x, w_router, bias, w_gate, w_up, w_down, stream=None, fused_dispatch=False):
+    """Route -> dispatch -> grouped SwiGLU experts -> combine into buf.y (4 C-ABI calls).
+    fused_dispatch: the experts fetch x rows by route instead (3 calls, no x_disp;
+    for a forward without backward)."""
     s = buf.shape
     route(s, x, w_router, bias, buf.topk_idx, buf.topk_gate, buf.route_row, buf.expert_count,
           buf.expert_offset, buf.expert_demand, buf.route_ws, stream)
-    dispatch(s, x, buf.route_row, buf.x_disp, stream)
-    expert_ffn(s, buf.x_disp, buf.expert_count, buf.expert_offset, w_gate, w_up, w_down,
-               buf.h_act, buf.g_save, buf.u_save, buf.y_disp, buf.ffn_ws, stream)
+    if fused_dispatch:
+        expert_ffn_gather(s, x, buf.route_row, buf.expert_count, buf.expert_offset, w_gate, w_up,
+                          w_down, buf.h_act, buf.g_save, buf.u_save, buf.y_disp, buf.gather_ws,
+                          stream)
+    else:
+        dispatch(s, x, buf.route_row, buf.x_disp, stream)
+        expert_ffn(s, buf.x_disp, buf.expert_count, buf.expert_offset, w_gate, w_up, w_down,
+                   buf.h_act, buf.g_save, buf.u_save, buf.y_disp, buf.ffn_ws, stream)
     combine(s, buf.y_disp, buf.route_row, buf.topk_gate, buf.y, stream)
     return buf.y
 

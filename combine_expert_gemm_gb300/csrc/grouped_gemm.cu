@@ -152,13 +152,18 @@ constexpr size_t smem_bytes_pair(int N) {
            16;
 }
 
-template <int EPI>
+// GATHER: A is not the packed buffer but the token rows themselves: the map
+// is over x [T, d] with a one-row box, and the producer fetches each packed
+// row r from x[row_token[r]] with tile::gather4 loads (four rows per load,
+// four producer lanes with 32 rows each).  Rows past the expert's count read
+// token 0; their accumulator rows are never stored.
+template <int EPI, bool GATHER>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_pair(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b0,
                   const __grid_constant__ CUtensorMap tm_b1, int N, int Kdim, int Nout,
                   const int32_t *__restrict__ count, const int32_t *__restrict__ offset,
-                  uint16_t *__restrict__ out, uint16_t *__restrict__ g_save,
-                  uint16_t *__restrict__ u_save, int *status) {
+                  const int32_t *__restrict__ row_token, uint16_t *__restrict__ out,
+                  uint16_t *__restrict__ g_save, uint16_t *__restrict__ u_save, int *status) {
     constexpr int BN_OUT = EPI == EPI_SWIGLU ? MMA_N / 2 : MMA_N;
     constexpr int PM = 2 * BM;  // rows per pair tile
     extern __shared__ uint8_t smem_raw[];
@@ -226,9 +231,15 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tm_a, const __grid_constan
 
     if (warp == 0) {
         // -------------------------------------------- TMA producer (both CTAs)
-        if (lane == 0) {
-            tma_prefetch_desc(&tm_a);
-            tma_prefetch_desc(rank && EPI == EPI_SWIGLU ? &tm_b1 : &tm_b0);
+        // lane 0 drives the ring; with GATHER lanes 0-3 each fetch 32 of the
+        // CTA's 128 A rows
+        constexpr int PL = GATHER ? 4 : 1;
+        constexpr unsigned PMASK = (1u << PL) - 1u;
+        if (lane < PL) {
+            if (lane == 0) {
+                tma_prefetch_desc(&tm_a);
+                tma_prefetch_desc(rank && EPI == EPI_SWIGLU ? &tm_b1 : &tm_b0);
+            }
             int stage = 0;
             uint32_t phase = 0;
             int issued = 0;
@@ -239,8 +250,20 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tm_a, const __grid_constan
                 const int b_row = EPI == EPI_SWIGLU ? t.e * Nout + t.n * BN_OUT
                                                     : t.e * Nout + t.n * BN_OUT + (int)rank * (MMA_N / 2);
                 const CUtensorMap *mb = rank && EPI == EPI_SWIGLU ? &tm_b1 : &tm_b0;
+                int tok[GATHER ? 32 : 1];
+                if (GATHER) {
+                    const int valid_end = offset[t.e] + count[t.e];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int r = a_row + lane * 32 + i;
+                        tok[i] = r < valid_end ? row_token[r] : 0;
+                    }
+                }
                 for (int kb = 0; kb < nk; ++kb) {
-                    if (!mbar_wait(smem_u32(&bars->empty[stage]), phase ^ 1, status, abort)) {
+                    bool got = true;
+                    if (lane == 0)
+                        got = mbar_wait(smem_u32(&bars->empty[stage]), phase ^ 1, status, abort);
+                    if (!__shfl_sync(PMASK, (int)got, 0)) {
                         ok = false;
                         break;
                     }
@@ -248,27 +271,38 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tm_a, const __grid_constan
                     const uint32_t full = cluster_map(own_full, 0);
                     const uint32_t sa = smem_u32(smem + (size_t)stage * P_STAGE_BYTES);
                     const uint32_t sb = sa + A_BYTES;
-                    if (leader) mbar_arrive_expect_tx(own_full, 2 * P_STAGE_BYTES);
-                    tma_load_2d_pair(sa, &tm_a, full, kb * BK, a_row);
-                    tma_load_2d_pair(sb, mb, full, kb * BK, b_row);
+                    if (lane == 0 && leader) mbar_arrive_expect_tx(own_full, 2 * P_STAGE_BYTES);
+                    if (GATHER) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            tma_gather4_pair(sa + (uint32_t)(lane * 32 + 4 * i) * 128, &tm_a, full,
+                                             kb * BK, tok[4 * i], tok[4 * i + 1], tok[4 * i + 2],
+                                             tok[4 * i + 3]);
+                    } else {
+                        tma_load_2d_pair(sa, &tm_a, full, kb * BK, a_row);
+                    }
+                    if (lane == 0) tma_load_2d_pair(sb, mb, full, kb * BK, b_row);
                     ++issued;
                     if (++stage == P_STAGES) { stage = 0; phase ^= 1; }
                 }
             }
-            if (!ok && leader) {
-                // the leader's full barriers count both CTAs' copies: let the ones
-                // already issued land before the pair leaves
-                for (int s = 0; s < P_STAGES; ++s) {
-                    volatile int no_abort = 0;
-                    mbar_wait(smem_u32(&bars->full[s]), phase ^ (s >= stage ? 1 : 0), status,
-                              &no_abort);
+            if (lane == 0) {
+                if (!ok && leader) {
+                    // the leader's full barriers count both CTAs' copies: let the
+                    // ones already issued land before the pair leaves
+                    for (int s = 0; s < P_STAGES; ++s) {
+                        volatile int no_abort = 0;
+                        mbar_wait(smem_u32(&bars->full[s]), phase ^ (s >= stage ? 1 : 0), status,
+                                  &no_abort);
+                    }
                 }
-            }
-            // every release of every stage (the leader's commits) has arrived
-            for (int s = 0; s < P_STAGES; ++s) {
-                const int uses = issued / P_STAGES + (s < issued % P_STAGES ? 1 : 0);
-                if (uses > 0)
-                    mbar_wait(smem_u32(&bars->empty[s]), (uint32_t)((uses - 1) & 1), status, abort);
+                // every release of every stage (the leader's commits) has arrived
+                for (int s = 0; s < P_STAGES; ++s) {
+                    const int uses = issued / P_STAGES + (s < issued % P_STAGES ? 1 : 0);
+                    if (uses > 0)
+                        mbar_wait(smem_u32(&bars->empty[s]), (uint32_t)((uses - 1) & 1), status,
+                                  abort);
+                }
             }
         }
     } else if (warp == 1) {
@@ -340,15 +374,16 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tm_a, const __grid_constan
 
 // ---------------------------------------------------------------- host side --
 
-template <int EPI>
+template <int EPI, bool GATHER>
 moe_status launch_gemm_pair(const CUtensorMap &a, const CUtensorMap &b0, const CUtensorMap &b1,
                             int N, int Kdim, int Nout, int max_row_tiles, const int32_t *count,
-                            const int32_t *offset, uint16_t *out, uint16_t *gs, uint16_t *us,
-                            int *status, cudaStream_t st) {
+                            const int32_t *offset, const int32_t *row_token, uint16_t *out,
+                            uint16_t *gs, uint16_t *us, int *status, cudaStream_t st) {
     const size_t smem = smem_bytes_pair(N);
     static size_t configured = 0;
     if (smem > configured) {
-        if (cudaFuncSetAttribute(grouped_gemm_pair<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(grouped_gemm_pair<EPI, GATHER>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem_bytes_pair(kMaxN)) != cudaSuccess)
             return MOE_ERR_CUDA;
         configured = smem_bytes_pair(kMaxN);
@@ -368,10 +403,21 @@ moe_status launch_gemm_pair(const CUtensorMap &a, const CUtensorMap &b0, const C
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, grouped_gemm_pair<EPI>, a, b0, b1, N, Kdim, Nout, count, offset,
-                           out, gs, us, status) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, grouped_gemm_pair<EPI, GATHER>, a, b0, b1, N, Kdim, Nout, count,
+                           offset, row_token, out, gs, us, status) != cudaSuccess)
         return MOE_ERR_CUDA;
     return launch_status();
+}
+
+// row_token[route_row[t, k]] = t for every accepted route (the inverse of the
+// route map over the packed rows).
+__global__ void __launch_bounds__(256)
+invert_route_rows(int64_t routes, int K, const int32_t *__restrict__ route_row,
+                  int32_t *__restrict__ row_token) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= routes) return;
+    const int32_t r = route_row[i];
+    if (r >= 0) row_token[r] = (int32_t)(i / K);
 }
 
 }  // namespace
@@ -413,9 +459,64 @@ MOE_API moe_status moe_expert_ffn(const moe_shape *s, const moe_bf16 *x_disp,
     int *status = static_cast<int *>(ws);
     const int64_t rows = std::min<int64_t>(R, (int64_t)s->T * s->K);
     const int max_row_tiles = (int)((rows + BM - 1) / BM + s->N);
-    r = launch_gemm_pair<EPI_SWIGLU>(ma, mg, mu, s->N, s->d, s->h, max_row_tiles, expert_count,
-                                     expert_offset, h_act, g_save, u_save, status, stream);
+    r = launch_gemm_pair<EPI_SWIGLU, false>(ma, mg, mu, s->N, s->d, s->h, max_row_tiles,
+                                            expert_count, expert_offset, nullptr, h_act, g_save,
+                                            u_save, status, stream);
     if (r != MOE_OK) return r;
-    return launch_gemm_pair<EPI_STORE>(mh, md, md, s->N, s->h, s->d, max_row_tiles, expert_count,
-                                       expert_offset, y_disp, nullptr, nullptr, status, stream);
+    return launch_gemm_pair<EPI_STORE, false>(mh, md, md, s->N, s->h, s->d, max_row_tiles,
+                                              expert_count, expert_offset, nullptr, y_disp, nullptr,
+                                              nullptr, status, stream);
+}
+
+MOE_API size_t moe_expert_ffn_gather_workspace_bytes(const moe_shape *s) {
+    if (check_shape(s) != MOE_OK) return 0;
+    return 256 + (((size_t)buffer_rows(s) * sizeof(int32_t) + 255) & ~(size_t)255);
+}
+
+MOE_API moe_status moe_expert_ffn_gather(const moe_shape *s, const moe_bf16 *x,
+                                         const int32_t *route_row, const int32_t *expert_count,
+                                         const int32_t *expert_offset, const moe_bf16 *w_gate,
+                                         const moe_bf16 *w_up, const moe_bf16 *w_down,
+                                         moe_bf16 *h_act, moe_bf16 *g_save, moe_bf16 *u_save,
+                                         moe_bf16 *y_disp, void *ws, size_t ws_bytes,
+                                         cudaStream_t stream) {
+    moe_status r = check_shape(s);
+    if (r != MOE_OK) return r;
+    if (s->d % BK != 0 || s->h % BK != 0) return MOE_ERR_UNSUPPORTED;
+    if (!expert_count || !expert_offset || !ws) return MOE_ERR_INVALID_ARG;
+    if ((g_save == nullptr) != (u_save == nullptr)) return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < moe_expert_ffn_gather_workspace_bytes(s) ||
+        (reinterpret_cast<uintptr_t>(ws) & 255u))
+        return MOE_ERR_WORKSPACE;
+    const int64_t R = buffer_rows(s);
+    if (R == 0 || s->T == 0) return MOE_OK;
+    if (!x || !route_row || !w_gate || !w_up || !w_down || !h_act || !y_disp)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(route_row) || !aligned16(w_gate) || !aligned16(w_up) ||
+        !aligned16(w_down) || !aligned16(h_act) || !aligned16(y_disp) ||
+        (g_save && !aligned16(g_save)) || (u_save && !aligned16(u_save)) ||
+        !aligned16(expert_count) || !aligned16(expert_offset))
+        return MOE_ERR_ALIGNMENT;
+    int32_t *row_token = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + 256);
+    CUtensorMap mx, mg, mu, mh, md;
+    if (!make_map(&mx, x, s->d, s->T, 1) ||
+        !make_map(&mg, w_gate, s->d, (uint64_t)s->N * s->h, 128) ||
+        !make_map(&mu, w_up, s->d, (uint64_t)s->N * s->h, 128) ||
+        !make_map(&mh, h_act, s->h, R, BM) ||
+        !make_map(&md, w_down, s->h, (uint64_t)s->N * s->d, MMA_N / 2))
+        return MOE_ERR_CUDA;
+    int *status = static_cast<int *>(ws);
+    const int64_t routes = (int64_t)s->T * s->K;
+    invert_route_rows<<<(unsigned)((routes + 255) / 256), 256, 0, stream>>>(routes, s->K, route_row,
+                                                                          row_token);
+    if ((r = launch_status()) != MOE_OK) return r;
+    const int64_t rows = std::min<int64_t>(R, routes);
+    const int max_row_tiles = (int)((rows + BM - 1) / BM + s->N);
+    r = launch_gemm_pair<EPI_SWIGLU, true>(mx, mg, mu, s->N, s->d, s->h, max_row_tiles, expert_count,
+                                           expert_offset, row_token, h_act, g_save, u_save, status,
+                                           stream);
+    if (r != MOE_OK) return r;
+    return launch_gemm_pair<EPI_STORE, false>(mh, md, md, s->N, s->h, s->d, max_row_tiles,
+                                              expert_count, expert_offset, nullptr, y_disp, nullptr,
+                                              nullptr, status, stream);
 }

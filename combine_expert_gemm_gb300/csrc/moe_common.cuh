@@ -351,6 +351,20 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// Gather of four rows (r0..r3, any rows of the tensor) x one 64-element box
+// into this CTA's shared memory, completion signalled on the pair leader's
+// mbarrier (bar is a cluster address).  The map's box is one row high; the
+// four rows land as four consecutive 128-byte rows.
+__device__ __forceinline__ void tma_gather4_pair(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                                 int32_t x, int32_t r0, int32_t r1, int32_t r2,
+                                                 int32_t r3) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile::gather4.mbarrier::"
+        "complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
+        : "memory");
+}
+
 // MMA over the CTA pair: A rows 0-127 / 128-255 and B columns 0-N/2 / N/2-N
 // come from the leader's / peer's shared memory at the same offsets; the
 // accumulator rows land in each CTA's own tensor memory.

@@ -186,6 +186,32 @@ moe_status moe_expert_ffn(const moe_shape *s, const moe_bf16 *x_disp, const int3
                           moe_bf16 *g_save, moe_bf16 *u_save, moe_bf16 *y_disp, void *ws,
                           size_t ws_bytes, cudaStream_t stream);
 
+/* Bytes of workspace moe_expert_ffn_gather needs: the device status word plus
+ * one int32 per capacity-buffer row (0 if the shape is invalid). */
+size_t moe_expert_ffn_gather_workspace_bytes(const moe_shape *s);
+
+/*
+ * moe_expert_ffn_gather -- steps D and F1-F2 fused: the same results as
+ * moe_dispatch followed by moe_expert_ffn (h_act, g_save, u_save and y_disp
+ * bit for bit), without writing or reading x_disp.  Section 05 Table 8
+ * "Dispatch forward PUT" and 5.6 (each accepted route's row is the token's
+ * row); Section 08, 8.5 (grouped GEMM over device offsets).  GEMM1 fetches
+ * each packed row straight from x: a small kernel inverts the route map
+ * (row -> token, into ws) and the GEMM's producer loads four token rows at a
+ * time by TMA gather.  For a forward without backward: the expert backward
+ * reads x_disp, which this call does not produce.
+ *   x [T, d] bf16; route_row [T, K] as moe_route wrote it; the rest as in
+ *   moe_expert_ffn; ws of moe_expert_ffn_gather_workspace_bytes bytes,
+ *   256-byte aligned.
+ * Errors: as moe_expert_ffn.
+ */
+moe_status moe_expert_ffn_gather(const moe_shape *s, const moe_bf16 *x, const int32_t *route_row,
+                                 const int32_t *expert_count, const int32_t *expert_offset,
+                                 const moe_bf16 *w_gate, const moe_bf16 *w_up,
+                                 const moe_bf16 *w_down, moe_bf16 *h_act, moe_bf16 *g_save,
+                                 moe_bf16 *u_save, moe_bf16 *y_disp, void *ws, size_t ws_bytes,
+                                 cudaStream_t stream);
+
 /* Bytes of workspace moe_expert_ffn_backward needs: the device status word
  * and the two [R, h] bf16 intermediates dG and dU. */
 size_t moe_expert_ffn_backward_workspace_bytes(const moe_shape *s);

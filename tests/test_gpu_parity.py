@@ -265,3 +265,35 @@ def test_dropless_capacity(moe):
     assert (ref["route_row"] >= 0).all()
     assert int(ref["expert_offset"][-1]) == cfg.T * cfg.K
     assert_close_bf16(bits(buf.y), ref["y"], "dropless y")
+
+
+FUSED = ["tiny", "ragged", "zipf_drops", "wide_ragged", "dense_N1", "K_eq_N", "cap0", "N200"]
+
+
+@pytest.mark.parametrize("name", FUSED + ["olmoe"])
+def test_fused_dispatch_gemm_equals_two_step(moe, name):
+    """moe_expert_ffn_gather (x rows fetched by route inside GEMM1) gives the
+    bits of moe_dispatch + moe_expert_ffn on every valid row, and with it the
+    same layer output."""
+    cfg = synth.CONFIGS["olmoe"] if name == "olmoe" else SMALL[name]
+    x, wr, bias, wg, wu, wd = _inputs(cfg)
+    s = _shape(moe, cfg)
+    W = [bf(wg), bf(wu), bf(wd)]
+    outs = []
+    for fused in (False, True):
+        buf = moe.LayerBuffers(s, DEV, save_for_backward=True)
+        for t in (buf.h_act, buf.y_disp, buf.g_save, buf.u_save):
+            t.view(torch.int16).fill_(SENT)
+        moe.layer_forward(buf, bf(x), f32(wr), None if bias is None else f32(bias), *W,
+                          fused_dispatch=fused)
+        torch.cuda.synchronize()
+        assert moe.read_device_error(buf.gather_ws if fused else buf.ffn_ws) == 0
+        outs.append(buf)
+    A = int(outs[0].expert_offset[-1].item())
+    for k in ("h_act", "g_save", "u_save", "y_disp"):
+        a, b = bits(getattr(outs[0], k))[:A], bits(getattr(outs[1], k))[:A]
+        assert np.array_equal(a, b), k
+    assert np.array_equal(bits(outs[0].y), bits(outs[1].y))
+    if name != "olmoe":
+        ref = oracle.layer_forward(x, wr, bias, wg, wu, wd, cfg.K, cfg.cap)
+        assert_close_bf16(bits(outs[1].y), ref["y"], f"{name} fused y")
