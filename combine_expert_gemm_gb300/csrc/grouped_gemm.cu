@@ -122,6 +122,67 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tbase, int half, bool row
     }
 }
 
+// The same epilogue for a warp whose 32 rows are all valid: each 32-column
+// chunk is packed to bf16 and stored through the warp's 2 KB shared-memory
+// block by TMA (one instruction per chunk and output), instead of 32 row
+// segments per store instruction.
+template <int EPI>
+__device__ __forceinline__ void epilogue_tile_tma(uint32_t tbase, int half, int row0, int n,
+                                                  int Nout, uint8_t *blk, const CUtensorMap *mo,
+                                                  const CUtensorMap *mg, const CUtensorMap *mu,
+                                                  bool save, int lane) {
+    constexpr int BN_OUT = EPI == EPI_SWIGLU ? MMA_N / 2 : MMA_N;
+    for (int c = half * (BN_OUT / 2); c < (half + 1) * (BN_OUT / 2); c += 32) {
+        const int col = n * BN_OUT + c;
+        if (EPI == EPI_SWIGLU) {
+            uint32_t g0[16], g1[16], u0[16], u1[16];
+            tmem_ld16(tbase + c, g0);
+            tmem_ld16(tbase + c + 16, g1);
+            tmem_ld16(tbase + BN_OUT + c, u0);
+            tmem_ld16(tbase + BN_OUT + c + 16, u1);
+            tmem_ld_wait();
+            reg_fence(g0);
+            reg_fence(g1);
+            reg_fence(u0);
+            reg_fence(u1);
+            if (col >= Nout) continue;  // warp-uniform
+            uint32_t hp[16], gp[16], up[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const uint32_t *gs = i < 8 ? g0 : g1;
+                const uint32_t *us = i < 8 ? u0 : u1;
+                const int k = 2 * (i & 7);
+                const float ga = __uint_as_float(gs[k]), gb = __uint_as_float(gs[k + 1]);
+                const float ua = __uint_as_float(us[k]), ub = __uint_as_float(us[k + 1]);
+                hp[i] = pack_bf16x2(__fdividef(ga, 1.0f + __expf(-ga)) * ua,
+                                    __fdividef(gb, 1.0f + __expf(-gb)) * ub);
+                gp[i] = pack_bf16x2(ga, gb);
+                up[i] = pack_bf16x2(ua, ub);
+            }
+            warp_store_bf16_32x32(blk, hp, mo, col, row0, lane);
+            if (save) {
+                warp_store_bf16_32x32(blk, gp, mg, col, row0, lane);
+                warp_store_bf16_32x32(blk, up, mu, col, row0, lane);
+            }
+        } else {
+            uint32_t r0[16], r1[16];
+            tmem_ld16(tbase + c, r0);
+            tmem_ld16(tbase + c + 16, r1);
+            tmem_ld_wait();
+            reg_fence(r0);
+            reg_fence(r1);
+            if (col >= Nout) continue;  // warp-uniform
+            uint32_t p[16];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                p[i] = pack_bf16x2(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]));
+                p[8 + i] = pack_bf16x2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1]));
+            }
+            warp_store_bf16_32x32(blk, p, mo, col, row0, lane);
+        }
+    }
+}
+
 // ------------------------------------------------------------ CTA-pair kernel
 //
 // Two CTAs of a cluster compute one 256-row x 256-column tile with
@@ -147,9 +208,11 @@ struct alignas(8) PairBars {
     int abort;
 };
 
+constexpr int P_STG_BYTES = P_EPI_WARPS * 2048;  // one 32 x 32 bf16 store block per epilogue warp
+
 constexpr size_t smem_bytes_pair(int N) {
-    return 1024 + (size_t)P_STAGES * P_STAGE_BYTES + sizeof(PairBars) + sizeof(int32_t) * (N + 1) +
-           16;
+    return 1024 + (size_t)P_STAGES * P_STAGE_BYTES + P_STG_BYTES + sizeof(PairBars) +
+           sizeof(int32_t) * (N + 1) + 16;
 }
 
 // GATHER: A is not the packed buffer but the token rows themselves: the map
@@ -160,7 +223,9 @@ constexpr size_t smem_bytes_pair(int N) {
 template <int EPI, bool GATHER>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_pair(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b0,
-                  const __grid_constant__ CUtensorMap tm_b1, int N, int Kdim, int Nout,
+                  const __grid_constant__ CUtensorMap tm_b1, const __grid_constant__ CUtensorMap tm_o,
+                  const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_u,
+                  int N, int Kdim, int Nout,
                   const int32_t *__restrict__ count, const int32_t *__restrict__ offset,
                   const int32_t *__restrict__ row_token, uint16_t *__restrict__ out,
                   uint16_t *__restrict__ g_save, uint16_t *__restrict__ u_save, int *status) {
@@ -169,7 +234,8 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tm_a, const __grid_constan
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    PairBars *bars = reinterpret_cast<PairBars *>(smem + (size_t)P_STAGES * P_STAGE_BYTES);
+    uint8_t *stage_out = smem + (size_t)P_STAGES * P_STAGE_BYTES;  // [8 warps][2 KB]
+    PairBars *bars = reinterpret_cast<PairBars *>(stage_out + P_STG_BYTES);
     int32_t *tile_start = reinterpret_cast<int32_t *>(bars + 1);
     volatile int *abort = &bars->abort;
     const uint32_t rank = cluster_rank();
@@ -355,12 +421,18 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tm_a, const __grid_constan
             if (!mbar_wait(smem_u32(&bars->tfull[acc]), acc_phase, status, abort)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * ACC_COLS;
-            epilogue_tile<EPI>(tbase, half, row_ok, row, t.n, Nout, out, g_save, u_save);
+            if (rows_valid - (row_in_tile - lane) >= 32)  // all 32 rows of this warp are valid
+                epilogue_tile_tma<EPI>(tbase, half, (int)(row - lane), t.n, Nout,
+                                       stage_out + (warp - 2) * 2048, &tm_o, &tm_g, &tm_u,
+                                       g_save != nullptr, lane);
+            else
+                epilogue_tile<EPI>(tbase, half, row_ok, row, t.n, Nout, out, g_save, u_save);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(cluster_map(smem_u32(&bars->tempty[acc]), 0));
             if (++acc == 2) { acc = 0; acc_phase ^= 1; }
         }
+        if (lane == 0) bulk_wait<0>();  // stores complete before the CTA ends
     }
 
     tc_fence_before();
@@ -376,6 +448,7 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tm_a, const __grid_constan
 
 template <int EPI, bool GATHER>
 moe_status launch_gemm_pair(const CUtensorMap &a, const CUtensorMap &b0, const CUtensorMap &b1,
+                            const CUtensorMap &o, const CUtensorMap &og, const CUtensorMap &ou,
                             int N, int Kdim, int Nout, int max_row_tiles, const int32_t *count,
                             const int32_t *offset, const int32_t *row_token, uint16_t *out,
                             uint16_t *gs, uint16_t *us, int *status, cudaStream_t st) {
@@ -403,8 +476,8 @@ moe_status launch_gemm_pair(const CUtensorMap &a, const CUtensorMap &b0, const C
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, grouped_gemm_pair<EPI, GATHER>, a, b0, b1, N, Kdim, Nout, count,
-                           offset, row_token, out, gs, us, status) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, grouped_gemm_pair<EPI, GATHER>, a, b0, b1, o, og, ou, N, Kdim,
+                           Nout, count, offset, row_token, out, gs, us, status) != cudaSuccess)
         return MOE_ERR_CUDA;
     return launch_status();
 }
@@ -456,16 +529,21 @@ MOE_API moe_status moe_expert_ffn(const moe_shape *s, const moe_bf16 *x_disp,
         !make_map(&mh, h_act, s->h, R, BM) ||
         !make_map(&md, w_down, s->h, (uint64_t)s->N * s->d, MMA_N / 2))
         return MOE_ERR_CUDA;
+    CUtensorMap oh, og, ou, oy;
+    if (!make_map_bf16_store(&oh, h_act, s->h, R) || !make_map_bf16_store(&oy, y_disp, s->d, R) ||
+        !make_map_bf16_store(&og, g_save ? g_save : h_act, s->h, R) ||
+        !make_map_bf16_store(&ou, u_save ? u_save : h_act, s->h, R))
+        return MOE_ERR_CUDA;
     int *status = static_cast<int *>(ws);
     const int64_t rows = std::min<int64_t>(R, (int64_t)s->T * s->K);
     const int max_row_tiles = (int)((rows + BM - 1) / BM + s->N);
-    r = launch_gemm_pair<EPI_SWIGLU, false>(ma, mg, mu, s->N, s->d, s->h, max_row_tiles,
-                                            expert_count, expert_offset, nullptr, h_act, g_save,
-                                            u_save, status, stream);
+    r = launch_gemm_pair<EPI_SWIGLU, false>(ma, mg, mu, oh, og, ou, s->N, s->d, s->h,
+                                            max_row_tiles, expert_count, expert_offset, nullptr,
+                                            h_act, g_save, u_save, status, stream);
     if (r != MOE_OK) return r;
-    return launch_gemm_pair<EPI_STORE, false>(mh, md, md, s->N, s->h, s->d, max_row_tiles,
-                                              expert_count, expert_offset, nullptr, y_disp, nullptr,
-                                              nullptr, status, stream);
+    return launch_gemm_pair<EPI_STORE, false>(mh, md, md, oy, oy, oy, s->N, s->h, s->d,
+                                              max_row_tiles, expert_count, expert_offset, nullptr,
+                                              y_disp, nullptr, nullptr, status, stream);
 }
 
 MOE_API size_t moe_expert_ffn_gather_workspace_bytes(const moe_shape *s) {
@@ -505,6 +583,11 @@ MOE_API moe_status moe_expert_ffn_gather(const moe_shape *s, const moe_bf16 *x,
         !make_map(&mh, h_act, s->h, R, BM) ||
         !make_map(&md, w_down, s->h, (uint64_t)s->N * s->d, MMA_N / 2))
         return MOE_ERR_CUDA;
+    CUtensorMap oh, og, ou, oy;
+    if (!make_map_bf16_store(&oh, h_act, s->h, R) || !make_map_bf16_store(&oy, y_disp, s->d, R) ||
+        !make_map_bf16_store(&og, g_save ? g_save : h_act, s->h, R) ||
+        !make_map_bf16_store(&ou, u_save ? u_save : h_act, s->h, R))
+        return MOE_ERR_CUDA;
     int *status = static_cast<int *>(ws);
     const int64_t routes = (int64_t)s->T * s->K;
     invert_route_rows<<<(unsigned)((routes + 255) / 256), 256, 0, stream>>>(routes, s->K, route_row,
@@ -512,11 +595,11 @@ MOE_API moe_status moe_expert_ffn_gather(const moe_shape *s, const moe_bf16 *x,
     if ((r = launch_status()) != MOE_OK) return r;
     const int64_t rows = std::min<int64_t>(R, routes);
     const int max_row_tiles = (int)((rows + BM - 1) / BM + s->N);
-    r = launch_gemm_pair<EPI_SWIGLU, true>(mx, mg, mu, s->N, s->d, s->h, max_row_tiles, expert_count,
-                                           expert_offset, row_token, h_act, g_save, u_save, status,
-                                           stream);
+    r = launch_gemm_pair<EPI_SWIGLU, true>(mx, mg, mu, oh, og, ou, s->N, s->d, s->h, max_row_tiles,
+                                           expert_count, expert_offset, row_token, h_act, g_save,
+                                           u_save, status, stream);
     if (r != MOE_OK) return r;
-    return launch_gemm_pair<EPI_STORE, false>(mh, md, md, s->N, s->h, s->d, max_row_tiles,
-                                              expert_count, expert_offset, nullptr, y_disp, nullptr,
-                                              nullptr, status, stream);
+    return launch_gemm_pair<EPI_STORE, false>(mh, md, md, oy, oy, oy, s->N, s->h, s->d,
+                                              max_row_tiles, expert_count, expert_offset, nullptr,
+                                              y_disp, nullptr, nullptr, status, stream);
 }

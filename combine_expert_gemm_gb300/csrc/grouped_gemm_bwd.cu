@@ -73,8 +73,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32_major(int M, int N, int a_
 }
 
 constexpr int kEpiThreads = 256;                      // 8 epilogue warps
-constexpr int STG_LD = 17;                           // padded fp32 row of a staging block
-constexpr int STG_BYTES = 8 * 32 * STG_LD * 4;       // one 32 x 16 block per epilogue warp
 
 struct Params {
     int N, d, h;
@@ -106,55 +104,68 @@ __device__ __forceinline__ int k_blocks(const Params &p, int cnt) {
 }
 
 // Epilogue of a dgrad tile for one warp: 32 rows (TMEM lanes) and one half of
-// the 256 columns.  DGRAD_DH: dU = dH * silu(G), dG = dH * U * silu'(G) from the
-// saved G, U (prefetched three 16-column chunks ahead, they come from DRAM);
-// DGRAD_DX: a bf16 store of dX.
+// the 256 columns, in 32-column chunks.  DGRAD_DH: dU = dH * silu(G) and
+// dG = dH * U * silu'(G) from the saved G, U; DGRAD_DX: a bf16 copy of dX.
+// When all 32 rows of the warp are valid each output chunk goes through the
+// warp's 2 KB shared-memory block and out by one TMA instruction; otherwise
+// the valid rows store their own 64 bytes.  DGRAD_DH: the saved G, U of the next chunk are fetched
+// while the current one is computed (slots gq/uq[ch & 1]); the first chunk's
+// were fetched into slot 0 by the caller before the accumulator was ready.
 template <int MODE>
-__device__ __forceinline__ void dgrad_epilogue(uint32_t tbase, int half, bool row_ok, int64_t row,
-                                               int n, const Params &p) {
+__device__ __forceinline__ void dgrad_epilogue_tma(uint32_t tbase, int half, int64_t row, int row0,
+                                                   int n, const Params &p, uint8_t *blk,
+                                                   const CUtensorMap *m0, const CUtensorMap *m1,
+                                                   uint4 (&gq)[2][4], uint4 (&uq)[2][4], bool full,
+                                                   bool row_ok, int lane) {
+    constexpr int NCH = (MMA_N / 2) / 32;
     const int width = MODE == DGRAD_DH ? p.h : p.d;
-    // saved G, U of this thread's row, prefetched three 16-column
-    // chunks ahead of their use (they come from DRAM)
-    constexpr int PF = 3, NCH = MMA_N / 32;  // 16-column chunks of this half
-    uint4 gq[PF + 1][2], uq[PF + 1][2];
-    auto fetch = [&](int ch, int slot) {
-        const int col = n * MMA_N + half * (MMA_N / 2) + ch * 16;
-        if (MODE == DGRAD_DH && row_ok && col < width) {
-            const uint4 *gp = reinterpret_cast<const uint4 *>(p.g_save + row * p.h + col);
-            const uint4 *up = reinterpret_cast<const uint4 *>(p.u_save + row * p.h + col);
-            gq[slot][0] = __ldcs(gp);
-            gq[slot][1] = __ldcs(gp + 1);
-            uq[slot][0] = __ldcs(up);
-            uq[slot][1] = __ldcs(up + 1);
+    // a 32-column bf16 chunk of this lane's row: the warp's TMA block when all
+    // 32 rows are valid, else four 16-byte stores of the valid rows
+    auto put = [&](const uint32_t (&w)[16], const CUtensorMap *m, uint16_t *base, int ld, int col) {
+        if (full) {
+            warp_store_bf16_32x32(blk, w, m, col, row0, lane);
+        } else if (row_ok) {
+            uint4 *dst = reinterpret_cast<uint4 *>(base + row * ld + col);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
         }
     };
-    if (MODE == DGRAD_DH) {
-#pragma unroll
-        for (int ch = 0; ch < PF; ++ch) fetch(ch, ch);
-    }
 #pragma unroll
     for (int ch = 0; ch < NCH; ++ch) {
-        const int c = half * (MMA_N / 2) + ch * 16;
-        if (MODE == DGRAD_DH && ch + PF < NCH) fetch(ch + PF, (ch + PF) % (PF + 1));
-        uint32_t r[16];
-        tmem_ld16(tbase + c, r);
-        tmem_ld_wait();
-        reg_fence(r);
-        const int col = n * MMA_N + c;
-        if (!row_ok || col >= width) continue;
-        if (MODE == DGRAD_DH) {
-            const int slot = ch % (PF + 1);
-            const uint32_t *gw = reinterpret_cast<const uint32_t *>(gq[slot]);
-            const uint32_t *uw = reinterpret_cast<const uint32_t *>(uq[slot]);
-            uint32_t dg[8], du[8];
+        const int c = half * (MMA_N / 2) + ch * 32;
+        if (MODE == DGRAD_DH && ch + 1 < NCH) {
+            const int ncol = n * MMA_N + c + 32;
+            if (ncol < width && row_ok) {
+                const uint4 *gp = reinterpret_cast<const uint4 *>(p.g_save + row * p.h + ncol);
+                const uint4 *up = reinterpret_cast<const uint4 *>(p.u_save + row * p.h + ncol);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
+                for (int i = 0; i < 4; ++i) {
+                    gq[(ch + 1) & 1][i] = __ldcs(gp + i);
+                    uq[(ch + 1) & 1][i] = __ldcs(up + i);
+                }
+            }
+        }
+        uint32_t r0[16], r1[16];
+        tmem_ld16(tbase + c, r0);
+        tmem_ld16(tbase + c + 16, r1);
+        tmem_ld_wait();
+        reg_fence(r0);
+        reg_fence(r1);
+        const int col = n * MMA_N + c;
+        if (col >= width) continue;  // warp-uniform
+        if (MODE == DGRAD_DH) {
+            const uint32_t *gw = reinterpret_cast<const uint32_t *>(gq[ch & 1]);
+            const uint32_t *uw = reinterpret_cast<const uint32_t *>(uq[ch & 1]);
+            uint32_t dg[16], du[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
                 float rg[2], ru[2];
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                     const float z = hf ? bf16_hi(gw[i]) : bf16_lo(gw[i]);
                     const float u = hf ? bf16_hi(uw[i]) : bf16_lo(uw[i]);
-                    const float dh = __uint_as_float(r[2 * i + hf]);
+                    const uint32_t rv = i < 8 ? r0[2 * i + hf] : r1[2 * (i - 8) + hf];
+                    const float dh = __uint_as_float(rv);
                     const float sg = __fdividef(1.0f, 1.0f + __expf(-z));
                     ru[hf] = dh * (z * sg);
                     rg[hf] = dh * u * sg * (1.0f + z * (1.0f - sg));
@@ -162,21 +173,16 @@ __device__ __forceinline__ void dgrad_epilogue(uint32_t tbase, int half, bool ro
                 dg[i] = pack_bf16x2(rg[0], rg[1]);
                 du[i] = pack_bf16x2(ru[0], ru[1]);
             }
-            uint4 *gd = reinterpret_cast<uint4 *>(p.out0 + row * p.h + col);
-            uint4 *ud = reinterpret_cast<uint4 *>(p.out1 + row * p.h + col);
-            gd[0] = make_uint4(dg[0], dg[1], dg[2], dg[3]);
-            gd[1] = make_uint4(dg[4], dg[5], dg[6], dg[7]);
-            ud[0] = make_uint4(du[0], du[1], du[2], du[3]);
-            ud[1] = make_uint4(du[4], du[5], du[6], du[7]);
+            put(dg, m0, p.out0, p.h, col);
+            put(du, m1, p.out1, p.h, col);
         } else {
-            uint32_t pk[8];
+            uint32_t pk[16];
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]),
-                                    __uint_as_float(r[2 * i + 1]));
-            uint4 *dst = reinterpret_cast<uint4 *>(p.out0 + row * p.d + col);
-            dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            for (int i = 0; i < 8; ++i) {
+                pk[i] = pack_bf16x2(__uint_as_float(r0[2 * i]), __uint_as_float(r0[2 * i + 1]));
+                pk[8 + i] = pack_bf16x2(__uint_as_float(r1[2 * i]), __uint_as_float(r1[2 * i + 1]));
+            }
+            put(pk, m0, p.out0, p.d, col);
         }
     }
 }
@@ -202,22 +208,26 @@ struct alignas(8) PairBars {
     int abort;
 };
 
+constexpr int P_STG_BYTES = P_EPI_WARPS * 2048;  // one 32 x 32 bf16 store block per epilogue warp
+
 constexpr size_t smem_bytes_pair(int N) {
-    return 1024 + (size_t)P_STAGES * P_STAGE_BYTES + sizeof(PairBars) + sizeof(int32_t) * (N + 1) +
-           16;
+    return 1024 + (size_t)P_STAGES * P_STAGE_BYTES + P_STG_BYTES + sizeof(PairBars) +
+           sizeof(int32_t) * (N + 1) + 16;
 }
 
 template <int MODE>
 __global__ void __launch_bounds__(ModeT<MODE>::threads, 1)
 grouped_dgrad_pair(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
                    const __grid_constant__ CUtensorMap tm_b0, const __grid_constant__ CUtensorMap tm_b1,
+                   const __grid_constant__ CUtensorMap tm_o0, const __grid_constant__ CUtensorMap tm_o1,
                    const Params p) {
     static_assert(MODE == DGRAD_DH || MODE == DGRAD_DX, "dgrad only");
     constexpr int PM = 2 * BM;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    PairBars *bars = reinterpret_cast<PairBars *>(smem + (size_t)P_STAGES * P_STAGE_BYTES);
+    uint8_t *stage_out = smem + (size_t)P_STAGES * P_STAGE_BYTES;  // [8 warps][2 KB]
+    PairBars *bars = reinterpret_cast<PairBars *>(stage_out + P_STG_BYTES);
     int32_t *tile_start = reinterpret_cast<int32_t *>(bars + 1);
     volatile int *abort = &bars->abort;
     int *status = p.status;
@@ -364,17 +374,35 @@ grouped_dgrad_pair(const __grid_constant__ CUtensorMap tm_a0, const __grid_const
         for (int g = unit0; g < total; g += units) {
             const Tile t = map_pair(g);
             const int cnt = p.count[t.e], off = p.offset[t.e];
+            const bool row_ok = rit < cnt - t.m * PM;
+            const int64_t row = (int64_t)off + t.m * PM + rit;
+            const bool full_block = cnt - t.m * PM - (rit - lane) >= 32;  // all 32 rows valid
+            uint4 gq[2][4], uq[2][4];
+            if (MODE == DGRAD_DH && row_ok) {
+                // the first chunk's saved G, U, fetched before the accumulator is ready
+                const int col = t.n * MMA_N + half * (MMA_N / 2);
+                if (col < p.h) {
+                    const uint4 *gp = reinterpret_cast<const uint4 *>(p.g_save + row * p.h + col);
+                    const uint4 *up = reinterpret_cast<const uint4 *>(p.u_save + row * p.h + col);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        gq[0][i] = __ldcs(gp + i);
+                        uq[0][i] = __ldcs(up + i);
+                    }
+                }
+            }
             if (!mbar_wait(smem_u32(&bars->tfull[acc]), acc_phase, status, abort)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * ACC_COLS;
-            const bool row_ok = rit < cnt - t.m * PM;
-            const int64_t row = (int64_t)off + t.m * PM + rit;
-            dgrad_epilogue<MODE>(tbase, half, row_ok, row, t.n, p);
+            dgrad_epilogue_tma<MODE>(tbase, half, row, (int)(row - lane), t.n, p,
+                                     stage_out + (warp - 2) * 2048, &tm_o0, &tm_o1, gq, uq,
+                                     full_block, row_ok, lane);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(cluster_map(smem_u32(&bars->tempty[acc]), 0));
             if (++acc == 2) { acc = 0; acc_phase ^= 1; }
         }
+        if (lane == 0) bulk_wait<0>();  // stores complete before the CTA ends
     }
 
     tc_fence_before();
@@ -388,7 +416,8 @@ grouped_dgrad_pair(const __grid_constant__ CUtensorMap tm_a0, const __grid_const
 
 template <int MODE>
 moe_status launch_dgrad_pair(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap &b0,
-                             const CUtensorMap &b1, const Params &p, int max_units, cudaStream_t st) {
+                             const CUtensorMap &b1, const CUtensorMap &o0, const CUtensorMap &o1,
+                             const Params &p, int max_units, cudaStream_t st) {
     static size_t configured = 0;
     const size_t smem = smem_bytes_pair(p.N);
     if (smem > configured) {
@@ -411,7 +440,7 @@ moe_status launch_dgrad_pair(const CUtensorMap &a0, const CUtensorMap &a1, const
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, grouped_dgrad_pair<MODE>, a0, a1, b0, b1, p) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, grouped_dgrad_pair<MODE>, a0, a1, b0, b1, o0, o1, p) != cudaSuccess)
         return MOE_ERR_CUDA;
     return launch_status();
 }
@@ -817,6 +846,10 @@ MOE_API moe_status moe_expert_ffn_backward(
         !make_map(&dg_mn, dG, s->h, R, 64) || !make_map(&du_mn, dU, s->h, R, 64) ||
         !make_map(&x_mn, x_disp, s->d, R, 64))
         return MOE_ERR_CUDA;
+    CUtensorMap o_dg, o_du, o_dx;
+    if (!make_map_bf16_store(&o_dg, dG, s->h, R) || !make_map_bf16_store(&o_du, dU, s->h, R) ||
+        !make_map_bf16_store(&o_dx, dx_disp, s->d, R))
+        return MOE_ERR_CUDA;
     CUtensorMap o_down, o_gate, o_up;
     if (!make_map_f32_3d(&o_down, dw_down, s->h, s->d, s->N) ||
         !make_map_f32_3d(&o_gate, dw_gate, s->d, s->h, s->N) ||
@@ -830,13 +863,15 @@ MOE_API moe_status moe_expert_ffn_backward(
     p.out0 = dG;
     p.out1 = dU;
     const int pair_tiles = (row_tiles + 1) / 2 + s->N;
-    r = launch_dgrad_pair<DGRAD_DH>(dy_k, dy_k, wd_mn, wd_mn, p, pair_tiles * p.ntn, stream);
+    r = launch_dgrad_pair<DGRAD_DH>(dy_k, dy_k, wd_mn, wd_mn, o_dg, o_du, p, pair_tiles * p.ntn,
+                                    stream);
     if (r != MOE_OK) return r;
     // dX = dG W_gate + dU W_up
     p.ntn = (s->d + MMA_N - 1) / MMA_N;
     p.out0 = dx_disp;
     p.out1 = nullptr;
-    r = launch_dgrad_pair<DGRAD_DX>(dg_k, du_k, wg_mn, wu_mn, p, pair_tiles * p.ntn, stream);
+    r = launch_dgrad_pair<DGRAD_DX>(dg_k, du_k, wg_mn, wu_mn, o_dx, o_dx, p, pair_tiles * p.ntn,
+                                    stream);
     if (r != MOE_OK) return r;
     // dW_down = dY^T H
     p.mtn = (s->d + 2 * BM - 1) / (2 * BM);

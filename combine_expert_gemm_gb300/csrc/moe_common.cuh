@@ -105,6 +105,20 @@ inline bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D bf16 map over a row-major [rows, inner] matrix for TMA stores of
+// 32 x 32 blocks, 64-byte swizzle (a 32-element bf16 row is 64 bytes).
+inline bool make_map_bf16_store(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {inner, rows};
+    const cuuint64_t strides[1] = {inner * 2};
+    const cuuint32_t box[2] = {32, 32};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 3-D fp32 map over [planes, rows, inner] (row-major, planes of rows x inner)
 // for TMA stores of 32 x 32 blocks, 128-byte swizzle: a block never crosses a
 // plane, and rows past `rows` or columns past `inner` are clipped.
@@ -218,6 +232,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src, int32_t x,
+                                             int32_t y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(src)
+                 : "memory");
+}
+
 // TMA store of a 3-D box from this CTA's shared memory (bulk-group
 // completion: commit, then wait before the source is reused or the CTA ends).
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t src, int32_t x,
@@ -241,6 +263,29 @@ template <int N>
 __device__ __forceinline__ void bulk_wait() {
     asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
 }
+
+// One warp stores a 32-row x 32-column bf16 block: lane r holds its row as 16
+// packed bf16 pairs.  The row goes into the warp's 2 KB block of shared memory
+// (512-byte aligned) in the 64-byte swizzled layout, and lane 0 stores the
+// block with one TMA instruction at (x, y) of the map.  The block is reused:
+// the previous store from it must have finished reading first.
+__device__ __forceinline__ void warp_store_bf16_32x32(uint8_t *blk, const uint32_t (&w)[16],
+                                                      const CUtensorMap *map, int x, int y,
+                                                      int lane) {
+    if (lane == 0) bulk_wait_read<0>();
+    __syncwarp();
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<uint4 *>(blk + lane * 64 + ((q ^ ((lane >> 1) & 3)) * 16)) =
+            make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) {
+        tma_store_2d(map, smem_u32(blk), x, y);
+        bulk_commit();
+    }
+}
+
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
