@@ -8,12 +8,13 @@
 // int32 cumulative offsets produced and kept on the device).  AWS Neuron
 // "Expert Parallelism (EP)", "Router Weights" (logits for every expert).
 //
-// Four launches, none of which waits on another CTA:
-//   1. route_logits_topk: per tile of tokens, fp32 logits for all experts in
-//      shared memory (per 512-wide block of j one fused multiply-add chain
-//      over j ascending, the block sums added in block order, so the values
-//      are reproducible bit for bit), then one thread per token selects the
-//      top K and computes the gates.
+// Five launches, none of which waits on another CTA:
+//   1. route_logit_blocks: fp32 block sums of the logits (per 512-wide block
+//      of j one fused multiply-add chain over j ascending), one CTA per
+//      (token tile, block);
+//   1b. route_topk: the block sums added in block order (+ bias), so the
+//      logits are reproducible bit for bit; then one thread per token selects
+//      the top K and computes the gates.
 //   2. route_block_rank: per block of 256 tokens, a per-warp bitmask of the
 //      tokens choosing each expert gives every route its rank among earlier
 //      routes to the same expert inside the block, and the block's count per
@@ -38,67 +39,77 @@ __device__ __forceinline__ bool beats(float a, int ia, float b, int ib) {
     return a > b || (a == b && ia < ib);
 }
 
-// Logit tile: WT x WE warps; a warp covers 16 tokens x 32 experts, each lane
-// 4 tokens x 4 experts (16 independent fma chains, advanced in pairs by packed
-// fp32x2 fma): lane = tx + 8 ty (tx in 0..7, ty in 0..3) owns tokens ty + 4a
-// and experts tx + 8b of its warp's block.  A CTA covers TB = 16 WT tokens and
-// EC = 32 WE experts per pass (passes loop over the experts).  The dot product
-// over j is cut into 512-wide blocks: each chain restarts from 0 at a block
-// boundary and the block sums are added in block order (the order the logits
-// are defined by).  x (bf16) and W_r (fp32) stream through a 4-stage cp.async
-// ring of 32-wide j-chunks in their natural row-major layouts; per 4 j a lane
-// reads 8 bytes of each of its x rows and 16 bytes of each of its W rows (rows
-// padded so that the 8 distinct rows of a warp load hit distinct banks).
-constexpr int kLogitStages = 4;
+// Router logits in two launches.
+//
+// route_logit_blocks: the dot product over j is cut into 512-wide blocks (one
+// fp32 chain per block; the block sums are added in block order, the order
+// the logits are defined by).  CTA (token tile, block b) computes the block
+// sums of 64 tokens x all experts (passes of 64 experts; 128 tokens x 32
+// experts when N <= 32) and writes them to part[b][t][e].  4 warps, each 32
+// tokens x 32 experts; lane = tx +
+// 8 ty (tx in 0..7, ty in 0..3) owns tokens ty + 4i (i = 0..7) and experts
+// tx + 8b (b = 0..3): 32 chains, advanced two tokens at a time by the packed
+// fp32x2 fma.  x (bf16) and W_r (fp32) stream through a 4-stage cp.async ring
+// of 32-wide j-chunks in their natural layouts (rows padded so that a warp
+// load's distinct rows hit distinct banks).  Per 4 j a lane loads 8 x 8 bytes
+// of x and 4 x 16 bytes of W_r for 128 fmas: one byte of shared memory per
+// fma, which the shared-memory port sustains at the fma rate.  Splitting j
+// into blocks gives 4 times the warps of a single chain per logit.
+//
+// route_topk: one CTA per 32 tokens adds the block sums in order (+ bias)
+// into shared memory, then one thread per token selects the top K and
+// computes the gates.
 constexpr int kLogitJC = 32;
 constexpr int kLogitBlock = 512;  // j per block sum (a multiple of kLogitJC)
+constexpr int kLogitStages = 4;
+constexpr int kLogitThreads = 128;
+constexpr int kLogitXR = kLogitJC + 8;  // bf16 per padded x row
+constexpr int kLogitWR = kLogitJC + 4;  // fp32 per padded W row
 
-template <int WT, int WE>
+// WE warps along the experts, 4 / WE along the tokens: 64 tokens x 64
+// experts per pass (WE = 2), or 128 x 32 for N <= 32 (WE = 1)
+template <int WE>
 struct LogitTile {
-    static constexpr int THREADS = 32 * WT * WE;
-    static constexpr int TB = 16 * WT;
+    static constexpr int WT = 4 / WE;
+    static constexpr int TB = 32 * WT;
     static constexpr int EC = 32 * WE;
-    static constexpr int XR = kLogitJC + 8;  // bf16 per padded x row
-    static constexpr int WR = kLogitJC + 4;  // fp32 per padded W row
-    static constexpr int STAGE = TB * XR * 2 + EC * WR * 4;  // bytes
-    static constexpr size_t smem_bytes(int N) {
-        return (size_t)kLogitStages * STAGE + sizeof(float) * (size_t)TB * (N + 1);
-    }
+    static constexpr int STAGE = TB * kLogitXR * 2 + EC * kLogitWR * 4;
+    static constexpr size_t SMEM = (size_t)kLogitStages * STAGE;
 };
 
-template <int WT, int WE>
-__global__ void __launch_bounds__(LogitTile<WT, WE>::THREADS)
-route_logits_topk(int T, int d, int N, int K, const uint16_t *__restrict__ x,
-                  const float *__restrict__ w_r, const float *__restrict__ bias,
-                  int32_t *__restrict__ topk_idx, float *__restrict__ topk_gate) {
-    using L = LogitTile<WT, WE>;
-    constexpr int TB = L::TB, EC = L::EC, XR = L::XR, WR = L::WR, JC = kLogitJC;
-    constexpr int THREADS = L::THREADS;
-    constexpr int CPB = kLogitBlock / JC;  // chunks per block
-    extern __shared__ __align__(16) uint8_t smem_l[];
-    const int LDS = N + 1;  // padded logit row: one thread per token reads its row
-    float *lg = reinterpret_cast<float *>(smem_l + (size_t)kLogitStages * L::STAGE);  // [TB][LDS]
+inline int logit_blocks(int d) { return (d + kLogitBlock - 1) / kLogitBlock; }
 
+template <int WE>
+__global__ void __launch_bounds__(kLogitThreads)
+route_logit_blocks(int T, int d, int N, const uint16_t *__restrict__ x,
+                   const float *__restrict__ w_r, float *__restrict__ part) {
+    using L = LogitTile<WE>;
+    constexpr int JC = kLogitJC, XR = kLogitXR, WR = kLogitWR, TB = L::TB, EC = L::EC;
+    constexpr int kLogitStage = L::STAGE;
+    extern __shared__ __align__(16) uint8_t smem_l[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int tx = lane & 7, ty = lane >> 3;
-    const int tok0 = (warp % WT) * 16 + ty;   // + 4a
-    const int exp0 = (warp / WT) * 32 + tx;   // + 8b
+    const int tok0 = (warp % L::WT) * 32 + ty;   // + 4i
+    const int exp0 = (warp / L::WT) * 32 + tx;   // + 8b
     const int t0 = blockIdx.x * TB;
-    const int nchunks = (d + JC - 1) / JC;
+    const int b = blockIdx.y;
+    const int jb0 = b * kLogitBlock, jlen = min(kLogitBlock, d - jb0);  // a multiple of 8
+    const int nchunks = (jlen + JC - 1) / JC;
+    float *pb = part + (size_t)b * T * N;
 
     for (int ec0 = 0; ec0 < N; ec0 += EC) {
         auto issue = [&](int c) {
             if (c < nchunks) {
-                uint8_t *st = smem_l + (size_t)(c % kLogitStages) * L::STAGE;
+                uint8_t *st = smem_l + (size_t)(c % kLogitStages) * kLogitStage;
                 uint16_t *xs = reinterpret_cast<uint16_t *>(st);
                 float *ws = reinterpret_cast<float *>(st + TB * XR * 2);
-                const int j0 = c * JC, jn = min(JC, d - j0);
-                for (int i = tid; i < TB * (JC / 8); i += THREADS) {
+                const int j0 = jb0 + c * JC, jn = min(JC, jlen - c * JC);
+                for (int i = tid; i < TB * (JC / 8); i += kLogitThreads) {
                     const int r = i / (JC / 8), q = (i % (JC / 8)) * 8;
                     if (t0 + r < T && q < jn)
                         cp_async16(xs + r * XR + q, x + (int64_t)(t0 + r) * d + j0 + q);
                 }
-                for (int i = tid; i < EC * (JC / 4); i += THREADS) {
+                for (int i = tid; i < EC * (JC / 4); i += kLogitThreads) {
                     const int r = i / (JC / 4), q = (i % (JC / 4)) * 4;
                     if (ec0 + r < N && q < jn)
                         cp_async16(ws + r * WR + q, w_r + (int64_t)(ec0 + r) * d + j0 + q);
@@ -107,83 +118,125 @@ route_logits_topk(int T, int d, int N, int K, const uint16_t *__restrict__ x,
             cp_async_commit();
         };
 
-        // acc[ap][b] = the current block's chains (token 2ap, expert b) and
-        // (token 2ap + 1, expert b), advanced together by one paired fma;
-        // tot holds the sum of the finished blocks
-        float2 acc[2][4], tot[2][4];
+        // acc[p][e]: chains (token tok0 + 8p, expert e) and (token tok0 + 8p + 4,
+        // expert e) of this lane, e = exp0 + 8 * (0..3)
+        float2 acc[4][4];
 #pragma unroll
-        for (int a = 0; a < 2; ++a)
+        for (int p = 0; p < 4; ++p)
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                acc[a][q] = make_float2(0.0f, 0.0f);
-                tot[a][q] = make_float2(0.0f, 0.0f);
-            }
-        auto fold = [&](bool first) {
-#pragma unroll
-            for (int a = 0; a < 2; ++a)
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    tot[a][q] = first ? acc[a][q]
-                                      : make_float2(__fadd_rn(tot[a][q].x, acc[a][q].x),
-                                                    __fadd_rn(tot[a][q].y, acc[a][q].y));
-                    acc[a][q] = make_float2(0.0f, 0.0f);
-                }
-        };
+            for (int e = 0; e < 4; ++e) acc[p][e] = make_float2(0.0f, 0.0f);
 
         __syncthreads();  // the previous pass is done with every stage
 #pragma unroll
         for (int c = 0; c < kLogitStages - 1; ++c) issue(c);
         for (int c = 0; c < nchunks; ++c) {
-            if (c > 0 && c % CPB == 0) fold(c == CPB);  // a block boundary
             cp_async_wait<kLogitStages - 2>();
             __syncthreads();
             issue(c + kLogitStages - 1);
-            const uint8_t *st = smem_l + (size_t)(c % kLogitStages) * L::STAGE;
+            const uint8_t *st = smem_l + (size_t)(c % kLogitStages) * kLogitStage;
             const uint16_t *xs = reinterpret_cast<const uint16_t *>(st) + tok0 * XR;
             const float *ws = reinterpret_cast<const float *>(st + TB * XR * 2) + exp0 * WR;
-            const int jn = min(JC, d - c * JC);  // a multiple of 8
-#pragma unroll 4
+            const int jn = min(JC, jlen - c * JC);  // a multiple of 8
+#pragma unroll 2
             for (int j = 0; j < jn; j += 4) {
-                // xp[ap][q] = (x of token 2ap, x of token 2ap + 1) at j + q
-                float2 xp[2][4];
+                uint2 xv[8];  // tokens tok0 + 4i, 4 bf16 at j .. j + 3
 #pragma unroll
-                for (int ap = 0; ap < 2; ++ap) {
-                    const uint2 v0 = *reinterpret_cast<const uint2 *>(xs + 8 * ap * XR + j);
-                    const uint2 v1 = *reinterpret_cast<const uint2 *>(xs + (8 * ap + 4) * XR + j);
-                    xp[ap][0] = make_float2(bf16_lo(v0.x), bf16_lo(v1.x));
-                    xp[ap][1] = make_float2(bf16_hi(v0.x), bf16_hi(v1.x));
-                    xp[ap][2] = make_float2(bf16_lo(v0.y), bf16_lo(v1.y));
-                    xp[ap][3] = make_float2(bf16_hi(v0.y), bf16_hi(v1.y));
-                }
-                float4 wf[4];
+                for (int i = 0; i < 8; ++i) xv[i] = *reinterpret_cast<const uint2 *>(xs + 4 * i * XR + j);
+                float4 wv[4];
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    wf[q] = *reinterpret_cast<const float4 *>(ws + 8 * q * WR + j);
+                for (int e = 0; e < 4; ++e) wv[e] = *reinterpret_cast<const float4 *>(ws + 8 * e * WR + j);
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
+                for (int q = 0; q < 4; ++q) {
 #pragma unroll
-                    for (int eb = 0; eb < 4; ++eb) {
-                        const float w = q == 0 ? wf[eb].x : q == 1 ? wf[eb].y : q == 2 ? wf[eb].z : wf[eb].w;
-                        const float2 w2 = make_float2(w, w);
+                    for (int p = 0; p < 4; ++p) {
+                        const uint32_t a = (q < 2) ? xv[2 * p].x : xv[2 * p].y;
+                        const uint32_t bb = (q < 2) ? xv[2 * p + 1].x : xv[2 * p + 1].y;
+                        const float2 xp = (q & 1) ? make_float2(bf16_hi(a), bf16_hi(bb))
+                                                  : make_float2(bf16_lo(a), bf16_lo(bb));
 #pragma unroll
-                        for (int ap = 0; ap < 2; ++ap) acc[ap][eb] = __ffma2_rn(xp[ap][q], w2, acc[ap][eb]);
+                        for (int e = 0; e < 4; ++e) {
+                            const float w = q == 0 ? wv[e].x : q == 1 ? wv[e].y : q == 2 ? wv[e].z : wv[e].w;
+                            acc[p][e] = __ffma2_rn(xp, make_float2(w, w), acc[p][e]);
+                        }
                     }
+                }
             }
         }
         cp_async_wait<0>();
-        fold(nchunks <= CPB);
 #pragma unroll
-        for (int eb = 0; eb < 4; ++eb) {
-            const int e = ec0 + exp0 + 8 * eb;
-            if (e < N) {
-                const float bb = bias ? bias[e] : 0.0f;
+        for (int p = 0; p < 4; ++p) {
+            const int ta = t0 + tok0 + 8 * p, tb = ta + 4;
 #pragma unroll
-                for (int ap = 0; ap < 2; ++ap) {
-                    const float l0 = tot[ap][eb].x, l1 = tot[ap][eb].y;  // tokens 2ap, 2ap + 1
-                    lg[(tok0 + 8 * ap) * LDS + e] = bias ? __fadd_rn(l0, bb) : l0;
-                    lg[(tok0 + 8 * ap + 4) * LDS + e] = bias ? __fadd_rn(l1, bb) : l1;
+            for (int e = 0; e < 4; ++e) {
+                const int ex = ec0 + exp0 + 8 * e;
+                if (ex >= N) continue;
+                if (ta < T) pb[(int64_t)ta * N + ex] = acc[p][e].x;
+                if (tb < T) pb[(int64_t)tb * N + ex] = acc[p][e].y;
+            }
+        }
+    }
+}
+
+constexpr int kTopkTB = 32;
+
+template <int MAXK>
+__global__ void __launch_bounds__(128)
+route_topk(int T, int N, int K, int nb, const float *__restrict__ part,
+           const float *__restrict__ bias, int32_t *__restrict__ topk_idx,
+           float *__restrict__ topk_gate) {
+    extern __shared__ __align__(16) uint8_t smem_t[];
+    const int LDS = N + 1;  // padded logit row: one thread per token reads its row
+    float *lg = reinterpret_cast<float *>(smem_t);  // [kTopkTB][LDS]
+    const int tid = threadIdx.x;
+    const int t0 = blockIdx.x * kTopkTB;
+    const int tn = min(kTopkTB, T - t0);
+    // the tile's block sums are contiguous in each block's [T][N] array: read
+    // them as float4 (when N allows) with four groups in flight per thread
+    const int64_t tile = (int64_t)t0 * N, n = (int64_t)tn * N;
+    const int64_t plane = (int64_t)T * N;
+    if ((N & 3) == 0) {
+        for (int64_t g0 = tid; g0 < n / 4; g0 += 4 * blockDim.x) {
+            float4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int64_t g = g0 + u * blockDim.x;
+                if (g < n / 4) v[u] = __ldcs(reinterpret_cast<const float4 *>(part + tile) + g);
+            }
+            for (int b = 1; b < nb; ++b) {
+                float4 w[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int64_t g = g0 + u * blockDim.x;
+                    if (g < n / 4)
+                        w[u] = __ldcs(reinterpret_cast<const float4 *>(part + b * plane + tile) + g);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    v[u].x = __fadd_rn(v[u].x, w[u].x);
+                    v[u].y = __fadd_rn(v[u].y, w[u].y);
+                    v[u].z = __fadd_rn(v[u].z, w[u].z);
+                    v[u].w = __fadd_rn(v[u].w, w[u].w);
                 }
             }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int64_t g = g0 + u * blockDim.x;
+                if (g >= n / 4) continue;
+                const float vv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const int i = (int)(4 * g + h), tt = i / N, e = i - tt * N;
+                    lg[tt * LDS + e] = bias ? __fadd_rn(vv[h], bias[e]) : vv[h];
+                }
+            }
+        }
+    } else {
+        for (int i = tid; i < n; i += blockDim.x) {
+            const int tt = i / N, e = i - tt * N;
+            float v = part[tile + i];
+            for (int b = 1; b < nb; ++b) v = __fadd_rn(v, part[b * plane + tile + i]);
+            if (bias) v = __fadd_rn(v, bias[e]);
+            lg[tt * LDS + e] = v;
         }
     }
     __syncthreads();
@@ -191,28 +244,26 @@ route_logits_topk(int T, int d, int N, int K, const uint16_t *__restrict__ x,
     // top-K and gates, one thread per token: the logits stream past a
     // sorted list of the best K so far (logit descending, lower expert first
     // on ties, NaN as -inf); a logit that beats the K-th is swapped down into
-    // place.  The list sits at the end of a kMaxK-entry register array whose
-    // first kMaxK - K entries hold sentinels that nothing beats, so the K-th
+    // place.  The list sits at the end of a MAXK-entry register array whose
+    // first MAXK - K entries hold sentinels that nothing beats, so the K-th
     // is always the last entry and every index is a constant.
-    for (int tt = tid; tt < TB; tt += THREADS) {
+    for (int tt = tid; tt < tn; tt += blockDim.x) {
         const int t = t0 + tt;
         if (t >= T) break;
         const float *l = lg + tt * LDS;
-        const int first = kMaxK - K;
-        float tv[kMaxK];
-        int ti[kMaxK];
+        const int first = MAXK - K;
+        float tv[MAXK];
+        int ti[MAXK];
 #pragma unroll
-        for (int q = 0; q < kMaxK; ++q) {
+        for (int q = 0; q < MAXK; ++q) {
             const bool real = q >= first;
             tv[q] = real ? -INFINITY : INFINITY;
             ti[q] = real ? 0x7FFFFFFF : -1;
         }
-        for (int e = 0; e < N; ++e) {
-            float v = canon(l[e]);
-            if (!beats(v, e, tv[kMaxK - 1], ti[kMaxK - 1])) continue;
-            int ie = e;
+        auto insert = [&](float v, int ie) {
+            if (!beats(v, ie, tv[MAXK - 1], ti[MAXK - 1])) return;
 #pragma unroll
-            for (int q = 0; q < kMaxK; ++q) {
+            for (int q = 0; q < MAXK; ++q) {
                 const bool sw = beats(v, ie, tv[q], ti[q]);
                 const float sv = tv[q];
                 const int si = ti[q];
@@ -221,17 +272,26 @@ route_logits_topk(int T, int d, int N, int K, const uint16_t *__restrict__ x,
                 v = sw ? sv : v;
                 ie = sw ? si : ie;
             }
+        };
+        int e = 0;
+        for (; e + 8 <= N; e += 8) {
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = canon(l[e + u]);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) insert(v[u], e + u);
         }
+        for (; e < N; ++e) insert(canon(l[e]), e);
         float top = 0.0f;
 #pragma unroll
-        for (int q = 0; q < kMaxK; ++q)
+        for (int q = 0; q < MAXK; ++q)
             if (q == first) top = tv[q];
         float sum = 0.0f;
 #pragma unroll
-        for (int q = 0; q < kMaxK; ++q)
+        for (int q = 0; q < MAXK; ++q)
             if (q >= first) sum += (tv[q] == top) ? 1.0f : expf(tv[q] - top);
 #pragma unroll
-        for (int q = 0; q < kMaxK; ++q) {
+        for (int q = 0; q < MAXK; ++q) {
             if (q >= first) {
                 const float ex = (tv[q] == top) ? 1.0f : expf(tv[q] - top);
                 topk_idx[(int64_t)t * K + (q - first)] = ti[q];
@@ -348,46 +408,66 @@ __global__ void route_assign(int T, int N, int K, int cap, const int32_t *__rest
     route_row[i] = slot < cap ? expert_offset[e] + slot : -1;
 }
 
-template <int WT, int WE>
 moe_status launch_logits(const moe_shape *s, const uint16_t *x, const float *w, const float *b,
-                         int32_t *idx, float *gate, cudaStream_t st) {
-    using L = LogitTile<WT, WE>;
-    const size_t smem = L::smem_bytes(s->N);
-    static size_t configured = 0;
-    if (smem > 48 * 1024 && smem > configured) {
-        if (cudaFuncSetAttribute(route_logits_topk<WT, WE>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem) != cudaSuccess)
+                         int32_t *idx, float *gate, float *part, cudaStream_t st) {
+    static bool configured = false;
+    if (!configured) {
+        if (cudaFuncSetAttribute(route_logit_blocks<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)LogitTile<1>::SMEM) != cudaSuccess ||
+            cudaFuncSetAttribute(route_logit_blocks<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)LogitTile<2>::SMEM) != cudaSuccess ||
+            cudaFuncSetAttribute(route_topk<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)(sizeof(float) * kTopkTB * (kMaxN + 1))) != cudaSuccess ||
+            cudaFuncSetAttribute(route_topk<kMaxK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)(sizeof(float) * kTopkTB * (kMaxN + 1))) != cudaSuccess)
             return MOE_ERR_CUDA;
-        configured = smem;
+        configured = true;
     }
-    const int grid = (s->T + L::TB - 1) / L::TB;
-    route_logits_topk<WT, WE><<<grid, L::THREADS, smem, st>>>(s->T, s->d, s->N, s->K, x, w, b, idx,
-                                                              gate);
+    const int nb = logit_blocks(s->d);
+    if (s->N <= 32) {
+        const dim3 grid((s->T + LogitTile<1>::TB - 1) / LogitTile<1>::TB, nb);
+        route_logit_blocks<1><<<grid, kLogitThreads, LogitTile<1>::SMEM, st>>>(s->T, s->d, s->N, x,
+                                                                             w, part);
+    } else {
+        const dim3 grid((s->T + LogitTile<2>::TB - 1) / LogitTile<2>::TB, nb);
+        route_logit_blocks<2><<<grid, kLogitThreads, LogitTile<2>::SMEM, st>>>(s->T, s->d, s->N, x,
+                                                                             w, part);
+    }
+    moe_status r = launch_status();
+    if (r != MOE_OK) return r;
+    const size_t tsmem = sizeof(float) * kTopkTB * (s->N + 1);
+    auto *topk = s->K <= 8 ? route_topk<8> : route_topk<kMaxK>;
+    topk<<<(s->T + kTopkTB - 1) / kTopkTB, 128, tsmem, st>>>(s->T, s->N, s->K, nb, part, b, idx,
+                                                           gate);
     return launch_status();
 }
 
 }  // namespace
 
-size_t route_ws_bytes(const moe_shape *s) {
+inline size_t route_block_count_bytes(const moe_shape *s) {
     const size_t nblk = (size_t)(s->T + kRankBlock - 1) / kRankBlock;
-    const size_t bc = (nblk * (size_t)s->N * sizeof(int32_t) + 255) & ~(size_t)255;
-    return 256 + bc;
+    return (nblk * (size_t)s->N * sizeof(int32_t) + 255) & ~(size_t)255;
 }
 
-// Enqueues the four routing kernels; `status` is the device status word and
-// `block_count` a [ceil(T/256), N] int32 scratch array.
+// status word (256 B), the per-block count array, then the logit block sums
+// [ceil(d / 512)][T][N] fp32
+size_t route_ws_bytes(const moe_shape *s) {
+    const size_t part = (size_t)logit_blocks(s->d) * s->T * s->N * sizeof(float);
+    return 256 + route_block_count_bytes(s) + ((part + 255) & ~(size_t)255);
+}
+
+// Enqueues the routing kernels; `scratch` is the workspace past its status
+// word (route_ws_bytes(s) - 256 bytes).
 moe_status route_enqueue(const moe_shape *s, const moe_bf16 *x, const float *w_router,
                          const float *bias, int32_t *topk_idx, float *topk_gate,
                          int32_t *route_row, int32_t *expert_count, int32_t *expert_offset,
-                         int32_t *expert_demand, int32_t *block_count, cudaStream_t st) {
+                         int32_t *expert_demand, void *scratch, cudaStream_t st) {
     const int nblk = (s->T + kRankBlock - 1) / kRankBlock;
+    int32_t *block_count = static_cast<int32_t *>(scratch);
+    float *part = reinterpret_cast<float *>(static_cast<char *>(scratch) + route_block_count_bytes(s));
     moe_status r = MOE_OK;
     if (s->T > 0) {
-        const int n = s->N;
-        if (n <= 32) r = launch_logits<2, 1>(s, x, w_router, bias, topk_idx, topk_gate, st);
-        else if (n <= 64) r = launch_logits<2, 2>(s, x, w_router, bias, topk_idx, topk_gate, st);
-        else r = launch_logits<2, 4>(s, x, w_router, bias, topk_idx, topk_gate, st);
+        r = launch_logits(s, x, w_router, bias, topk_idx, topk_gate, part, st);
         if (r != MOE_OK) return r;
         const size_t smem = sizeof(uint32_t) * 2 * (kRankBlock / 32) * (size_t)s->N;
         static bool configured = false;
@@ -440,9 +520,8 @@ MOE_API moe_status moe_route(const moe_shape *s, const moe_bf16 *x, const float 
         !aligned16(route_row) || !aligned16(expert_count) || !aligned16(expert_offset) ||
         !aligned16(expert_demand) || (bias && !aligned16(bias)))
         return MOE_ERR_ALIGNMENT;
-    int32_t *block_count = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + 256);
     return route_enqueue(s, x, w_router, bias, topk_idx, topk_gate, route_row, expert_count,
-                         expert_offset, expert_demand, block_count, stream);
+                         expert_offset, expert_demand, static_cast<char *>(ws) + 256, stream);
 }
 
 // ------------------------------------------------------------------------
@@ -505,7 +584,6 @@ MOE_API moe_status moe_route_noalloc(const moe_shape *s, const moe_bf16 *x, cons
     if (route_ws_bytes(s) > kNoAllocScratchBytes) return MOE_ERR_UNSUPPORTED;
     void *base = nullptr;
     if ((r = noalloc_scratch(&base)) != MOE_OK) return r;
-    int32_t *block_count = reinterpret_cast<int32_t *>(static_cast<char *>(base) + 256);
     return route_enqueue(s, x, w_router, bias, topk_idx, topk_gate, route_row, expert_count,
-                         expert_offset, expert_demand, block_count, stream);
+                         expert_offset, expert_demand, static_cast<char *>(base) + 256, stream);
 }

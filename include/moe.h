@@ -130,11 +130,13 @@ moe_status moe_route(const moe_shape *s, const moe_bf16 *x, const float *w_route
  *
  * Same arguments, outputs and results as moe_route.  The scratch that
  * moe_route keeps in `ws` lives instead in a fixed device array of
- * MOE_ROUTE_NOALLOC_SCRATCH_BYTES (1 MiB) inside this library; every GPU that
+ * MOE_ROUTE_NOALLOC_SCRATCH_BYTES (64 MiB) inside this library; every GPU that
  * loads the library holds that array until the process exits.  The call
- * allocates nothing.  Shapes whose scratch (moe_route_workspace_bytes) would
- * exceed the array -- roughly ceil(T / 256) * N > 262,000 -- are rejected
- * with MOE_ERR_UNSUPPORTED before anything is enqueued.
+ * allocates nothing.  Shapes whose scratch (moe_route_workspace_bytes: the
+ * per-block counts, 4 * ceil(T / 256) * N bytes, and the logit block sums,
+ * 4 * ceil(d / 512) * T * N bytes) would exceed the array -- roughly
+ * ceil(d / 512) * T * N > 16.7 million -- are rejected with
+ * MOE_ERR_UNSUPPORTED before anything is enqueued.
  *
  * The first call on a device looks up the array's device address there
  * (cudaGetSymbolAddress, with that device current); make that first call
@@ -143,7 +145,7 @@ moe_status moe_route(const moe_shape *s, const moe_bf16 *x, const float *w_route
  * that overlap on the GPU (e.g. on two streams at once) race on the array.
  * Device-side errors cannot be read back through moe_read_device_error here.
  */
-#define MOE_ROUTE_NOALLOC_SCRATCH_BYTES ((size_t)1 << 20)
+#define MOE_ROUTE_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 moe_status moe_route_noalloc(const moe_shape *s, const moe_bf16 *x, const float *w_router,
                              const float *bias, int32_t *topk_idx, float *topk_gate,
                              int32_t *route_row, int32_t *expert_count, int32_t *expert_offset,

@@ -84,7 +84,7 @@ def test_route_noalloc_matches_route_on_two_calls_in_a_row(moe):
 
 
 def test_route_noalloc_refuses_shapes_past_its_scratch(moe):
-    s = moe.Shape(70000, 64, 1024, 2, 64, 1)   # ceil(70000/256) * 1024 counts > 1 MiB
+    s = moe.Shape(70000, 64, 1024, 2, 64, 1)   # 70000 x 1024 fp32 logit block sums > 64 MiB
     P = ctypes.c_void_p(4096)
     rc = moe.lib().moe_route_noalloc(ctypes.byref(s), P, P, None, P, P, P, P, P, P, None)
     assert rc == 5  # MOE_ERR_UNSUPPORTED, before anything is enqueued
