@@ -286,6 +286,24 @@ def run_ours(args, cfg, rank, world):
         e_ms.append(e0.elapsed_time(e1))
     e2e_ms = float(np.mean(e_ms))
 
+    # dispatch fused into GEMM1 (moe_expert_ffn_gather): the same expert
+    # outputs without x_disp; timed here on the same routing for comparison
+    fused_ms = None
+    if not cfg.backward:
+        f_ms = []
+        for i in range(max(5, min(args.steps, 20))):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            moe.expert_ffn_gather(shape, x, buf.route_row, buf.expert_count, buf.expert_offset, wg,
+                                  wu, wd, buf.h_act, buf.g_save, buf.u_save, buf.y_disp,
+                                  buf.gather_ws)
+            e1.record(stream)
+            e1.synchronize()
+            f_ms.append(e0.elapsed_time(e1))
+        assert moe.read_device_error(buf.gather_ws) == 0
+        fused_ms = float(np.median(f_ms[2:]))
+
     if rank != 0:
         if dist:
             dist.destroy_process_group()
@@ -337,6 +355,10 @@ def run_ours(args, cfg, rank, world):
         "clocks": clocks,
         "wall_s_timed_region": t_wall,
     }
+    if fused_ms is not None:
+        line["fused_dispatch_ffn"] = {
+            "ms": fused_ms, "two_step_ms": ph_ms["dispatch"] + ph_ms["ffn"],
+            "note": "moe_expert_ffn_gather (x rows fetched by TMA gather4 in GEMM1) vs dispatch + expert_ffn"}
     if cfg.backward:
         bt = alg["gemm_bwd_flop"] / (ph_ms["ffn_bwd"] / 1e3) / 1e12
         line["backward"] = {

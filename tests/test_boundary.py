@@ -143,3 +143,40 @@ def test_product_path_refuses_to_run_without_library(tmp_path):
     r = subprocess.run([sys.executable, "-c", "import combine_expert_gemm_gb300"],
                        capture_output=True, text=True, cwd=tmp_path)
     assert r.returncode != 0 and "no CPU fallback" in r.stderr
+
+
+def test_fused_entry_points_argument_errors(moe):
+    """moe_expert_ffn_gather, moe_dispatch_router_backward and
+    moe_router_weight_backward refuse bad arguments before enqueuing anything
+    (every call here fails validation, so nothing reaches a GPU)."""
+    s = _shape(moe)
+    lib = moe.lib()
+    A, mis = ctypes.c_void_p(4096), ctypes.c_void_p(4096 + 8)
+    ws_g = lib.moe_expert_ffn_gather_workspace_bytes(ctypes.byref(s))
+    assert ws_g >= 256 + 4 * s.R
+    args = [A] * 11                                    # x .. y_disp
+    assert lib.moe_expert_ffn_gather(ctypes.byref(s), *args, A, ws_g - 1, None) == 3
+    assert lib.moe_expert_ffn_gather(ctypes.byref(s), *args, mis, ws_g, None) == 3
+    bad = list(args); bad[1] = None                    # route_row
+    assert lib.moe_expert_ffn_gather(ctypes.byref(s), *bad, A, ws_g, None) == 1
+    bad = list(args); bad[0] = mis                     # x misaligned
+    assert lib.moe_expert_ffn_gather(ctypes.byref(s), *bad, A, ws_g, None) == 2
+    bad = list(args); bad[8] = None                    # g_save given without u_save
+    assert lib.moe_expert_ffn_gather(ctypes.byref(s), *bad, A, ws_g, None) == 1
+    s2 = _shape(moe, d=136)
+    assert lib.moe_expert_ffn_gather(ctypes.byref(s2), *args, A, ws_g, None) == 5
+
+    d8 = [A] * 8                                       # dx_disp .. dx
+    bad = list(d8); bad[3] = None                      # topk_idx
+    assert lib.moe_dispatch_router_backward(ctypes.byref(s), *bad, None) == 1
+    bad = list(d8); bad[6] = mis                       # dlogit misaligned
+    assert lib.moe_dispatch_router_backward(ctypes.byref(s), *bad, None) == 2
+    assert lib.moe_dispatch_router_backward(ctypes.byref(_shape(moe, K=0)), *d8, None) == 1
+
+    ws_r = lib.moe_router_backward_workspace_bytes(ctypes.byref(s))
+    w5 = [A] * 4 + [None]                              # x, topk_idx, dlogit, dw_router, dbias
+    assert lib.moe_router_weight_backward(ctypes.byref(s), *w5, A, ws_r - 1, None) == 3
+    bad = list(w5); bad[3] = None                      # dw_router
+    assert lib.moe_router_weight_backward(ctypes.byref(s), *bad, A, ws_r, None) == 1
+    bad = list(w5); bad[0] = mis                       # x misaligned
+    assert lib.moe_router_weight_backward(ctypes.byref(s), *bad, A, ws_r, None) == 2
