@@ -19,7 +19,12 @@
 //   warps 2-9  epilogue (two warps per TMEM lane quadrant, each half of the
 //              columns): tcgen05.ld of this CTA's 128 accumulator rows, then
 //              SwiGLU (F1: columns 0-127 are the gate rows, loaded by the leader,
-//              128-255 the up rows, loaded by the peer) or a bf16 store (F2).
+//              128-255 the up rows, loaded by the peer) or a bf16 copy (F2);
+//              a warp whose 32 rows are all valid writes each 32 x 32 output
+//              block to its 2 KB of shared memory (64-byte swizzle) and stores
+//              it with one TMA instruction; other warps store their valid rows.
+// With GATHER (moe_expert_ffn_gather) the F1 producer reads A rows straight
+// from x by route (tile::gather4 loads), so no dispatched copy is made.
 // Work list: every CTA derives, from expert_count in device memory, the tiles
 // of every expert (ceil(count/256) row tiles x output-column tiles) and walks
 // them round-robin.  Rows past an expert's count (the next expert's rows or

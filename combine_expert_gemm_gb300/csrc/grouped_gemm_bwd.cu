@@ -17,7 +17,8 @@
 // tiles, one tcgen05.mma.cta_group::2 per K-step, each CTA holding its own 128
 // rows of A and half of B, 32 KB per k-block in a 6-stage ring; persistent,
 // 128-byte swizzle, one thread of the leader issuing MMAs into a double-
-// buffered TMEM accumulator, eight epilogue warps per CTA.  The backward
+// buffered TMEM accumulator, eight epilogue warps per CTA whose full 32-row
+// output blocks leave through swizzled shared memory by TMA store.  The backward
 // operands that are transposed relative to their storage (weights in dgrad,
 // activations in wgrad) are read MN-major: a TMA box of 64 M/N elements x 64 K
 // rows lands as 64 swizzled 128-byte rows and the MMA descriptor walks it with

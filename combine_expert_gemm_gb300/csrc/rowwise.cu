@@ -9,7 +9,9 @@
 //
 // One warp per token; every access is a 16-byte vector (8 bf16); the K route
 // rows and gates of the token are read once by lanes 0..K-1 and broadcast with
-// shuffles.  All four kernels are HBM-bound.
+// shuffles.  All four kernels are HBM-bound.  The dispatch backward can also
+// add the router's share of dx (and write dlogit) in the same pass over the
+// token's rows.
 #include "moe_common.cuh"
 
 namespace moe {

@@ -36,6 +36,9 @@ SMALL = {
     "cap0": MoEConfig("cap0", T=100, d=64, N=8, K=2, h=64, cf_num=0, cf_den=1, seed=16),
     "N1024": MoEConfig("N1024", T=300, d=64, N=1024, K=16, h=64, cf_num=1, cf_den=1, seed=17),
     "N200": MoEConfig("N200", T=600, d=192, N=200, K=6, h=64, cf_num=2, cf_den=1, seed=18),
+    # three 512-wide logit blocks, the last one ragged (64 wide)
+    "multi_block": MoEConfig("multi_block", T=333, d=1088, N=24, K=3, h=128, cf_num=5, cf_den=4,
+                             seed=19),
 }
 
 
