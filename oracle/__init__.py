@@ -49,6 +49,12 @@ def _declare(L):
         "oracle_expert_ffn_bwd": [_I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                   _P, _P],
         "oracle_router_bwd": [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P],
+        "oracle_mx_quantize_f64": [_I64, _I, _P, _P, _P],
+        "oracle_mx_quantize_bf16": [_I64, _I, _P, _P, _P],
+        "oracle_mx_dequantize": [_I64, _I, _P, _P, _P],
+        "oracle_expert_ffn_mx": [_I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                 _P, _P],
+        "oracle_combine_mx": [_I, _I, _I, _P, _P, _P, _P, _P],
     }
     for name, args in sig.items():
         f = getattr(L, name)
@@ -284,4 +290,80 @@ def layer_forward(x, w_r, bias, wg, wu, wd, K, cap, save=False):
                                        wg, wu, wd, save=save)
     y = combine(y_disp, r["route_row"], r["topk_gate"])
     r.update(x_disp=x_disp, h_act=h_act, g_save=gs, u_save=us, y_disp=y_disp, y=y)
+    return r
+
+
+# ------------------------------------------------------------------- MXFP8 --
+
+def mx_quantize(v):
+    """MXFP8 of the rows of v (last dimension a multiple of 32): returns codes
+    (uint8, same shape) and E8M0 scale bytes (uint8, last dimension / 32).
+    uint16 input is read as bf16 bit patterns, anything else as float64."""
+    v = np.asarray(v)
+    k = v.shape[-1]
+    rows = int(np.prod(v.shape[:-1], dtype=np.int64))
+    q = np.empty(v.shape, dtype=np.uint8)
+    sc = np.empty(v.shape[:-1] + (k // 32,), dtype=np.uint8)
+    if v.dtype == np.uint16:
+        v = _c(v, np.uint16)
+        lib().oracle_mx_quantize_bf16(rows, k, _p(v), _p(q), _p(sc))
+    else:
+        v = _c(v, np.float64)
+        lib().oracle_mx_quantize_f64(rows, k, _p(v), _p(q), _p(sc))
+    return q, sc
+
+
+def mx_dequantize(q, sc):
+    """float64 values of MXFP8 codes q with scale bytes sc (one per 32 along the last dimension)."""
+    q = _c(q, np.uint8); sc = _c(sc, np.uint8)
+    k = q.shape[-1]
+    rows = int(np.prod(q.shape[:-1], dtype=np.int64))
+    out = np.empty(q.shape, dtype=np.float64)
+    lib().oracle_mx_dequantize(rows, k, _p(q), _p(sc), _p(out))
+    return out
+
+
+def expert_ffn_mx(xq, xs, count, offset, wg, wu, wd, fill=0):
+    """Grouped MXFP8 SwiGLU experts.  wg, wu, wd are (codes, scales) pairs of
+    shapes [N,h,d]/[N,h,d/32] and [N,d,h]/[N,d,h/32].  Returns hq, hs, yq, ys
+    (row-major scale rows); rows outside the experts' intervals keep ``fill``."""
+    xq = _c(xq, np.uint8); xs = _c(xs, np.uint8)
+    count = _c(count, np.int32); offset = _c(offset, np.int32)
+    (wgq, wgs), (wuq, wus), (wdq, wds) = [(_c(a, np.uint8), _c(b, np.uint8)) for a, b in (wg, wu, wd)]
+    R, d = xq.shape
+    N, h, _ = wgq.shape
+    hq = np.full((R, h), fill, np.uint8); hs = np.full((R, h // 32), fill, np.uint8)
+    yq = np.full((R, d), fill, np.uint8); ys = np.full((R, d // 32), fill, np.uint8)
+    lib().oracle_expert_ffn_mx(N, d, h, _p(count), _p(offset), _p(xq), _p(xs), _p(wgq), _p(wgs),
+                               _p(wuq), _p(wus), _p(wdq), _p(wds), _p(hq), _p(hs), _p(yq), _p(ys))
+    return hq, hs, yq, ys
+
+
+def combine_mx(yq, ys, route_row, gate):
+    """Gate-weighted sum of dequantized expert rows into token order (bf16 result)."""
+    yq = _c(yq, np.uint8); ys = _c(ys, np.uint8)
+    route_row = _c(route_row, np.int32); gate = _c(gate, np.float32)
+    T, K = route_row.shape
+    d = yq.shape[1]
+    y = np.empty((T, d), dtype=np.uint16)
+    lib().oracle_combine_mx(T, d, K, _p(yq), _p(ys), _p(route_row), _p(gate), _p(y))
+    return y
+
+
+def layer_forward_mx(x, w_r, bias, wg, wu, wd, K, cap):
+    """The MXFP8 layer: route as in bf16; token rows quantized as they are
+    dispatched; MXFP8 experts; quantized outputs combined.  Weights are bf16
+    and quantized here along each product's reduction dimension."""
+    r = route(x, w_r, bias, K, cap)
+    N = w_r.shape[0]
+    R = min(N * cap, x.shape[0] * K)
+    xq_tok, xs_tok = mx_quantize(x)
+    xq = np.zeros((R, x.shape[1]), np.uint8); xs = np.zeros((R, x.shape[1] // 32), np.uint8)
+    rr = r["route_row"]
+    for t, k in zip(*np.nonzero(rr >= 0)):
+        xq[rr[t, k]] = xq_tok[t]; xs[rr[t, k]] = xs_tok[t]
+    wq = [mx_quantize(w) for w in (wg, wu, wd)]
+    hq, hs, yq, ys = expert_ffn_mx(xq, xs, r["expert_count"], r["expert_offset"], *wq)
+    y = combine_mx(yq, ys, rr, r["topk_gate"])
+    r.update(xq=xq, xs=xs, w_mx=wq, hq=hq, hs=hs, yq=yq, ys=ys, y=y)
     return r

@@ -4,7 +4,8 @@
  * A plain, slow, single-threaded CPU statement of what the routed-expert
  * (MoE) layer computes: router logits, top-K gates, fixed-capacity slot
  * assignment, rowwise dispatch, bias-free SwiGLU experts, gate-weighted
- * combine, and the backward of combine, experts and dispatch.
+ * combine, the backward of combine, experts, dispatch and router, and the
+ * MXFP8 variant of dispatch, experts and combine.
  *
  * Only the tests, the smoke check and the benchmark's CPU-baseline leg may
  * load this library.  It shares no source with the CUDA path.
@@ -38,7 +39,12 @@
  *     silu(z) = z / (1 + exp(-z)); reductions in fp64; bf16 rounding (nearest
  *     even) only where a payload is stored (H, Y, saved G/U, dG/dU, dX);
  *   - combine / dispatch backward: fp32 accumulation over k ascending from 0;
- *     dropped routes add nothing and the kept gates are not renormalised.
+ *     dropped routes add nothing and the kept gates are not renormalised;
+ *   - MXFP8 variant ([EP] 5.4, 5.7, 5.8 name E4M3 data with E8M0 scales but
+ *     not the format's rules): the OCP Microscaling (MX) v1.0 definition,
+ *     blocks of 32 along each product's reduction dimension, shared exponent
+ *     floor(log2 max|v|) - 8, elements rounded to nearest even and saturated
+ *     at 448; G, U, H and Y in fp64 between the quantization points.
  */
 #include <math.h>
 #include <stdint.h>
@@ -504,4 +510,171 @@ void oracle_router_bwd(int T, int d, int N, int K, const uint16_t *x, const floa
     free(accb);
     free(dl);
     free(row);
+}
+
+/* ================================================================ MXFP8 ===
+ * [EP] 5.4 (rows are quantized as they are dispatched; the grouped GEMM reads
+ * the quantized data and its scales as they arrived; the experts' outputs go
+ * back quantized and are dequantized by the local reduction), 5.7 (a quantized
+ * route carries a data row and a scale row at the same destination row and
+ * with the same validity as the bf16 row), 5.8 (data in E4M3, scales in E8M0,
+ * both expert GEMMs in MXFP8).
+ * The pages name the format but not its rules.  Reading: MXFP8 as the OCP
+ * Microscaling (MX) v1.0 specification defines it -- blocks of 32 consecutive
+ * elements along a row share one power-of-two scale X = 2^E, stored as the
+ * E8M0 byte E + 127, with E = floor(log2(max |v|)) - 8 (8 is the exponent of
+ * the largest E4M3 normal, 448 = 1.75 * 2^8) clamped to [-127, 127]; each
+ * element is stored as v / X rounded to the nearest E4M3 value, ties to the
+ * even code, magnitudes past 448 saturating to 448.  An all-zero block gets
+ * E = -127 (byte 0).  Inputs are finite.
+ */
+
+/* E4M3 code -> value: sign bit 7, exponent bits 6-3 (bias 7), mantissa bits
+ * 2-0; exponent field 0 holds the subnormals m * 2^-9; S.1111.111 is NaN and
+ * there are no infinities. */
+static double e4m3_value(uint8_t c) {
+    int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    if (e == 15 && m == 7) return NAN;
+    double v = e == 0 ? ldexp((double)m, -9) : ldexp(1.0 + m / 8.0, e - 7);
+    return s ? -v : v;
+}
+
+/* value -> the nearest finite E4M3 code by exhaustive search over the 127
+ * non-negative finite codes (ties: the code whose mantissa LSB is 0); the sign
+ * is copied, so values that round to zero keep it. */
+static uint8_t e4m3_nearest(double v) {
+    static double table[127];
+    static int ready = 0;
+    if (!ready) {
+        for (int c = 0; c < 127; ++c) table[c] = e4m3_value((uint8_t)c);
+        ready = 1;
+    }
+    double a = fabs(v), best_d = INFINITY;
+    int best = 0;
+    for (int c = 0; c < 127; ++c) {
+        double dist = fabs(table[c] - a);
+        if (dist < best_d || (dist == best_d && (c & 1) == 0)) {
+            best_d = dist;
+            best = c;
+        }
+    }
+    return (uint8_t)(best | (signbit(v) ? 0x80 : 0));
+}
+
+/* Shared exponent E of one block (see the reading above). */
+static int mx_block_exponent(const double *v, int n) {
+    double amax = 0.0;
+    for (int i = 0; i < n; ++i) amax = fmax(amax, fabs(v[i]));
+    if (amax == 0.0) return -127;
+    int e;
+    frexp(amax, &e); /* amax = m * 2^e, 0.5 <= m < 1, so floor(log2 amax) = e - 1 */
+    int E = (e - 1) - 8;
+    return E < -127 ? -127 : (E > 127 ? 127 : E);
+}
+
+#define MX_BLOCK 32
+
+/* rows x k values (k a multiple of 32) -> codes q [rows, k] and E8M0 scale
+ * bytes [rows, k / 32], row-major. */
+void oracle_mx_quantize_f64(int64_t rows, int k, const double *v, uint8_t *q, uint8_t *scale) {
+    const int nb = k / MX_BLOCK;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int b = 0; b < nb; ++b) {
+            const double *blk = v + r * k + (int64_t)b * MX_BLOCK;
+            int E = mx_block_exponent(blk, MX_BLOCK);
+            scale[r * nb + b] = (uint8_t)(E + 127);
+            for (int i = 0; i < MX_BLOCK; ++i)
+                q[r * k + (int64_t)b * MX_BLOCK + i] = e4m3_nearest(ldexp(blk[i], -E));
+        }
+}
+
+void oracle_mx_quantize_bf16(int64_t rows, int k, const uint16_t *x, uint8_t *q, uint8_t *scale) {
+    double *v = (double *)malloc((size_t)k * sizeof(double));
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int i = 0; i < k; ++i) v[i] = (double)bf16_to_f32(x[r * k + i]);
+        oracle_mx_quantize_f64(1, k, v, q + r * k, scale + r * (k / MX_BLOCK));
+    }
+    free(v);
+}
+
+/* codes and scale bytes -> values: e4m3(q) * 2^(scale - 127); a scale byte of
+ * 255 (NaN) gives NaN. */
+void oracle_mx_dequantize(int64_t rows, int k, const uint8_t *q, const uint8_t *scale,
+                          double *out) {
+    const int nb = k / MX_BLOCK;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int i = 0; i < k; ++i) {
+            uint8_t s = scale[r * nb + i / MX_BLOCK];
+            out[r * k + i] = s == 255 ? NAN : ldexp(e4m3_value(q[r * k + i]), (int)s - 127);
+        }
+}
+
+/* Grouped SwiGLU experts in MXFP8 over each expert's valid rows ([EP] 5.4,
+ * 5.8; [SYNC] 8.5).  Inputs: dispatched rows xq [R, d] with scales xs [R, d/32];
+ * weights wgq, wuq [N, h, d] with scales [N, h, d/32] and wdq [N, d, h] with
+ * scales [N, d, h/32] (blocks run along each product's reduction dimension).
+ * Per valid row, in fp64 on the dequantized values:
+ *   g = x Wg^T, u = x Wu^T, a = silu(g) * u, (hq, hs) = MX(a) along h,
+ *   y = deq(hq, hs) Wd^T, (yq, ys) = MX(y) along d.
+ * Rows outside every expert's interval are left untouched. */
+void oracle_expert_ffn_mx(int N, int d, int h, const int32_t *count, const int32_t *offset,
+                          const uint8_t *xq, const uint8_t *xs, const uint8_t *wgq,
+                          const uint8_t *wgs, const uint8_t *wuq, const uint8_t *wus,
+                          const uint8_t *wdq, const uint8_t *wds, uint8_t *hq, uint8_t *hs,
+                          uint8_t *yq, uint8_t *ys) {
+    const int64_t hd = (int64_t)h * d;
+    double *wg = (double *)malloc((size_t)hd * sizeof(double));
+    double *wu = (double *)malloc((size_t)hd * sizeof(double));
+    double *wd = (double *)malloc((size_t)hd * sizeof(double));
+    double *x = (double *)malloc((size_t)d * sizeof(double));
+    double *a = (double *)malloc((size_t)h * sizeof(double));
+    double *ad = (double *)malloc((size_t)h * sizeof(double));
+    double *y = (double *)malloc((size_t)d * sizeof(double));
+    for (int e = 0; e < N; ++e) {
+        if (count[e] <= 0) continue;
+        oracle_mx_dequantize(h, d, wgq + e * hd, wgs + e * hd / MX_BLOCK, wg);
+        oracle_mx_dequantize(h, d, wuq + e * hd, wus + e * hd / MX_BLOCK, wu);
+        oracle_mx_dequantize(d, h, wdq + e * hd, wds + e * hd / MX_BLOCK, wd);
+        for (int i = 0; i < count[e]; ++i) {
+            const int64_t r = (int64_t)offset[e] + i;
+            oracle_mx_dequantize(1, d, xq + r * d, xs + r * (d / MX_BLOCK), x);
+            for (int c = 0; c < h; ++c) {
+                double g = 0.0, u = 0.0;
+                for (int j = 0; j < d; ++j) {
+                    g += x[j] * wg[(int64_t)c * d + j];
+                    u += x[j] * wu[(int64_t)c * d + j];
+                }
+                a[c] = silu(g) * u;
+            }
+            oracle_mx_quantize_f64(1, h, a, hq + r * h, hs + r * (h / MX_BLOCK));
+            oracle_mx_dequantize(1, h, hq + r * h, hs + r * (h / MX_BLOCK), ad);
+            for (int o = 0; o < d; ++o) {
+                double s = 0.0;
+                for (int c = 0; c < h; ++c) s += ad[c] * wd[(int64_t)o * h + c];
+                y[o] = s;
+            }
+            oracle_mx_quantize_f64(1, d, y, yq + r * d, ys + r * (d / MX_BLOCK));
+        }
+    }
+    free(wg); free(wu); free(wd); free(x); free(a); free(ad); free(y);
+}
+
+/* Combine of quantized expert outputs ([EP] 5.4: the reduction dequantizes):
+ * y[t] = bf16( sum over k ascending (route_row >= 0) of gate[t, k] *
+ * deq(yq, ys)[route_row[t, k]] ), fp32 fused multiply-add chain from 0; the
+ * dequantized values are exact in fp32. */
+void oracle_combine_mx(int T, int d, int K, const uint8_t *yq, const uint8_t *ys,
+                       const int32_t *route_row, const float *gate, uint16_t *y) {
+    for (int t = 0; t < T; ++t)
+        for (int j = 0; j < d; ++j) {
+            float acc = 0.0f;
+            for (int k = 0; k < K; ++k) {
+                int32_t r = route_row[(int64_t)t * K + k];
+                if (r < 0) continue;
+                uint8_t s = ys[(int64_t)r * (d / MX_BLOCK) + j / MX_BLOCK];
+                float v = (float)ldexp(e4m3_value(yq[(int64_t)r * d + j]), (int)s - 127);
+                acc = fmaf(gate[(int64_t)t * K + k], v, acc);
+            }
+            y[(int64_t)t * d + j] = bf16_from_f32(acc);
+        }
 }
