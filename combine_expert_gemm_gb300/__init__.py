@@ -1,4 +1,5 @@
-"""Python binding of the routed-expert layer C ABI (``include/moe.h``).
+"""Python binding of the routed-expert layer C ABI (``include/moe.h`` and
+``include/moe_mxfp8.h``).
 
 Argument marshalling only: every step of the layer runs in the sm_103a
 kernels of ``_build/libmoe_gb300.so``.  Tensors are torch CUDA tensors (the
@@ -20,7 +21,9 @@ __all__ = ["Shape", "MoEError", "lib", "route", "dispatch", "expert_ffn", "combi
            "combine_backward", "dispatch_backward", "read_device_error",
            "route_workspace_bytes", "expert_ffn_workspace_bytes", "capacity", "LayerBuffers",
            "layer_forward", "expert_ffn_backward", "expert_ffn_backward_workspace_bytes",
-           "BackwardBuffers", "layer_backward"]
+           "BackwardBuffers", "layer_backward", "MxWeights", "MxLayerBuffers", "mx_act_scale_bytes",
+           "mx_quantize_weights", "dispatch_mxfp8", "expert_ffn_mxfp8", "combine_mxfp8",
+           "layer_forward_mxfp8"]
 
 if not os.path.exists(LIB):
     raise ImportError(f"{LIB} is missing: build it with `python combine_expert_gemm_gb300/build.py` "
@@ -70,6 +73,11 @@ _SIG = {
     "moe_router_weight_backward": ([_SP] + [_P] * 5 + [_P, _SZ, _P], ctypes.c_int),
     "moe_expert_ffn_gather_workspace_bytes": ([_SP], _SZ),
     "moe_expert_ffn_gather": ([_SP] + [_P] * 11 + [_P, _SZ, _P], ctypes.c_int),
+    "moe_mx_act_scale_bytes": ([_SP, ctypes.c_int32], _SZ),
+    "moe_mx_quantize_weights": ([ctypes.c_int32] * 3 + [_P] * 3 + [_P], ctypes.c_int),
+    "moe_dispatch_mxfp8": ([_SP] + [_P] * 7 + [_P], ctypes.c_int),
+    "moe_expert_ffn_mxfp8": ([_SP] + [_P] * 14 + [_P, _SZ, _P], ctypes.c_int),
+    "moe_combine_mxfp8": ([_SP] + [_P] * 5 + [_P], ctypes.c_int),
 }
 for _name, (_args, _res) in _SIG.items():
     _f = getattr(_lib, _name)
@@ -353,3 +361,99 @@ def layer_backward(fwd, bwd, dy, w_gate, w_up, w_down, stream=None, x=None, w_ro
         router_weight_backward(s, x, fwd.topk_idx, bwd.dlogit, bwd.dw_router,
                                bwd.dbias if with_bias else None, bwd.router_ws, stream)
     return bwd
+
+
+# ------------------------------------------------------------------- MXFP8 --
+# include/moe_mxfp8.h: E4M3 codes and E8M0 scale bytes are torch.uint8.
+
+_u8 = torch.uint8
+
+
+def mx_act_scale_bytes(shape, k):
+    """Bytes of the scale chunks of a capacity buffer with k columns (k = d or h)."""
+    return int(_lib.moe_mx_act_scale_bytes(ctypes.byref(shape), int(k)))
+
+
+def mx_quantize_weights(w, q, sf, stream=None):
+    """w [E, rows, k] bf16 -> q [E, rows, k] E4M3 codes and sf (E*rows*k/32 bytes of chunks)."""
+    E, rows, k = w.shape
+    _check(_lib.moe_mx_quantize_weights(E, rows, k, _ptr(w, _bf16, "w"), _ptr(q, _u8, "q"),
+                                        _ptr(sf, _u8, "sf"), _stream(stream)),
+           "moe_mx_quantize_weights")
+
+
+def dispatch_mxfp8(shape, x, route_row, topk_idx, expert_count, expert_offset, x_q, x_sf,
+                   stream=None):
+    _check(_lib.moe_dispatch_mxfp8(ctypes.byref(shape), _ptr(x, _bf16, "x"),
+                                   _ptr(route_row, _i32, "route_row"),
+                                   _ptr(topk_idx, _i32, "topk_idx"),
+                                   _ptr(expert_count, _i32, "expert_count"),
+                                   _ptr(expert_offset, _i32, "expert_offset"),
+                                   _ptr(x_q, _u8, "x_q"), _ptr(x_sf, _u8, "x_sf"),
+                                   _stream(stream)), "moe_dispatch_mxfp8")
+
+
+def expert_ffn_mxfp8(shape, x_q, x_sf, expert_count, expert_offset, w, h_q, h_sf, y_q, y_scale, ws,
+                     stream=None):
+    """w: an MxWeights.  Fills h_q/h_sf (SwiGLU output) and y_q/y_scale."""
+    _check(_lib.moe_expert_ffn_mxfp8(
+        ctypes.byref(shape), _ptr(x_q, _u8, "x_q"), _ptr(x_sf, _u8, "x_sf"),
+        _ptr(expert_count, _i32, "expert_count"), _ptr(expert_offset, _i32, "expert_offset"),
+        _ptr(w.gate_q, _u8, "w_gate_q"), _ptr(w.gate_sf, _u8, "w_gate_sf"),
+        _ptr(w.up_q, _u8, "w_up_q"), _ptr(w.up_sf, _u8, "w_up_sf"),
+        _ptr(w.down_q, _u8, "w_down_q"), _ptr(w.down_sf, _u8, "w_down_sf"),
+        _ptr(h_q, _u8, "h_q"), _ptr(h_sf, _u8, "h_sf"), _ptr(y_q, _u8, "y_q"),
+        _ptr(y_scale, _u8, "y_scale"), _ptr(ws, None, "ws"), ws.numel() * ws.element_size(),
+        _stream(stream)), "moe_expert_ffn_mxfp8")
+
+
+def combine_mxfp8(shape, y_q, y_scale, route_row, topk_gate, y, stream=None):
+    _check(_lib.moe_combine_mxfp8(ctypes.byref(shape), _ptr(y_q, _u8, "y_q"),
+                                  _ptr(y_scale, _u8, "y_scale"), _ptr(route_row, _i32, "route_row"),
+                                  _ptr(topk_gate, _f32, "topk_gate"), _ptr(y, _bf16, "y"),
+                                  _stream(stream)), "moe_combine_mxfp8")
+
+
+class MxWeights:
+    """Expert weights in MXFP8, quantized once from bf16 [N,h,d], [N,h,d],
+    [N,d,h] along each product's reduction dimension."""
+
+    def __init__(self, w_gate, w_up, w_down, stream=None):
+        def q(w):
+            E, rows, k = w.shape
+            codes = torch.empty((E, rows, k), dtype=_u8, device=w.device)
+            sf = torch.empty(E * rows * k // 32, dtype=_u8, device=w.device)
+            mx_quantize_weights(w, codes, sf, stream)
+            return codes, sf
+        self.gate_q, self.gate_sf = q(w_gate)
+        self.up_q, self.up_sf = q(w_up)
+        self.down_q, self.down_sf = q(w_down)
+
+
+class MxLayerBuffers(LayerBuffers):
+    """LayerBuffers plus the quantized payloads of the MXFP8 path."""
+
+    def __init__(self, shape, device="cuda"):
+        super().__init__(shape, device)
+        d, h, R = shape.d, shape.h, shape.R
+        e = dict(device=device, dtype=_u8)
+        self.x_q = torch.empty((R, d), **e)
+        self.x_sf = torch.zeros(max(mx_act_scale_bytes(shape, d), 16), **e)
+        self.h_q = torch.empty((R, h), **e)
+        self.h_sf = torch.zeros(max(mx_act_scale_bytes(shape, h), 16), **e)
+        self.y_q = torch.empty((R, d), **e)
+        self.y_scale = torch.empty((R, d // 32), **e)
+
+
+def layer_forward_mxfp8(buf, x, w_router, bias, w, stream=None):
+    """Route -> quantizing dispatch -> MXFP8 experts -> dequantizing combine
+    into buf.y (4 C-ABI calls); w is an MxWeights."""
+    s = buf.shape
+    route(s, x, w_router, bias, buf.topk_idx, buf.topk_gate, buf.route_row, buf.expert_count,
+          buf.expert_offset, buf.expert_demand, buf.route_ws, stream)
+    dispatch_mxfp8(s, x, buf.route_row, buf.topk_idx, buf.expert_count, buf.expert_offset,
+                   buf.x_q, buf.x_sf, stream)
+    expert_ffn_mxfp8(s, buf.x_q, buf.x_sf, buf.expert_count, buf.expert_offset, w, buf.h_q,
+                     buf.h_sf, buf.y_q, buf.y_scale, buf.ffn_ws, stream)
+    combine_mxfp8(s, buf.y_q, buf.y_scale, buf.route_row, buf.topk_gate, buf.y, stream)
+    return buf.y

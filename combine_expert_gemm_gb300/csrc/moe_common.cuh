@@ -5,6 +5,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -132,6 +133,64 @@ inline bool make_map_f32_3d(CUtensorMap *m, const void *base, uint64_t inner, ui
     const cuuint32_t estr[3] = {1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(base), dims, strides, box,
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ---- host: MXFP8 -----------------------------------------------------------
+//
+// Scale chunks.  Every MXFP8 operand of the tensor cores (dispatched rows,
+// SwiGLU outputs, weights) keeps its E8M0 scales in 512-byte chunks, one per
+// 128 rows x 128 columns (4 blocks of 32): the scale of row r (0-127 within
+// the 128-row block) and block b (0-3 within the 128 columns) sits at byte
+// (r % 32) * 16 + (r / 32) * 4 + b.  This is the order tcgen05.cp 32x128b.warpx4
+// copies into tensor memory and the block-scaled MMA reads there: row r's
+// scales at TMEM lane r, column r / 32, byte b.  Chunk (block128, kgroup) of an
+// operand with K columns starts at (block128 * K / 128 + kgroup) * 512.
+// Weights number their 128-row blocks e * rows / 128 + row / 128; packed
+// capacity-buffer rows number them per expert from that expert's first row:
+// block128 = pad_block[e] + (r - offset[e]) / 128, pad_block[e] = the sum of
+// ceil(count[e'] / 128) over e' < e (each expert starts a fresh block).
+constexpr int kMxBlock = 32;
+constexpr int kMxChunk = 512;
+
+__host__ __device__ inline int64_t mx_chunk_byte(int64_t block128, int kcols, int r_in, int kb) {
+    return (block128 * (kcols / 128) + kb / 4) * kMxChunk + (r_in % 32) * 16 + (r_in / 32) * 4 +
+           (kb % 4);
+}
+
+// Bytes of the scale-chunk array of a packed capacity buffer with k columns:
+// sum over experts of ceil(count / 128) <= R / 128 + N blocks.
+inline size_t mx_act_scale_bytes(int64_t R, int N, int k) {
+    return (size_t)((R + 127) / 128 + N) * (size_t)(k / 128) * kMxChunk;
+}
+
+// 2-D uint8 map over a row-major [rows, inner] fp8 matrix; box 128 x
+// box_rows, 128-byte swizzle (one 128-element row per 128-byte smem row).
+inline bool make_map_u8(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows,
+                        uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {inner, rows};
+    const cuuint64_t strides[1] = {inner};
+    const cuuint32_t box[2] = {128, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Map over a scale-chunk array viewed as [chunks, 128] uint32: one box is one
+// 512-byte chunk; chunks past the end read as zero.
+inline bool make_map_chunks(CUtensorMap *m, const void *base, uint64_t chunks) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {128, chunks};
+    const cuuint64_t strides[1] = {kMxChunk};
+    const cuuint32_t box[2] = {128, 1};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -467,6 +526,84 @@ __device__ __forceinline__ void tmem_ld_wait() {
 __device__ __forceinline__ void reg_fence(uint32_t (&r)[16]) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) asm volatile("" : "+r"(r[i]));
+}
+
+// ---- MXFP8 ----------------------------------------------------------------
+
+// Shared exponent of a block from its largest magnitude (finite, >= 0):
+// floor(log2 amax) - 8, clamped below at -127 (zero and fp32 subnormals land
+// there).  The E8M0 byte is the result + 127.
+__device__ __forceinline__ int mx_exponent(float amax) {
+    const int ef = (int)((__float_as_uint(amax) >> 23) & 0xFFu);
+    return ef - 135 < -127 ? -127 : ef - 135;
+}
+
+// 2^-E as an fp32 multiplier (E in [-127, 119], so the result is normal).
+__device__ __forceinline__ float mx_inv_scale(int E) {
+    return __uint_as_float((uint32_t)(127 - E) << 23);
+}
+
+// Four fp32 values -> four E4M3 codes (round to nearest even, saturating at
+// 448), a0 in the lowest byte.
+__device__ __forceinline__ uint32_t e4m3x4(float a0, float a1, float a2, float a3) {
+    uint16_t lo, hi;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(a1), "f"(a0));
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(a3), "f"(a2));
+    return (uint32_t)lo | ((uint32_t)hi << 16);
+}
+
+// Two E4M3 codes (c0 in the low byte) -> their exact fp32 values.
+__device__ __forceinline__ float2 e4m3x2_to_f32(uint16_t c) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c));
+    const __half2 hv = *reinterpret_cast<const __half2 *>(&h2);
+    return __half22float2(hv);
+}
+
+// 2^(s - 127) for an E8M0 byte s < 255 (s = 0 gives the subnormal 2^-127).
+__device__ __forceinline__ float e8m0_value(uint32_t s) {
+    return s == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(s << 23);
+}
+
+// Instruction descriptor for kind::mxf8f6f4 with E4M3 A and B, E8M0 scales
+// (bit 23), both operands K-major: B's scale byte (bits 4-5), N >> 3 (bits
+// 17-22), M >> 4 (bits 24-28), A's scale byte (bits 29-30).  The byte picks
+// which of the four blocks held in each 32-bit TMEM scale word this MMA uses.
+__host__ __device__ constexpr uint32_t idesc_mxf8(int M, int N, int sf_byte) {
+    return ((uint32_t)sf_byte << 4) | ((uint32_t)(N >> 3) << 17) | (1u << 23) |
+           ((uint32_t)(M >> 4) << 24) | ((uint32_t)sf_byte << 29);
+}
+
+// Block-scaled MMA over the CTA pair: as tc_mma_bf16_pair, with each CTA's
+// A scales at TMEM address sfa and the B scales of all N columns at sfb.
+__device__ __forceinline__ void tc_mma_mxf8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                 uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                                 uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+        " tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X"
+        " [%0], %1, %2, %3, [%4], [%5], p;\n}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+        : "memory");
+}
+
+// Shared-memory descriptor of one 512-byte scale chunk: 32 rows of 16 bytes,
+// no swizzle, 8-row groups 128 bytes apart.
+__device__ __forceinline__ uint64_t chunk_desc(uint32_t smem_addr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((smem_addr >> 4) & 0x3FFFu);
+    d |= (uint64_t)(128u >> 4) << 16;
+    d |= (uint64_t)(128u >> 4) << 32;
+    d |= (uint64_t)1u << 46;
+    return d;
+}
+
+// Issued by the pair's leader: each CTA's chunk at this shared-memory offset
+// goes to its own tensor memory, 32 lanes x 4 columns copied to all four lane
+// quadrants (ordered before later tcgen05.mma of the same thread).
+__device__ __forceinline__ void tc_cp_chunk_pair(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+                 : "memory");
 }
 
 }  // namespace moe

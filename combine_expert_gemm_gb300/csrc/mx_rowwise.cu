@@ -1,0 +1,270 @@
+// MXFP8 row kernels: weight quantization, the quantizing dispatch (step D)
+// and the dequantizing combine (step C).
+//
+// OLMo-core MoE report, "Section 05: Expert Parallelism": 5.4 (rows are
+// quantized as they are dispatched; the outputs come back quantized and the
+// local reduction dequantizes them), 5.7 (a quantized route's data row and
+// scale row follow the bf16 row's destination and validity), 5.8 (E4M3 data,
+// E8M0 scales), Table 8 ("Dispatch forward PUT", "Combine forward GET").
+// Format: OCP Microscaling (MX) v1.0 MXFP8, blocks of 32 along each row.
+//
+// All three are HBM-bound row movers, one warp per row (a token, or a weight
+// row) and persistent grids of a few CTAs per SM.  A lane holds 4 consecutive
+// elements of a 128-column group, so one block of 32 is 8 lanes: its maximum
+// comes from three xor-shuffles, and the group's four scale bytes, one per
+// block, meet in lane 0 and leave as one 32-bit store into the scale chunk.
+#include <algorithm>
+
+#include "../../include/moe_mxfp8.h"
+#include "moe_common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kMxThreads = 256;
+constexpr int kMxWarps = kMxThreads / 32;
+constexpr int kMxUnroll = 4;  // 128-column groups in flight per warp
+
+inline unsigned mx_grid(int64_t items) {
+    const int64_t per_cta = kMxWarps;
+    const int64_t want = (items + per_cta - 1) / per_cta;
+    return (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)num_sms() * 8));
+}
+
+// The quantization of one lane's 4 elements within its 8-lane block: codes
+// (a0 in the low byte) and, in every lane, the block's E8M0 byte.
+__device__ __forceinline__ uint32_t mx_quant_lane(float a0, float a1, float a2, float a3,
+                                                  uint32_t &scale_byte) {
+    float m = fmaxf(fmaxf(fabsf(a0), fabsf(a1)), fmaxf(fabsf(a2), fabsf(a3)));
+    m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+    m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+    m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
+    const int E = mx_exponent(m);
+    const float inv = mx_inv_scale(E);
+    scale_byte = (uint32_t)(E + 127);
+    return e4m3x4(a0 * inv, a1 * inv, a2 * inv, a3 * inv);
+}
+
+// The four blocks' scale bytes of a 128-column group, block 0 in the low byte
+// (valid in lane 0).
+__device__ __forceinline__ uint32_t mx_group_scales(uint32_t scale_byte) {
+    const uint32_t s1 = __shfl_sync(0xFFFFFFFFu, scale_byte, 8);
+    const uint32_t s2 = __shfl_sync(0xFFFFFFFFu, scale_byte, 16);
+    const uint32_t s3 = __shfl_sync(0xFFFFFFFFu, scale_byte, 24);
+    return scale_byte | (s1 << 8) | (s2 << 16) | (s3 << 24);
+}
+
+__device__ __forceinline__ void bf16x4(uint2 w, float &a0, float &a1, float &a2, float &a3) {
+    a0 = bf16_lo(w.x);
+    a1 = bf16_hi(w.x);
+    a2 = bf16_lo(w.y);
+    a3 = bf16_hi(w.y);
+}
+
+// Weights: item = (matrix row, 128-column group).
+__global__ void __launch_bounds__(kMxThreads)
+mx_quantize_weight_rows(int64_t rows, int k, const uint2 *__restrict__ w, uint32_t *__restrict__ q,
+                        uint8_t *__restrict__ sf) {
+    const int lane = threadIdx.x & 31;
+    const int groups = k / 128;
+    const int64_t items = rows * groups;
+    for (int64_t it = (int64_t)blockIdx.x * kMxWarps + (threadIdx.x >> 5); it < items;
+         it += (int64_t)gridDim.x * kMxWarps) {
+        const int64_t row = it / groups;
+        const int g = (int)(it % groups);
+        const int64_t e4 = (row * k + (int64_t)g * 128) / 4 + lane;  // in 4-element units
+        float a0, a1, a2, a3;
+        bf16x4(__ldcs(w + e4), a0, a1, a2, a3);
+        uint32_t sb;
+        q[e4] = mx_quant_lane(a0, a1, a2, a3, sb);
+        const uint32_t word = mx_group_scales(sb);
+        if (lane == 0)
+            *reinterpret_cast<uint32_t *>(sf + mx_chunk_byte(row / 128, k, (int)(row % 128), 4 * g)) =
+                word;
+    }
+}
+
+// pad_block[e] = sum over e' < e of ceil(count[e'] / 128), by warp 0.
+__device__ __forceinline__ void pad_block_prefix(int N, const int32_t *__restrict__ count,
+                                                 int32_t *pad_block, int lane) {
+    int carry = 0;
+    for (int base = 0; base < N; base += 32) {
+        const int e = base + lane;
+        const int v = e < N ? (count[e] + 127) / 128 : 0;
+        int incl = v;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int u = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+            if (lane >= off) incl += u;
+        }
+        if (e < N) pad_block[e] = carry + incl - v;
+        carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+    }
+}
+
+// Dispatch: one warp per token; each 128-column group is quantized once and
+// its codes and scale word go to every accepted route row.
+__global__ void __launch_bounds__(kMxThreads)
+dispatch_mx_rows(int T, int d, int K, int N, const uint2 *__restrict__ x,
+                 const int32_t *__restrict__ route_row, const int32_t *__restrict__ topk_idx,
+                 const int32_t *__restrict__ count, const int32_t *__restrict__ offset,
+                 uint32_t *__restrict__ xq, uint8_t *__restrict__ xsf) {
+    extern __shared__ int32_t pad_block[];
+    const int lane = threadIdx.x & 31;
+    if ((threadIdx.x >> 5) == 0) pad_block_prefix(N, count, pad_block, lane);
+    __syncthreads();
+    const int groups = d / 128;
+    const int64_t q4 = d / 4;  // 4-element units per row
+    for (int t = blockIdx.x * kMxWarps + (threadIdx.x >> 5); t < T; t += gridDim.x * kMxWarps) {
+        int32_t my_row = -1, my_blk = 0, my_rin = 0;
+        if (lane < K) {
+            my_row = route_row[(int64_t)t * K + lane];
+            if (my_row >= 0) {
+                const int e = topk_idx[(int64_t)t * K + lane];
+                const int slot = my_row - offset[e];
+                my_blk = pad_block[e] + slot / 128;
+                my_rin = slot % 128;
+            }
+        }
+        const uint2 *src = x + (int64_t)t * q4;
+        for (int g0 = 0; g0 < groups; g0 += kMxUnroll) {
+            uint2 v[kMxUnroll];
+#pragma unroll
+            for (int u = 0; u < kMxUnroll; ++u)
+                if (g0 + u < groups) v[u] = __ldcs(src + (int64_t)(g0 + u) * 32 + lane);
+#pragma unroll
+            for (int u = 0; u < kMxUnroll; ++u) {
+                if (g0 + u >= groups) break;  // warp-uniform
+                float a0, a1, a2, a3;
+                bf16x4(v[u], a0, a1, a2, a3);
+                uint32_t sb;
+                const uint32_t codes = mx_quant_lane(a0, a1, a2, a3, sb);
+                const uint32_t word = mx_group_scales(sb);
+                for (int k = 0; k < K; ++k) {
+                    const int32_t r = __shfl_sync(0xFFFFFFFFu, my_row, k);
+                    if (r < 0) continue;
+                    const int32_t blk = __shfl_sync(0xFFFFFFFFu, my_blk, k);
+                    const int32_t rin = __shfl_sync(0xFFFFFFFFu, my_rin, k);
+                    xq[(int64_t)r * q4 + (int64_t)(g0 + u) * 32 + lane] = codes;
+                    if (lane == 0)
+                        *reinterpret_cast<uint32_t *>(xsf + mx_chunk_byte(blk, d, rin, 4 * (g0 + u))) =
+                            word;
+                }
+            }
+        }
+    }
+}
+
+// Combine: one warp per token, a lane owns 8 consecutive columns of a
+// 256-column step; y[t] = bf16(sum_k gate_k * deq(row_k)) with an fp32 FMA
+// chain over k ascending.
+template <int MAXK>
+__global__ void __launch_bounds__(kMxThreads)
+combine_mx_rows(int T, int d, int K, const uint2 *__restrict__ yq, const uint8_t *__restrict__ ys,
+                const int32_t *__restrict__ route_row, const float *__restrict__ gate,
+                uint4 *__restrict__ y) {
+    const int lane = threadIdx.x & 31;
+    const int q8 = d / 8;
+    const int sc_row = d / 32;
+    for (int t = blockIdx.x * kMxWarps + (threadIdx.x >> 5); t < T; t += gridDim.x * kMxWarps) {
+        const int32_t my_row = lane < K ? route_row[(int64_t)t * K + lane] : -1;
+        const float my_g = lane < K ? gate[(int64_t)t * K + lane] : 0.0f;
+        int32_t rows[MAXK];
+        float gs[MAXK];
+#pragma unroll
+        for (int k = 0; k < MAXK; ++k) {
+            rows[k] = __shfl_sync(0xFFFFFFFFu, my_row, k);
+            gs[k] = __shfl_sync(0xFFFFFFFFu, my_g, k);
+        }
+        for (int c = lane; c < q8; c += 32) {
+            uint2 code[MAXK];
+            uint32_t sc[MAXK];
+#pragma unroll
+            for (int k = 0; k < MAXK; ++k) {
+                if (k < K && rows[k] >= 0) {
+                    code[k] = __ldcs(yq + (int64_t)rows[k] * q8 + c);
+                    sc[k] = ys[(int64_t)rows[k] * sc_row + c / 4];
+                }
+            }
+            float acc[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+#pragma unroll
+            for (int k = 0; k < MAXK; ++k) {
+                if (k < K && rows[k] >= 0) {
+                    const float s = e8m0_value(sc[k]);
+                    const float2 v0 = e4m3x2_to_f32((uint16_t)(code[k].x & 0xFFFFu));
+                    const float2 v1 = e4m3x2_to_f32((uint16_t)(code[k].x >> 16));
+                    const float2 v2 = e4m3x2_to_f32((uint16_t)(code[k].y & 0xFFFFu));
+                    const float2 v3 = e4m3x2_to_f32((uint16_t)(code[k].y >> 16));
+                    const float vals[8] = {v0.x, v0.y, v1.x, v1.y, v2.x, v2.y, v3.x, v3.y};
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) acc[i] = fmaf(gs[k], vals[i] * s, acc[i]);
+                }
+            }
+            y[(int64_t)t * q8 + c] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                                                pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+        }
+    }
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+MOE_API size_t moe_mx_act_scale_bytes(const moe_shape *s, int32_t k) {
+    if (check_shape(s) != MOE_OK || k <= 0 || k % 128 != 0) return 0;
+    return mx_act_scale_bytes(buffer_rows(s), s->N, k);
+}
+
+MOE_API moe_status moe_mx_quantize_weights(int32_t E, int32_t rows, int32_t k, const moe_bf16 *w,
+                                           uint8_t *q, uint8_t *sf, cudaStream_t stream) {
+    if (E < 0 || rows < 0 || k < 0) return MOE_ERR_INVALID_ARG;
+    if (rows % 128 != 0 || k % 128 != 0) return MOE_ERR_UNSUPPORTED;
+    const int64_t n = (int64_t)E * rows;
+    if (n == 0 || k == 0) return MOE_OK;
+    if (!w || !q || !sf) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(w) || !aligned16(q) || !aligned16(sf)) return MOE_ERR_ALIGNMENT;
+    mx_quantize_weight_rows<<<mx_grid(n * (k / 128)), kMxThreads, 0, stream>>>(
+        n, k, reinterpret_cast<const uint2 *>(w), reinterpret_cast<uint32_t *>(q), sf);
+    return launch_status();
+}
+
+MOE_API moe_status moe_dispatch_mxfp8(const moe_shape *s, const moe_bf16 *x,
+                                      const int32_t *route_row, const int32_t *topk_idx,
+                                      const int32_t *expert_count, const int32_t *expert_offset,
+                                      uint8_t *x_q, uint8_t *x_sf, cudaStream_t stream) {
+    moe_status r = check_shape(s);
+    if (r != MOE_OK) return r;
+    if (s->d % 128 != 0) return MOE_ERR_UNSUPPORTED;
+    if (s->T == 0 || s->cap == 0) return MOE_OK;
+    if (!x || !route_row || !topk_idx || !expert_count || !expert_offset || !x_q || !x_sf)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(route_row) || !aligned16(topk_idx) || !aligned16(x_q) ||
+        !aligned16(x_sf))
+        return MOE_ERR_ALIGNMENT;
+    dispatch_mx_rows<<<mx_grid(s->T), kMxThreads, sizeof(int32_t) * s->N, stream>>>(
+        s->T, s->d, s->K, s->N, reinterpret_cast<const uint2 *>(x), route_row, topk_idx,
+        expert_count, expert_offset, reinterpret_cast<uint32_t *>(x_q), x_sf);
+    return launch_status();
+}
+
+MOE_API moe_status moe_combine_mxfp8(const moe_shape *s, const uint8_t *y_q, const uint8_t *y_scale,
+                                     const int32_t *route_row, const float *topk_gate, moe_bf16 *y,
+                                     cudaStream_t stream) {
+    moe_status r = check_shape(s);
+    if (r != MOE_OK) return r;
+    if (s->d % 128 != 0) return MOE_ERR_UNSUPPORTED;
+    if (s->T == 0) return MOE_OK;
+    if (!route_row || !topk_gate || !y || (s->cap > 0 && (!y_q || !y_scale)))
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16(y_q) || !aligned16(y_scale) || !aligned16(route_row) || !aligned16(topk_gate) ||
+        !aligned16(y))
+        return MOE_ERR_ALIGNMENT;
+    auto *kern = s->K <= 8 ? combine_mx_rows<8> : combine_mx_rows<16>;
+    kern<<<mx_grid(s->T), kMxThreads, 0, stream>>>(s->T, s->d, s->K,
+                                                 reinterpret_cast<const uint2 *>(y_q), y_scale,
+                                                 route_row, topk_gate, reinterpret_cast<uint4 *>(y));
+    return launch_status();
+}
