@@ -176,8 +176,12 @@ def run_ours(args, cfg, rank, world):
     stream = torch.cuda.current_stream()
     phases = ["route", "dispatch", "ffn", "combine"] + (
         ["combine_bwd", "ffn_bwd", "dispatch_router_bwd", "router_dw"] if cfg.backward else [])
+    # our kernels per step: route 5 (logit blocks, top-K, block ranks, scan,
+    # slot assignment), dispatch 1, experts 2, combine 1; backward: combine 1,
+    # experts 4 (two data-gradient and two weight-gradient GEMMs), dispatch +
+    # router dx 1, router dW 1 or 2 (the chunk sums need a second kernel)
     router_dw_launches = 2 if (cfg.T + 127) // 128 > 1 else 1
-    launches_per_step = 8 + (6 + router_dw_launches if cfg.backward else 0)
+    launches_per_step = 9 + (6 + router_dw_launches if cfg.backward else 0)
     db = None if (bias is None or bwd is None) else bwd.dbias
 
     def step(ev=None):
@@ -304,6 +308,39 @@ def run_ours(args, cfg, rank, world):
         assert moe.read_device_error(buf.gather_ws) == 0
         fused_ms = float(np.median(f_ms[2:]))
 
+    # MXFP8 variant of the forward (moe_dispatch_mxfp8 -> moe_expert_ffn_mxfp8
+    # -> moe_combine_mxfp8) on the same inputs and routing, timed per phase
+    # outside the headline's timed region; weights are quantized once before.
+    mx = None
+    if not cfg.backward and cfg.d % 128 == 0 and cfg.h % 128 == 0:
+        mbuf = moe.MxLayerBuffers(shape, dev)
+        mw = moe.MxWeights(wg, wu, wd)
+
+        def mx_step(ev):
+            ev[0].record(stream)
+            moe.route(shape, x, wr, bias, mbuf.topk_idx, mbuf.topk_gate, mbuf.route_row,
+                      mbuf.expert_count, mbuf.expert_offset, mbuf.expert_demand, mbuf.route_ws)
+            ev[1].record(stream)
+            moe.dispatch_mxfp8(shape, x, mbuf.route_row, mbuf.topk_idx, mbuf.expert_count,
+                               mbuf.expert_offset, mbuf.x_q, mbuf.x_sf)
+            ev[2].record(stream)
+            moe.expert_ffn_mxfp8(shape, mbuf.x_q, mbuf.x_sf, mbuf.expert_count, mbuf.expert_offset,
+                                 mw, mbuf.h_q, mbuf.h_sf, mbuf.y_q, mbuf.y_scale, mbuf.ffn_ws)
+            ev[3].record(stream)
+            moe.combine_mxfp8(shape, mbuf.y_q, mbuf.y_scale, mbuf.route_row, mbuf.topk_gate, mbuf.y)
+            ev[4].record(stream)
+
+        n_mx = max(5, min(args.steps, 20))
+        mev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n_mx + 3)]
+        for i in range(n_mx + 3):
+            flush.zero_()
+            mx_step(mev[i])
+        torch.cuda.synchronize()
+        assert moe.read_device_error(mbuf.ffn_ws) == 0
+        mph = np.array([[mev[i][p].elapsed_time(mev[i][p + 1]) for p in range(4)]
+                        for i in range(3, n_mx + 3)])
+        mx = dict(ms=mph.mean(axis=0), steps=n_mx)
+
     if rank != 0:
         if dist:
             dist.destroy_process_group()
@@ -359,6 +396,26 @@ def run_ours(args, cfg, rank, world):
         line["fused_dispatch_ffn"] = {
             "ms": fused_ms, "two_step_ms": ph_ms["dispatch"] + ph_ms["ffn"],
             "note": "moe_expert_ffn_gather (x rows fetched by TMA gather4 in GEMM1) vs dispatch + expert_ffn"}
+    if mx is not None:
+        mms = mx["ms"]
+        T, d, K = cfg.T, cfg.d, cfg.K
+        mx_disp_bytes = 2.0 * T * d + A * d * (1 + 1 / 32) + 8.0 * T * K
+        mx_comb_bytes = A * d * (1 + 1 / 32) + 2.0 * T * d + 8.0 * T * K
+        fp8_peak = 2.0 * pk["bf16"]
+        mtf = alg["gemm_flop"] / (mms[2] / 1e3) / 1e12
+        line["mxfp8"] = {
+            "tokens_per_s": world * cfg.T / (float(mms.sum()) / 1e3),
+            "ms_per_step": float(mms.sum()), "steps": mx["steps"],
+            "phase_ms": {"route": float(mms[0]), "dispatch_mxfp8": float(mms[1]),
+                         "ffn_mxfp8": float(mms[2]), "combine_mxfp8": float(mms[3])},
+            "gemm": {"kernel": "grouped_gemm_mx_pair (F1 + SwiGLU + quantize, F2 + quantize)",
+                     "bound": "tensor", "achieved": mtf, "peak": fp8_peak, "unit": "TFLOP/s",
+                     "frac": mtf / fp8_peak,
+                     "peak_source": pk["source"] + " bf16 burst x 2 (nominal fp8 / bf16 ratio)"},
+            "dispatch_gbs": mx_disp_bytes / (mms[1] / 1e3) / 1e9,
+            "combine_gbs": mx_comb_bytes / (mms[3] / 1e3) / 1e9,
+            "gpu_launches_per_step": 9,
+            "note": "E4M3 data, E8M0 scales per 32; timed outside the headline region, L2 flushed"}
     if cfg.backward:
         bt = alg["gemm_bwd_flop"] / (ph_ms["ffn_bwd"] / 1e3) / 1e12
         line["backward"] = {

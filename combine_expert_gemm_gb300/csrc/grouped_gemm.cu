@@ -434,7 +434,7 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tm_a, const __grid_constan
                 epilogue_tile<EPI>(tbase, half, row_ok, row, t.n, Nout, out, g_save, u_save);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(cluster_map(smem_u32(&bars->tempty[acc]), 0));
+            if (lane == 0) mbar_arrive_cluster_relaxed(cluster_map(smem_u32(&bars->tempty[acc]), 0));
             if (++acc == 2) { acc = 0; acc_phase ^= 1; }
         }
         if (lane == 0) bulk_wait<0>();  // stores complete before the CTA ends

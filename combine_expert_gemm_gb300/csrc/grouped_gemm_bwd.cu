@@ -400,7 +400,7 @@ grouped_dgrad_pair(const __grid_constant__ CUtensorMap tm_a0, const __grid_const
                                      full_block, row_ok, lane);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(cluster_map(smem_u32(&bars->tempty[acc]), 0));
+            if (lane == 0) mbar_arrive_cluster_relaxed(cluster_map(smem_u32(&bars->tempty[acc]), 0));
             if (++acc == 2) { acc = 0; acc_phase ^= 1; }
         }
         if (lane == 0) bulk_wait<0>();  // stores complete before the CTA ends
@@ -732,7 +732,7 @@ grouped_wgrad_pair(const __grid_constant__ CUtensorMap tm_a0, const __grid_const
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(cluster_map(smem_u32(&bars->tempty[acc]), 0));
+            if (lane == 0) mbar_arrive_cluster_relaxed(cluster_map(smem_u32(&bars->tempty[acc]), 0));
             if (++acc == 2) { acc = 0; acc_phase ^= 1; }
         }
         if (lane == 0) bulk_wait<0>();  // stores complete before the CTA ends
@@ -828,8 +828,9 @@ MOE_API moe_status moe_expert_ffn_backward(
     const int wg_mt = 2 * ((s->h + 2 * BM - 1) / (2 * BM));
 
     if (R == 0) {
-        // no rows at all: every weight gradient is zero; run the wgrad launches
-        // anyway?  They need row buffers for their maps, so clear directly.
+        // no rows at all: every weight gradient is zero; the weight-gradient
+        // kernels need row buffers for their maps, so the outputs are cleared
+        // directly.
         const size_t hd = (size_t)s->N * s->h * s->d * sizeof(float);
         if (cudaMemsetAsync(dw_gate, 0, hd, stream) != cudaSuccess ||
             cudaMemsetAsync(dw_up, 0, hd, stream) != cudaSuccess ||

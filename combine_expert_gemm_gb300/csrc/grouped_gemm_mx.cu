@@ -19,8 +19,9 @@
 //     instructions (K = 32 each), the k-th reading byte k of each scale word;
 //   - the fp32 accumulator (256 columns) is single: the scale ring needs the
 //     rest of tensor memory.  The epilogue drains all its columns into
-//     registers first and frees the accumulator at once, so the next tile's
-//     MMAs overlap the SwiGLU, quantization and stores;
+//     registers first and frees the accumulator at once (a relaxed arrival,
+//     which does not wait for its earlier stores), so the next tile's MMAs
+//     overlap the SwiGLU, quantization and stores;
 //   - the epilogue quantizes along its rows in blocks of 32: F1 writes the
 //     SwiGLU output H as E4M3 codes plus scale chunks (F2's A operand), F2
 //     writes Y as codes plus row-major scale rows for the combine.
@@ -291,7 +292,10 @@ grouped_gemm_mx_pair(const __grid_constant__ CUtensorMap tm_a, const __grid_cons
             for (int j = 0; j < 8; ++j) reg_fence(v[j]);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(cluster_map(smem_u32(&bars->tempty), 0));
+            // relaxed: the loads above have completed (tcgen05.wait::ld), and
+            // the previous tile's stores need not be complete before the MMA
+            // of the next tile may overwrite the accumulator
+            if (lane == 0) mbar_arrive_cluster_relaxed(cluster_map(smem_u32(&bars->tempty), 0));
             acc_phase ^= 1;
             if (!row_ok) continue;
             if (EPI == XEPI_SWIGLU) {

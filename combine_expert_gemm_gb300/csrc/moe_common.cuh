@@ -444,6 +444,15 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
                  : "memory");
 }
 
+// The same arrival without release semantics, for signals that order no
+// memory operation (an epilogue freeing an accumulator whose tcgen05.ld have
+// completed): a release arrival would first wait for the thread's earlier
+// global stores to complete.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
+
 // TMA load into this CTA's shared memory whose completion is signalled on an
 // mbarrier of the pair's leader CTA (bar is a cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map,
