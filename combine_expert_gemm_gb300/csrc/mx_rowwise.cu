@@ -9,10 +9,12 @@
 // Format: OCP Microscaling (MX) v1.0 MXFP8, blocks of 32 along each row.
 //
 // All three are HBM-bound row movers, one warp per row (a token, or a weight
-// row) and persistent grids of a few CTAs per SM.  A lane holds 4 consecutive
-// elements of a 128-column group, so one block of 32 is 8 lanes: its maximum
-// comes from three xor-shuffles, and the group's four scale bytes, one per
-// block, meet in lane 0 and leave as one 32-bit store into the scale chunk.
+// row) and persistent grids of a few CTAs per SM.  In the weight quantizer a
+// lane holds 4 consecutive elements of a 128-column group (a block of 32 is 8
+// lanes); in the dispatch and the combine a lane holds 16 (a block is two
+// lanes, so its maximum is one xor-shuffle away, and every access is 16
+// bytes).  The four scale bytes of a 128-column group meet in the group's
+// first lane and leave as one 32-bit store into the scale chunk.
 #include <algorithm>
 
 #include "../../include/moe_mxfp8.h"
@@ -23,7 +25,6 @@ namespace {
 
 constexpr int kMxThreads = 256;
 constexpr int kMxWarps = kMxThreads / 32;
-constexpr int kMxUnroll = 4;  // 128-column groups in flight per warp
 
 inline unsigned mx_grid(int64_t items) {
     const int64_t per_cta = kMxWarps;
@@ -102,19 +103,45 @@ __device__ __forceinline__ void pad_block_prefix(int N, const int32_t *__restric
     }
 }
 
-// Dispatch: one warp per token; each 128-column group is quantized once and
-// its codes and scale word go to every accepted route row.
+// 16 fp32 values of one lane (half of a 32-block; the other half is in the
+// neighbouring lane, lane ^ 1) -> 16 E4M3 codes and the block's E8M0 byte.
+__device__ __forceinline__ uint4 mx_quant_lane16(const float (&a)[16], uint32_t &scale_byte) {
+    float m = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(a[i]));
+    m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+    const int E = mx_exponent(m);
+    const float inv = mx_inv_scale(E);
+    scale_byte = (uint32_t)(E + 127);
+    return make_uint4(e4m3x4(a[0] * inv, a[1] * inv, a[2] * inv, a[3] * inv),
+                      e4m3x4(a[4] * inv, a[5] * inv, a[6] * inv, a[7] * inv),
+                      e4m3x4(a[8] * inv, a[9] * inv, a[10] * inv, a[11] * inv),
+                      e4m3x4(a[12] * inv, a[13] * inv, a[14] * inv, a[15] * inv));
+}
+
+__device__ __forceinline__ void bf16x8(uint4 w, float *a) {
+    a[0] = bf16_lo(w.x); a[1] = bf16_hi(w.x); a[2] = bf16_lo(w.y); a[3] = bf16_hi(w.y);
+    a[4] = bf16_lo(w.z); a[5] = bf16_hi(w.z); a[6] = bf16_lo(w.w); a[7] = bf16_hi(w.w);
+}
+
+// Dispatch: one warp per token, a lane owns 16 consecutive columns of a
+// 512-column step (a block of 32 is two lanes, a 128-column group eight).
+// Each step is quantized once; its codes (16 bytes per lane) and the four
+// scale words (lanes 0, 8, 16, 24) go to every accepted route row.
+constexpr int kDispStep = 512;
+
 __global__ void __launch_bounds__(kMxThreads)
-dispatch_mx_rows(int T, int d, int K, int N, const uint2 *__restrict__ x,
+dispatch_mx_rows(int T, int d, int K, int N, const uint4 *__restrict__ x,
                  const int32_t *__restrict__ route_row, const int32_t *__restrict__ topk_idx,
                  const int32_t *__restrict__ count, const int32_t *__restrict__ offset,
-                 uint32_t *__restrict__ xq, uint8_t *__restrict__ xsf) {
+                 uint4 *__restrict__ xq, uint8_t *__restrict__ xsf) {
     extern __shared__ int32_t pad_block[];
     const int lane = threadIdx.x & 31;
     if ((threadIdx.x >> 5) == 0) pad_block_prefix(N, count, pad_block, lane);
     __syncthreads();
-    const int groups = d / 128;
-    const int64_t q4 = d / 4;  // 4-element units per row
+    const int steps = (d + kDispStep - 1) / kDispStep;
+    const int64_t x8 = d / 8;    // uint4 (8 bf16) per token row
+    const int64_t q16 = d / 16;  // uint4 (16 codes) per packed row
     for (int t = blockIdx.x * kMxWarps + (threadIdx.x >> 5); t < T; t += gridDim.x * kMxWarps) {
         int32_t my_row = -1, my_blk = 0, my_rin = 0;
         if (lane < K) {
@@ -126,45 +153,65 @@ dispatch_mx_rows(int T, int d, int K, int N, const uint2 *__restrict__ x,
                 my_rin = slot % 128;
             }
         }
-        const uint2 *src = x + (int64_t)t * q4;
-        for (int g0 = 0; g0 < groups; g0 += kMxUnroll) {
-            uint2 v[kMxUnroll];
+        const uint4 *src = x + (int64_t)t * x8;
+        for (int st0 = 0; st0 < steps; st0 += 2) {
+            uint4 v[2][2];
 #pragma unroll
-            for (int u = 0; u < kMxUnroll; ++u)
-                if (g0 + u < groups) v[u] = __ldcs(src + (int64_t)(g0 + u) * 32 + lane);
+            for (int u = 0; u < 2; ++u) {
+                const int col = (st0 + u) * kDispStep + lane * 16;
+                if (col < d) {
+                    v[u][0] = __ldcs(src + col / 8);
+                    v[u][1] = __ldcs(src + col / 8 + 1);
+                }
+            }
 #pragma unroll
-            for (int u = 0; u < kMxUnroll; ++u) {
-                if (g0 + u >= groups) break;  // warp-uniform
-                float a0, a1, a2, a3;
-                bf16x4(v[u], a0, a1, a2, a3);
+            for (int u = 0; u < 2; ++u) {
+                const int st = st0 + u;
+                if (st >= steps) break;  // warp-uniform
+                const int col = st * kDispStep + lane * 16;
+                const bool on = col < d;  // whole 8-lane groups (d is a multiple of 128)
+                float a[16];
+                if (on) {
+                    bf16x8(v[u][0], a);
+                    bf16x8(v[u][1], a + 8);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) a[i] = 0.0f;
+                }
                 uint32_t sb;
-                const uint32_t codes = mx_quant_lane(a0, a1, a2, a3, sb);
-                const uint32_t word = mx_group_scales(sb);
+                const uint4 codes = mx_quant_lane16(a, sb);
+                // the group's four block scales meet in the group's first lane
+                const uint32_t s1 = __shfl_down_sync(0xFFFFFFFFu, sb, 2);
+                const uint32_t s2 = __shfl_down_sync(0xFFFFFFFFu, sb, 4);
+                const uint32_t s3 = __shfl_down_sync(0xFFFFFFFFu, sb, 6);
+                const uint32_t word = sb | (s1 << 8) | (s2 << 16) | (s3 << 24);
+                const bool group_lead = on && (lane & 7) == 0;
+                const int kb = col / 32;  // first block of the lane's group when group_lead
                 for (int k = 0; k < K; ++k) {
                     const int32_t r = __shfl_sync(0xFFFFFFFFu, my_row, k);
                     if (r < 0) continue;
                     const int32_t blk = __shfl_sync(0xFFFFFFFFu, my_blk, k);
                     const int32_t rin = __shfl_sync(0xFFFFFFFFu, my_rin, k);
-                    xq[(int64_t)r * q4 + (int64_t)(g0 + u) * 32 + lane] = codes;
-                    if (lane == 0)
-                        *reinterpret_cast<uint32_t *>(xsf + mx_chunk_byte(blk, d, rin, 4 * (g0 + u))) =
-                            word;
+                    if (on) xq[(int64_t)r * q16 + col / 16] = codes;
+                    if (group_lead)
+                        *reinterpret_cast<uint32_t *>(xsf + mx_chunk_byte(blk, d, rin, kb)) = word;
                 }
             }
         }
     }
 }
 
-// Combine: one warp per token, a lane owns 8 consecutive columns of a
-// 256-column step; y[t] = bf16(sum_k gate_k * deq(row_k)) with an fp32 FMA
-// chain over k ascending.
+// Combine: one warp per token, a lane owns 16 consecutive columns of a
+// 512-column step; y[t] = bf16(sum_k gate_k * deq(row_k)) with an fp32 FMA
+// chain over k ascending (each dequantized value e4m3 * 2^(s - 127) is exact).
 template <int MAXK>
 __global__ void __launch_bounds__(kMxThreads)
-combine_mx_rows(int T, int d, int K, const uint2 *__restrict__ yq, const uint8_t *__restrict__ ys,
+combine_mx_rows(int T, int d, int K, const uint4 *__restrict__ yq, const uint8_t *__restrict__ ys,
                 const int32_t *__restrict__ route_row, const float *__restrict__ gate,
                 uint4 *__restrict__ y) {
     const int lane = threadIdx.x & 31;
-    const int q8 = d / 8;
+    const int64_t q16 = d / 16;
+    const int64_t y8 = d / 8;
     const int sc_row = d / 32;
     for (int t = blockIdx.x * kMxWarps + (threadIdx.x >> 5); t < T; t += gridDim.x * kMxWarps) {
         const int32_t my_row = lane < K ? route_row[(int64_t)t * K + lane] : -1;
@@ -176,34 +223,40 @@ combine_mx_rows(int T, int d, int K, const uint2 *__restrict__ yq, const uint8_t
             rows[k] = __shfl_sync(0xFFFFFFFFu, my_row, k);
             gs[k] = __shfl_sync(0xFFFFFFFFu, my_g, k);
         }
-        for (int c = lane; c < q8; c += 32) {
-            uint2 code[MAXK];
+        for (int col = lane * 16; col < d; col += kDispStep) {
+            uint4 code[MAXK];
             uint32_t sc[MAXK];
 #pragma unroll
             for (int k = 0; k < MAXK; ++k) {
                 if (k < K && rows[k] >= 0) {
-                    code[k] = __ldcs(yq + (int64_t)rows[k] * q8 + c);
-                    sc[k] = ys[(int64_t)rows[k] * sc_row + c / 4];
+                    code[k] = __ldcs(yq + (int64_t)rows[k] * q16 + col / 16);
+                    sc[k] = ys[(int64_t)rows[k] * sc_row + col / 32];
                 }
             }
-            float acc[8];
+            float acc[16];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+            for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
 #pragma unroll
             for (int k = 0; k < MAXK; ++k) {
                 if (k < K && rows[k] >= 0) {
                     const float s = e8m0_value(sc[k]);
-                    const float2 v0 = e4m3x2_to_f32((uint16_t)(code[k].x & 0xFFFFu));
-                    const float2 v1 = e4m3x2_to_f32((uint16_t)(code[k].x >> 16));
-                    const float2 v2 = e4m3x2_to_f32((uint16_t)(code[k].y & 0xFFFFu));
-                    const float2 v3 = e4m3x2_to_f32((uint16_t)(code[k].y >> 16));
-                    const float vals[8] = {v0.x, v0.y, v1.x, v1.y, v2.x, v2.y, v3.x, v3.y};
+                    const uint32_t w[4] = {code[k].x, code[k].y, code[k].z, code[k].w};
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) acc[i] = fmaf(gs[k], vals[i] * s, acc[i]);
+                    for (int j = 0; j < 4; ++j) {
+                        const float2 lo = e4m3x2_to_f32((uint16_t)(w[j] & 0xFFFFu));
+                        const float2 hi = e4m3x2_to_f32((uint16_t)(w[j] >> 16));
+                        acc[4 * j] = fmaf(gs[k], lo.x * s, acc[4 * j]);
+                        acc[4 * j + 1] = fmaf(gs[k], lo.y * s, acc[4 * j + 1]);
+                        acc[4 * j + 2] = fmaf(gs[k], hi.x * s, acc[4 * j + 2]);
+                        acc[4 * j + 3] = fmaf(gs[k], hi.y * s, acc[4 * j + 3]);
+                    }
                 }
             }
-            y[(int64_t)t * q8 + c] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                                                pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+            uint4 *dst = y + (int64_t)t * y8 + col / 8;
+            dst[0] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                                pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+            dst[1] = make_uint4(pack_bf16x2(acc[8], acc[9]), pack_bf16x2(acc[10], acc[11]),
+                                pack_bf16x2(acc[12], acc[13]), pack_bf16x2(acc[14], acc[15]));
         }
     }
 }
@@ -245,8 +298,8 @@ MOE_API moe_status moe_dispatch_mxfp8(const moe_shape *s, const moe_bf16 *x,
         !aligned16(x_sf))
         return MOE_ERR_ALIGNMENT;
     dispatch_mx_rows<<<mx_grid(s->T), kMxThreads, sizeof(int32_t) * s->N, stream>>>(
-        s->T, s->d, s->K, s->N, reinterpret_cast<const uint2 *>(x), route_row, topk_idx,
-        expert_count, expert_offset, reinterpret_cast<uint32_t *>(x_q), x_sf);
+        s->T, s->d, s->K, s->N, reinterpret_cast<const uint4 *>(x), route_row, topk_idx,
+        expert_count, expert_offset, reinterpret_cast<uint4 *>(x_q), x_sf);
     return launch_status();
 }
 
@@ -264,7 +317,7 @@ MOE_API moe_status moe_combine_mxfp8(const moe_shape *s, const uint8_t *y_q, con
         return MOE_ERR_ALIGNMENT;
     auto *kern = s->K <= 8 ? combine_mx_rows<8> : combine_mx_rows<16>;
     kern<<<mx_grid(s->T), kMxThreads, 0, stream>>>(s->T, s->d, s->K,
-                                                 reinterpret_cast<const uint2 *>(y_q), y_scale,
+                                                 reinterpret_cast<const uint4 *>(y_q), y_scale,
                                                  route_row, topk_gate, reinterpret_cast<uint4 *>(y));
     return launch_status();
 }
