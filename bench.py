@@ -75,17 +75,18 @@ def algorithmic(cfg, A):
     return out
 
 
-def gemm_traffic(workload):
-    """DRAM bytes per moe_expert_ffn call from the committed ncu summary, or
-    None if that summary is for another workload or the kernel source has
-    changed since the counters were taken."""
+def gemm_traffic(workload, kernel="grouped_gemm", sources=("grouped_gemm.cu", "moe_common.cuh")):
+    """DRAM bytes per call of a GEMM from its committed ncu summary
+    (profiles/<kernel>_<workload>_ncu.md), or None if there is none for this
+    workload or the kernel sources have changed since the counters were taken
+    (the summary names the sha256 of the sources it was captured with)."""
     import hashlib
     csrc = os.path.join(ROOT, "combine_expert_gemm_gb300", "csrc")
-    prof = os.path.join(ROOT, "profiles", f"grouped_gemm_{workload}_ncu.md")
+    prof = os.path.join(ROOT, "profiles", f"{kernel}_{workload}_ncu.md")
     if not os.path.exists(prof):
         return None
     h = hashlib.sha256()
-    for name in ("grouped_gemm.cu", "moe_common.cuh"):
+    for name in sources:
         h.update(open(os.path.join(csrc, name), "rb").read())
     sha = h.hexdigest()
     for line in open(prof):
@@ -411,7 +412,9 @@ def run_ours(args, cfg, rank, world):
             "gemm": {"kernel": "grouped_gemm_mx_pair (F1 + SwiGLU + quantize, F2 + quantize)",
                      "bound": "tensor", "achieved": mtf, "peak": fp8_peak, "unit": "TFLOP/s",
                      "frac": mtf / fp8_peak,
-                     "peak_source": pk["source"] + " bf16 burst x 2 (nominal fp8 / bf16 ratio)"},
+                     "peak_source": pk["source"] + " bf16 burst x 2 (nominal fp8 / bf16 ratio)",
+                     "traffic": gemm_traffic(cfg.name, "grouped_gemm_mx",
+                                             ("grouped_gemm_mx.cu", "moe_common.cuh"))},
             "dispatch_gbs": mx_disp_bytes / (mms[1] / 1e3) / 1e9,
             "combine_gbs": mx_comb_bytes / (mms[3] / 1e3) / 1e9,
             "gpu_launches_per_step": 9,
