@@ -183,3 +183,49 @@ def test_fused_entry_points_argument_errors(moe):
     assert lib.moe_router_weight_backward(ctypes.byref(s), *bad, A, ws_r, None) == 1
     bad = list(w5); bad[0] = mis                       # x misaligned
     assert lib.moe_router_weight_backward(ctypes.byref(s), *bad, A, ws_r, None) == 2
+
+
+def test_mxfp8_entry_points_argument_errors(moe):
+    """The MXFP8 calls (include/moe_mxfp8.h) refuse bad arguments before
+    enqueuing anything; the accepted empty cases return without a launch."""
+    s = _shape(moe)                                    # d = 128, h = 256, R = 128
+    lib = moe.lib()
+    A, mis = ctypes.c_void_p(4096), ctypes.c_void_p(4096 + 8)
+    # scale-chunk bytes: (ceil(R / 128) + N) * (k / 128) * 512
+    assert lib.moe_mx_act_scale_bytes(ctypes.byref(s), 128) == (1 + 8) * 1 * 512
+    assert lib.moe_mx_act_scale_bytes(ctypes.byref(s), 256) == (1 + 8) * 2 * 512
+    assert lib.moe_mx_act_scale_bytes(ctypes.byref(s), 100) == 0
+    assert lib.moe_mx_act_scale_bytes(ctypes.byref(_shape(moe, K=0)), 128) == 0
+
+    q = lib.moe_mx_quantize_weights
+    assert q(-1, 128, 128, A, A, A, None) == 1
+    assert q(1, 100, 128, A, A, A, None) == 5          # rows not a multiple of 128
+    assert q(1, 128, 96, A, A, A, None) == 5           # k not a multiple of 128
+    assert q(1, 128, 128, None, A, A, None) == 1
+    assert q(1, 128, 128, A, mis, A, None) == 2
+    assert q(0, 128, 128, None, None, None, None) == 0  # nothing to do, nothing enqueued
+
+    d7 = [A] * 7                                       # x .. x_sf
+    bad = list(d7); bad[1] = None                      # route_row
+    assert lib.moe_dispatch_mxfp8(ctypes.byref(s), *bad, None) == 1
+    bad = list(d7); bad[0] = mis                       # x misaligned
+    assert lib.moe_dispatch_mxfp8(ctypes.byref(s), *bad, None) == 2
+    assert lib.moe_dispatch_mxfp8(ctypes.byref(_shape(moe, d=136)), *d7, None) == 5
+    assert lib.moe_dispatch_mxfp8(ctypes.byref(_shape(moe, cap=0)), *([None] * 7), None) == 0
+
+    f14 = [A] * 14                                     # x_q .. y_scale
+    assert lib.moe_expert_ffn_mxfp8(ctypes.byref(s), *f14, None, 256, None) == 1
+    assert lib.moe_expert_ffn_mxfp8(ctypes.byref(s), *f14, A, 255, None) == 3
+    assert lib.moe_expert_ffn_mxfp8(ctypes.byref(s), *f14, mis, 256, None) == 3
+    bad = list(f14); bad[5] = None                     # w_gate_sf
+    assert lib.moe_expert_ffn_mxfp8(ctypes.byref(s), *bad, A, 256, None) == 1
+    bad = list(f14); bad[11] = mis                     # h_sf misaligned
+    assert lib.moe_expert_ffn_mxfp8(ctypes.byref(s), *bad, A, 256, None) == 2
+    assert lib.moe_expert_ffn_mxfp8(ctypes.byref(_shape(moe, h=200)), *f14, A, 256, None) == 5
+
+    c5 = [A] * 5                                       # y_q .. y
+    bad = list(c5); bad[4] = None                      # y
+    assert lib.moe_combine_mxfp8(ctypes.byref(s), *bad, None) == 1
+    bad = list(c5); bad[1] = mis                       # y_scale misaligned
+    assert lib.moe_combine_mxfp8(ctypes.byref(s), *bad, None) == 2
+    assert lib.moe_combine_mxfp8(ctypes.byref(_shape(moe, d=136)), *c5, None) == 5
