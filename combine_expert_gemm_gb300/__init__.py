@@ -23,7 +23,7 @@ __all__ = ["Shape", "MoEError", "lib", "route", "dispatch", "expert_ffn", "combi
            "layer_forward", "expert_ffn_backward", "expert_ffn_backward_workspace_bytes",
            "BackwardBuffers", "layer_backward", "MxWeights", "MxLayerBuffers", "mx_act_scale_bytes",
            "mx_quantize_weights", "dispatch_mxfp8", "expert_ffn_mxfp8", "combine_mxfp8",
-           "layer_forward_mxfp8"]
+           "layer_forward_mxfp8", "StreamedLayer"]
 
 if not os.path.exists(LIB):
     raise ImportError(f"{LIB} is missing: build it with `python combine_expert_gemm_gb300/build.py` "
@@ -457,3 +457,72 @@ def layer_forward_mxfp8(buf, x, w_router, bias, w, stream=None):
                      buf.h_sf, buf.y_q, buf.y_scale, buf.ffn_ws, stream)
     combine_mxfp8(s, buf.y_q, buf.y_scale, buf.route_row, buf.topk_gate, buf.y, stream)
     return buf.y
+
+
+class StreamedLayer:
+    """A stream of token batches through the layer, with the host copies of
+    one batch overlapping the device work of its neighbours.
+
+    Each submit(x_host, y_host[, dy_host, dx_host]) enqueues, for one batch:
+    the input copy from pinned host memory to the device (stream h2d), the
+    layer forward -- and the backward when dy_host is given -- (stream
+    compute), and the output copy back to pinned host memory (stream d2h).
+    Two sets of device buffers alternate, so batch i's copies run while
+    batch i - 1 or i + 1 computes; events order each set's reuse (an input
+    copy waits for the layer that last read that set's input, a layer waits
+    for the output copy that last read that set's outputs).  submit returns
+    at once; synchronize() waits for every submitted batch.  The host
+    buffers of a batch must stay untouched until then.
+    """
+
+    def __init__(self, shape, w_router, bias, w_gate, w_up, w_down, device="cuda",
+                 backward=False):
+        self.shape = shape
+        self.w = (w_router, bias, w_gate, w_up, w_down)
+        self.backward = backward
+        dev = torch.device(device)
+        T, d = shape.T, shape.d
+        self.fwd = [LayerBuffers(shape, dev, save_for_backward=backward) for _ in range(2)]
+        self.bwd = [BackwardBuffers(shape, dev) for _ in range(2)] if backward else None
+        self.x = [torch.empty((T, d), dtype=_bf16, device=dev) for _ in range(2)]
+        self.dy = [torch.empty((T, d), dtype=_bf16, device=dev) for _ in range(2)] if backward else None
+        self.h2d, self.compute, self.d2h = (torch.cuda.Stream(dev) for _ in range(3))
+        ev = lambda: [torch.cuda.Event() for _ in range(2)]
+        self.copied, self.layer_done, self.read_done = ev(), ev(), ev()
+        self.i = 0
+
+    def submit(self, x_host, y_host, dy_host=None, dx_host=None):
+        j = self.i % 2
+        wr, bias, wg, wu, wd = self.w
+        self.h2d.wait_event(self.layer_done[j])
+        with torch.cuda.stream(self.h2d):
+            self.x[j].copy_(x_host, non_blocking=True)
+            if self.backward:
+                self.dy[j].copy_(dy_host, non_blocking=True)
+            self.copied[j].record(self.h2d)
+        self.compute.wait_event(self.copied[j])
+        self.compute.wait_event(self.read_done[j])
+        fb = self.fwd[j]
+        layer_forward(fb, self.x[j], wr, bias, wg, wu, wd, stream=self.compute)
+        if self.backward:
+            layer_backward(fb, self.bwd[j], self.dy[j], wg, wu, wd, stream=self.compute,
+                           x=self.x[j], w_router=wr, with_bias=bias is not None)
+        self.layer_done[j].record(self.compute)
+        self.d2h.wait_event(self.layer_done[j])
+        with torch.cuda.stream(self.d2h):
+            y_host.copy_(fb.y, non_blocking=True)
+            if self.backward:
+                dx_host.copy_(self.bwd[j].dx, non_blocking=True)
+            self.read_done[j].record(self.d2h)
+        self.i += 1
+
+    def synchronize(self):
+        self.d2h.synchronize()
+
+    def status(self):
+        """Device status words of every workspace (0 = no device error)."""
+        codes = [read_device_error(b.route_ws) for b in self.fwd]
+        codes += [read_device_error(b.ffn_ws) for b in self.fwd]
+        if self.backward:
+            codes += [read_device_error(b.ws) for b in self.bwd]
+        return max(codes)
