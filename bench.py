@@ -97,6 +97,23 @@ def gemm_traffic(workload, kernel="grouped_gemm", sources=("grouped_gemm.cu", "m
     return None
 
 
+def replica_config(cfg, rank):
+    """The workload of one replica: rank r routes its own tokens (seed offset
+    by 1000 r); rank 0 runs the named workload itself."""
+    return cfg.with_(seed=cfg.seed + 1000 * rank) if rank else cfg
+
+
+def max_over_ranks(x, dist=None, device="cpu"):
+    """The largest of every rank's x (the job's time is its slowest rank's);
+    x itself when there is one rank."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle-reason samples while the timed region runs."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -161,8 +178,7 @@ def run_ours(args, cfg, rank, world):
     def bf(a):
         return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
 
-    # each replica routes its own tokens (seed offset by rank)
-    rcfg = cfg.with_(seed=cfg.seed + 1000 * rank) if rank else cfg
+    rcfg = replica_config(cfg, rank)
     x_np = synth.gen_x(rcfg)
     wg, wu, wd = (bf(a) for a in synth.gen_expert_weights(cfg))
     wr = torch.from_numpy(synth.gen_router(cfg)).to(dev)
@@ -243,11 +259,7 @@ def run_ours(args, cfg, rank, world):
     per_phase = np.array([[evs[i][p].elapsed_time(evs[i][p + 1]) for p in range(len(phases))]
                           for i in range(args.steps)])  # ms
     step_ms = per_phase.sum(axis=1)
-    ms = float(step_ms.mean())
-    if dist:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(float(step_ms.mean()), dist, dev)
     A = int(buf.expert_offset[-1].item())
     alg = algorithmic(cfg, A)
     pk = peaks()
