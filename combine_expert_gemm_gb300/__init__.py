@@ -375,7 +375,8 @@ def mx_act_scale_bytes(shape, k):
 
 
 def mx_quantize_weights(w, q, sf, stream=None):
-    """w [E, rows, k] bf16 -> q [E, rows, k] E4M3 codes and sf (E*rows*k/32 bytes of chunks)."""
+    """w [E, rows, k] bf16 -> q [E, rows, k] E4M3 codes and sf (E*rows*k/8 bytes: the
+    scale chunks, each stored four times; see include/moe_mxfp8.h)."""
     E, rows, k = w.shape
     _check(_lib.moe_mx_quantize_weights(E, rows, k, _ptr(w, _bf16, "w"), _ptr(q, _u8, "q"),
                                         _ptr(sf, _u8, "sf"), _stream(stream)),
@@ -422,7 +423,7 @@ class MxWeights:
         def q(w):
             E, rows, k = w.shape
             codes = torch.empty((E, rows, k), dtype=_u8, device=w.device)
-            sf = torch.empty(E * rows * k // 32, dtype=_u8, device=w.device)
+            sf = torch.empty(E * rows * k // 8, dtype=_u8, device=w.device)
             mx_quantize_weights(w, codes, sf, stream)
             return codes, sf
         self.gate_q, self.gate_sf = q(w_gate)

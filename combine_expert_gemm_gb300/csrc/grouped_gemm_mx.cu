@@ -12,11 +12,14 @@
 // work list derived on the device from expert_count.  What changes:
 //   - operands are E4M3 codes: a k-block is 128 elements = one 128-byte
 //     swizzled row, so each 32 KB stage covers twice the K of a bf16 stage;
-//   - each stage also carries three 512-byte scale chunks (this CTA's A rows,
-//     and the B scales of all 256 columns, which every CTA's tensor memory
-//     needs); the issuer copies them into tensor memory with tcgen05.cp
-//     (32x128b.warpx4) and runs four tcgen05.mma kind::mxf8f6f4 block_scale
-//     instructions (K = 32 each), the k-th reading byte k of each scale word;
+//   - each stage also carries this CTA's 512-byte A-scale chunk and the B
+//     scales of all 256 columns, which every CTA's tensor memory needs, as
+//     the weights store them: each B chunk four times over (4 KB).  The
+//     issuer copies the A chunk with tcgen05.cp 32x128b.warpx4 and the B
+//     scales with one 128x256b copy (lane L gets 16 bytes of each chunk's
+//     copy L / 32, so all four lane quadrants hold them), then runs four
+//     tcgen05.mma kind::mxf8f6f4 block_scale instructions (K = 32 each), the
+//     k-th reading byte k of each scale word;
 //   - the fp32 accumulator (256 columns) is single: the scale ring needs the
 //     rest of tensor memory.  The epilogue drains all its columns into
 //     registers first and frees the accumulator at once (a relaxed arrival,
@@ -40,8 +43,10 @@ constexpr int XPM = 2 * XM;                  // rows per pair tile
 constexpr int X_A_BYTES = XM * XK;           // 16 KB
 constexpr int X_B_BYTES = (XN / 2) * XK;     // this CTA's half of B, 16 KB
 constexpr int X_AB_BYTES = X_A_BYTES + X_B_BYTES;
-constexpr int X_SF_BYTES = 3 * kMxChunk;     // A chunk, B chunks of columns 0-127 and 128-255
-constexpr int X_STAGES = 6;
+// A chunk, then the four copies of the B chunk of columns 0-127 and the four
+// of columns 128-255 (as the weights store them)
+constexpr int X_SF_BYTES = (1 + 2 * kMxWeightCopies) * kMxChunk;
+constexpr int X_STAGES = 5;
 constexpr int X_EPI_WARPS = 8;
 constexpr int X_THREADS = 64 + 32 * X_EPI_WARPS;
 constexpr int X_TMEM_COLS = 512;
@@ -206,8 +211,10 @@ grouped_gemm_mx_pair(const __grid_constant__ CUtensorMap tm_a, const __grid_cons
                     tma_load_2d_pair(sa, &tm_a, full, kb * XK, a_row);
                     tma_load_2d_pair(sb, mb, full, kb * XK, b_row);
                     tma_load_2d_pair(ss, &tm_sfa, full, 0, sfa_chunk + kb);
-                    tma_load_2d_pair(ss + kMxChunk, &tm_sfb0, full, 0, sfb0_chunk + kb);
-                    tma_load_2d_pair(ss + 2 * kMxChunk, &tm_sfb1, full, 0, sfb1_chunk + kb);
+                    tma_load_2d_pair(ss + kMxChunk, &tm_sfb0, full, 0,
+                                     (sfb0_chunk + kb) * kMxWeightCopies);
+                    tma_load_2d_pair(ss + (1 + kMxWeightCopies) * kMxChunk, &tm_sfb1, full, 0,
+                                     (sfb1_chunk + kb) * kMxWeightCopies);
                     ++issued;
                     if (++stage == X_STAGES) { stage = 0; phase ^= 1; }
                 }
@@ -246,8 +253,7 @@ grouped_gemm_mx_pair(const __grid_constant__ CUtensorMap tm_a, const __grid_cons
                     const uint32_t ss = smem_u32(sf_ring + (size_t)stage * X_SF_BYTES);
                     const uint32_t sf_t = tmem_base + (uint32_t)(X_SF_COL0 + 16 * stage);
                     tc_cp_chunk_pair(sf_t, chunk_desc(ss));
-                    tc_cp_chunk_pair(sf_t + 4, chunk_desc(ss + kMxChunk));
-                    tc_cp_chunk_pair(sf_t + 8, chunk_desc(ss + 2 * kMxChunk));
+                    tc_cp_sfb_pair(sf_t + 4, sfb_desc(ss + kMxChunk));
 #pragma unroll
                     for (int kk = 0; kk < XK / 32; ++kk)
                         tc_mma_mxf8_pair(tmem_base, sw128_kmajor_desc(sa + kk * 32),
@@ -416,10 +422,13 @@ MOE_API moe_status moe_expert_ffn_mxfp8(const moe_shape *s, const uint8_t *x_q, 
         !make_map_u8(&mu, w_up_q, d, (uint64_t)N * h, 128) || !make_map_u8(&mh, h_q, h, R, XM) ||
         !make_map_u8(&md, w_down_q, h, (uint64_t)N * d, XN / 2) ||
         !make_map_chunks(&sx, x_sf, act_blocks * (d / 128)) ||
-        !make_map_chunks(&sg, w_gate_sf, (uint64_t)N * (h / 128) * (d / 128)) ||
-        !make_map_chunks(&su, w_up_sf, (uint64_t)N * (h / 128) * (d / 128)) ||
+        !make_map_chunks(&sg, w_gate_sf, (uint64_t)N * (h / 128) * (d / 128) * kMxWeightCopies,
+                         kMxWeightCopies) ||
+        !make_map_chunks(&su, w_up_sf, (uint64_t)N * (h / 128) * (d / 128) * kMxWeightCopies,
+                         kMxWeightCopies) ||
         !make_map_chunks(&sh, h_sf, act_blocks * (h / 128)) ||
-        !make_map_chunks(&sd, w_down_sf, (uint64_t)N * (d / 128) * (h / 128)))
+        !make_map_chunks(&sd, w_down_sf, (uint64_t)N * (d / 128) * (h / 128) * kMxWeightCopies,
+                         kMxWeightCopies))
         return MOE_ERR_CUDA;
     int *status = static_cast<int *>(ws);
     const int64_t rows = std::min<int64_t>(R, (int64_t)s->T * s->K);

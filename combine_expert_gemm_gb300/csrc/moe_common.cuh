@@ -158,6 +158,18 @@ __host__ __device__ inline int64_t mx_chunk_byte(int64_t block128, int kcols, in
            (kb % 4);
 }
 
+// Weight scales are stored with every chunk written four times in a row
+// (2 KB per 128-row block and 128-column group): the GEMM stages the four
+// copies of two chunks with two TMA boxes and moves them into tensor memory,
+// already replicated for the four lane quadrants, with one 128x256b copy.
+constexpr int kMxWeightCopies = 4;
+
+__host__ __device__ inline int64_t mx_wchunk_byte(int64_t block128, int kcols, int r_in, int kb,
+                                                  int copy) {
+    return ((block128 * (kcols / 128) + kb / 4) * kMxWeightCopies + copy) * kMxChunk +
+           (r_in % 32) * 16 + (r_in / 32) * 4 + (kb % 4);
+}
+
 // Bytes of the scale-chunk array of a packed capacity buffer with k columns:
 // sum over experts of ceil(count / 128) <= R / 128 + N blocks.
 inline size_t mx_act_scale_bytes(int64_t R, int N, int k) {
@@ -180,14 +192,15 @@ inline bool make_map_u8(CUtensorMap *m, const void *base, uint64_t inner, uint64
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Map over a scale-chunk array viewed as [chunks, 128] uint32: one box is one
-// 512-byte chunk; chunks past the end read as zero.
-inline bool make_map_chunks(CUtensorMap *m, const void *base, uint64_t chunks) {
+// Map over a scale-chunk array viewed as [chunks, 128] uint32: one box is
+// box_chunks consecutive 512-byte chunks; chunks past the end read as zero.
+inline bool make_map_chunks(CUtensorMap *m, const void *base, uint64_t chunks,
+                            uint32_t box_chunks = 1) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {128, chunks};
     const cuuint64_t strides[1] = {kMxChunk};
-    const cuuint32_t box[2] = {128, 1};
+    const cuuint32_t box[2] = {128, box_chunks};
     const cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(base), dims, strides, box,
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -605,6 +618,25 @@ __device__ __forceinline__ uint64_t chunk_desc(uint32_t smem_addr) {
     d |= (uint64_t)(128u >> 4) << 32;
     d |= (uint64_t)1u << 46;
     return d;
+}
+
+// Shared-memory descriptor of the eight B-scale chunks of a stage: the low
+// 256 columns' chunk four times (2 KB), then the high columns' chunk four
+// times; row L of a 128x256b copy reads 16 bytes at 16 L of each half.
+__device__ __forceinline__ uint64_t sfb_desc(uint32_t smem_addr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((smem_addr >> 4) & 0x3FFFu);
+    d |= (uint64_t)(2048u >> 4) << 16;
+    d |= (uint64_t)(128u >> 4) << 32;
+    d |= (uint64_t)1u << 46;
+    return d;
+}
+
+// Issued by the pair's leader: 128 lanes x 32 bytes from each CTA's shared
+// memory at this offset into its own tensor memory (eight columns).
+__device__ __forceinline__ void tc_cp_sfb_pair(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::2.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc)
+                 : "memory");
 }
 
 // Issued by the pair's leader: each CTA's chunk at this shared-memory offset

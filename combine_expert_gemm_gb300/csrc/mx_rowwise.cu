@@ -62,7 +62,8 @@ __device__ __forceinline__ void bf16x4(uint2 w, float &a0, float &a1, float &a2,
     a3 = bf16_hi(w.y);
 }
 
-// Weights: item = (matrix row, 128-column group).
+// Weights: item = (matrix row, 128-column group); the group's scale word goes
+// into each of the four copies of its chunk.
 __global__ void __launch_bounds__(kMxThreads)
 mx_quantize_weight_rows(int64_t rows, int k, const uint2 *__restrict__ w, uint32_t *__restrict__ q,
                         uint8_t *__restrict__ sf) {
@@ -78,10 +79,10 @@ mx_quantize_weight_rows(int64_t rows, int k, const uint2 *__restrict__ w, uint32
         bf16x4(__ldcs(w + e4), a0, a1, a2, a3);
         uint32_t sb;
         q[e4] = mx_quant_lane(a0, a1, a2, a3, sb);
-        const uint32_t word = mx_group_scales(sb);
-        if (lane == 0)
-            *reinterpret_cast<uint32_t *>(sf + mx_chunk_byte(row / 128, k, (int)(row % 128), 4 * g)) =
-                word;
+        const uint32_t word = __shfl_sync(0xFFFFFFFFu, mx_group_scales(sb), 0);
+        if (lane < kMxWeightCopies)  // the same word into each of the chunk's copies
+            *reinterpret_cast<uint32_t *>(
+                sf + mx_wchunk_byte(row / 128, k, (int)(row % 128), 4 * g, lane)) = word;
     }
 }
 

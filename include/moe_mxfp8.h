@@ -27,7 +27,11 @@
  * chunk per 128 rows x 128 columns, the scale of row r (0-127) and block b
  * (0-3) at byte (r % 32) * 16 + (r / 32) * 4 + b, chunk (block128, g) at byte
  * (block128 * k / 128 + g) * 512.  Weights number their row blocks
- * e * rows / 128 + row / 128.  Packed capacity-buffer rows number them per
+ * e * rows / 128 + row / 128 and store every chunk four times in a row:
+ * copy c (0-3) of chunk (block128, g) at byte
+ * ((block128 * k / 128 + g) * 4 + c) * 512 -- the GEMM moves the copies into
+ * tensor memory, one per lane quadrant, with a single copy instruction.
+ * Packed capacity-buffer rows number them per
  * expert: block128 = pad_block[e] + (row - expert_offset[e]) / 128 with
  * pad_block[e] = sum over e' < e of ceil(expert_count[e'] / 128), so every
  * expert starts a fresh chunk and a GEMM tile never straddles two experts'
@@ -58,9 +62,9 @@ size_t moe_mx_act_scale_bytes(const moe_shape *s, int32_t k);
  * moe_mx_quantize_weights -- quantizes E stacked [rows, k] bf16 matrices
  * along k (the reduction dimension of the product that reads them):
  *   w [E, rows, k] bf16 -> q [E, rows, k] E4M3 codes and
- *   sf: E * rows * k / 32 bytes of scale chunks (block128 = e * rows / 128 +
- *   row / 128).  For the experts: w_gate, w_up [N, h, d] (rows = h, k = d)
- *   and w_down [N, d, h] (rows = d, k = h).
+ *   sf: E * rows * k / 8 bytes of scale chunks, each chunk four times over
+ *   (block128 = e * rows / 128 + row / 128).  For the experts: w_gate, w_up
+ *   [N, h, d] (rows = h, k = d) and w_down [N, d, h] (rows = d, k = h).
  * rows and k must be multiples of 128 (MOE_ERR_UNSUPPORTED otherwise).
  */
 moe_status moe_mx_quantize_weights(int32_t E, int32_t rows, int32_t k, const moe_bf16 *w,

@@ -100,11 +100,13 @@ def _to_chunks(scale_rows, blk, rin, k, nbytes):
 
 
 def _weight_chunks(scales):
-    """Row-major weight scales [E, rows, k/32] -> chunk bytes."""
+    """Row-major weight scales [E, rows, k/32] -> chunk bytes, every 512-byte
+    chunk stored four times in a row (the weights' layout)."""
     E, rows, nb = scales.shape
     flat = scales.reshape(E * rows, nb)
     r = np.arange(E * rows)
-    return _to_chunks(flat, r // 128, r % 128, nb * 32, E * rows * nb)
+    once = _to_chunks(flat, r // 128, r % 128, nb * 32, E * rows * nb).reshape(-1, 512)
+    return np.repeat(once[:, None, :], 4, axis=1).reshape(-1)
 
 
 # ---------------------------------------------------------------- bounds --
@@ -168,7 +170,7 @@ def test_quantize_weights_bit_exact(moe):
     w = oracle.bf16_from_f64(v)
     oq, os_ = oracle.mx_quantize(w)
     q = torch.full((E, rows, k), FILL, dtype=U8, device=DEV)
-    sf = torch.full((E * rows * k // 32,), FILL, dtype=U8, device=DEV)
+    sf = torch.full((E * rows * k // 8,), FILL, dtype=U8, device=DEV)
     moe.mx_quantize_weights(bf(w), q, sf)
     torch.cuda.synchronize()
     assert np.array_equal(_np(q), oq)
