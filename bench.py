@@ -292,7 +292,7 @@ def run_ours(args, cfg, rank, world):
         sl.submit(x_host, y_host[i % 2], dy_host, dx_host[i % 2])
     e1.record(sl.d2h)
     e1.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dist, dev)
     y_e2e = y_host[(e2e_steps - 1) % 2]
     assert torch.equal(y_e2e.to(dev).view(torch.int16), buf.y.view(torch.int16)), \
         "streamed layer output differs from the timed step's"
