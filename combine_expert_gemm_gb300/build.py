@@ -27,7 +27,7 @@ def _sources():
 
 def _deps():
     return (_sources() + glob.glob(os.path.join(CSRC, "*.cuh")) +
-            [os.path.join(ROOT, "include", "moe.h"), __file__])
+            glob.glob(os.path.join(ROOT, "include", "*.h")) + [__file__])
 
 
 def up_to_date() -> bool:
