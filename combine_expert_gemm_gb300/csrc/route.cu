@@ -44,53 +44,54 @@ __device__ __forceinline__ bool beats(float a, int ia, float b, int ib) {
 // route_logit_blocks: the dot product over j is cut into 512-wide blocks (one
 // fp32 chain per block; the block sums are added in block order, the order
 // the logits are defined by).  CTA (token tile, block b) computes the block
-// sums of 64 tokens x all experts (passes of 64 experts; 128 tokens x 32
-// experts when N <= 32) and writes them to part[b][t][e].  4 warps, each 32
-// tokens x 32 experts; lane = tx +
-// 8 ty (tx in 0..7, ty in 0..3) owns tokens ty + 4i (i = 0..7) and experts
-// tx + 8b (b = 0..3): 32 chains, advanced two tokens at a time by the packed
-// fp32x2 fma.  x (bf16) and W_r (fp32) stream through a 4-stage cp.async ring
-// of 32-wide j-chunks in their natural layouts (rows padded so that a warp
-// load's distinct rows hit distinct banks).  Per 4 j a lane loads 8 x 8 bytes
-// of x and 4 x 16 bytes of W_r for 128 fmas: one byte of shared memory per
-// fma, which the shared-memory port sustains at the fma rate.  Splitting j
-// into blocks gives 4 times the warps of a single chain per logit.
+// sums of 128 tokens x all experts (passes of EC experts) and writes them to
+// part[b][t][e].  4 warps, each 32 tokens x EC experts; lane = tx + 8 ty (tx in
+// 0..7, ty in 0..3) owns tokens ty + 4i (i = 0..7) and experts tx + 8b (b <
+// EPL): 8 EPL chains, advanced two tokens at a time by the packed fp32x2 fma.
+// EPL = 8 (64 experts per pass) when N > 32, else 4: each widened pair of x
+// values then feeds 8 paired fmas instead of 4, which halves the conversion
+// and register-move instructions per fma (they, not memory, bound the loop).
+// x (bf16) and W_r (fp32) stream through a 3-stage cp.async ring of 32-wide
+// j-chunks in their natural layouts (rows padded so that a warp load's
+// distinct rows hit distinct banks).  Splitting j into blocks gives 4 times
+// the warps of a single chain per logit.
 //
 // route_topk: one CTA per 32 tokens adds the block sums in order (+ bias)
 // into shared memory, then one thread per token selects the top K and
 // computes the gates.
 constexpr int kLogitJC = 32;
 constexpr int kLogitBlock = 512;  // j per block sum (a multiple of kLogitJC)
-constexpr int kLogitStages = 4;
+constexpr int kLogitStages = 3;
 constexpr int kLogitThreads = 128;
 constexpr int kLogitXR = kLogitJC + 8;  // bf16 per padded x row
 constexpr int kLogitWR = kLogitJC + 4;  // fp32 per padded W row
 
-// WE warps along the experts, 4 / WE along the tokens: 64 tokens x 64
-// experts per pass (WE = 2), or 128 x 32 for N <= 32 (WE = 1)
-template <int WE>
+// WE warps along the experts, 4 / WE along the tokens; EPL experts per lane:
+// 128 tokens x 64 experts per pass (EPL = 8), or 128 x 32 (EPL = 4) for
+// N <= 32
+template <int WE, int EPL = 4>
 struct LogitTile {
     static constexpr int WT = 4 / WE;
     static constexpr int TB = 32 * WT;
-    static constexpr int EC = 32 * WE;
+    static constexpr int EC = 8 * EPL * WE;
     static constexpr int STAGE = TB * kLogitXR * 2 + EC * kLogitWR * 4;
     static constexpr size_t SMEM = (size_t)kLogitStages * STAGE;
 };
 
 inline int logit_blocks(int d) { return (d + kLogitBlock - 1) / kLogitBlock; }
 
-template <int WE>
+template <int WE, int EPL>
 __global__ void __launch_bounds__(kLogitThreads)
 route_logit_blocks(int T, int d, int N, const uint16_t *__restrict__ x,
                    const float *__restrict__ w_r, float *__restrict__ part) {
-    using L = LogitTile<WE>;
+    using L = LogitTile<WE, EPL>;
     constexpr int JC = kLogitJC, XR = kLogitXR, WR = kLogitWR, TB = L::TB, EC = L::EC;
     constexpr int kLogitStage = L::STAGE;
     extern __shared__ __align__(16) uint8_t smem_l[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int tx = lane & 7, ty = lane >> 3;
     const int tok0 = (warp % L::WT) * 32 + ty;   // + 4i
-    const int exp0 = (warp / L::WT) * 32 + tx;   // + 8b
+    const int exp0 = (warp / L::WT) * (8 * EPL) + tx;   // + 8b
     const int t0 = blockIdx.x * TB;
     const int b = blockIdx.y;
     const int jb0 = b * kLogitBlock, jlen = min(kLogitBlock, d - jb0);  // a multiple of 8
@@ -120,11 +121,11 @@ route_logit_blocks(int T, int d, int N, const uint16_t *__restrict__ x,
 
         // acc[p][e]: chains (token tok0 + 8p, expert e) and (token tok0 + 8p + 4,
         // expert e) of this lane, e = exp0 + 8 * (0..3)
-        float2 acc[4][4];
+        float2 acc[4][EPL];
 #pragma unroll
         for (int p = 0; p < 4; ++p)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) acc[p][e] = make_float2(0.0f, 0.0f);
+            for (int e = 0; e < EPL; ++e) acc[p][e] = make_float2(0.0f, 0.0f);
 
         __syncthreads();  // the previous pass is done with every stage
 #pragma unroll
@@ -142,9 +143,9 @@ route_logit_blocks(int T, int d, int N, const uint16_t *__restrict__ x,
                 uint2 xv[8];  // tokens tok0 + 4i, 4 bf16 at j .. j + 3
 #pragma unroll
                 for (int i = 0; i < 8; ++i) xv[i] = *reinterpret_cast<const uint2 *>(xs + 4 * i * XR + j);
-                float4 wv[4];
+                float4 wv[EPL];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) wv[e] = *reinterpret_cast<const float4 *>(ws + 8 * e * WR + j);
+                for (int e = 0; e < EPL; ++e) wv[e] = *reinterpret_cast<const float4 *>(ws + 8 * e * WR + j);
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
 #pragma unroll
@@ -154,7 +155,7 @@ route_logit_blocks(int T, int d, int N, const uint16_t *__restrict__ x,
                         const float2 xp = (q & 1) ? make_float2(bf16_hi(a), bf16_hi(bb))
                                                   : make_float2(bf16_lo(a), bf16_lo(bb));
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
+                        for (int e = 0; e < EPL; ++e) {
                             const float w = q == 0 ? wv[e].x : q == 1 ? wv[e].y : q == 2 ? wv[e].z : wv[e].w;
                             acc[p][e] = __ffma2_rn(xp, make_float2(w, w), acc[p][e]);
                         }
@@ -167,7 +168,7 @@ route_logit_blocks(int T, int d, int N, const uint16_t *__restrict__ x,
         for (int p = 0; p < 4; ++p) {
             const int ta = t0 + tok0 + 8 * p, tb = ta + 4;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
+            for (int e = 0; e < EPL; ++e) {
                 const int ex = ec0 + exp0 + 8 * e;
                 if (ex >= N) continue;
                 if (ta < T) pb[(int64_t)ta * N + ex] = acc[p][e].x;
@@ -412,10 +413,10 @@ moe_status launch_logits(const moe_shape *s, const uint16_t *x, const float *w, 
                          int32_t *idx, float *gate, float *part, cudaStream_t st) {
     static bool configured = false;
     if (!configured) {
-        if (cudaFuncSetAttribute(route_logit_blocks<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)LogitTile<1>::SMEM) != cudaSuccess ||
-            cudaFuncSetAttribute(route_logit_blocks<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)LogitTile<2>::SMEM) != cudaSuccess ||
+        if (cudaFuncSetAttribute(route_logit_blocks<1, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)LogitTile<1, 4>::SMEM) != cudaSuccess ||
+            cudaFuncSetAttribute(route_logit_blocks<1, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)LogitTile<1, 8>::SMEM) != cudaSuccess ||
             cudaFuncSetAttribute(route_topk<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)(sizeof(float) * kTopkTB * (kMaxN + 1))) != cudaSuccess ||
             cudaFuncSetAttribute(route_topk<kMaxK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -425,12 +426,12 @@ moe_status launch_logits(const moe_shape *s, const uint16_t *x, const float *w, 
     }
     const int nb = logit_blocks(s->d);
     if (s->N <= 32) {
-        const dim3 grid((s->T + LogitTile<1>::TB - 1) / LogitTile<1>::TB, nb);
-        route_logit_blocks<1><<<grid, kLogitThreads, LogitTile<1>::SMEM, st>>>(s->T, s->d, s->N, x,
+        const dim3 grid((s->T + LogitTile<1, 4>::TB - 1) / LogitTile<1, 4>::TB, nb);
+        route_logit_blocks<1, 4><<<grid, kLogitThreads, LogitTile<1, 4>::SMEM, st>>>(s->T, s->d, s->N, x,
                                                                              w, part);
     } else {
-        const dim3 grid((s->T + LogitTile<2>::TB - 1) / LogitTile<2>::TB, nb);
-        route_logit_blocks<2><<<grid, kLogitThreads, LogitTile<2>::SMEM, st>>>(s->T, s->d, s->N, x,
+        const dim3 grid((s->T + LogitTile<1, 8>::TB - 1) / LogitTile<1, 8>::TB, nb);
+        route_logit_blocks<1, 8><<<grid, kLogitThreads, LogitTile<1, 8>::SMEM, st>>>(s->T, s->d, s->N, x,
                                                                              w, part);
     }
     moe_status r = launch_status();
