@@ -13,8 +13,8 @@
 //      of j one fused multiply-add chain over j ascending), one CTA per
 //      (token tile, block);
 //   1b. route_topk: the block sums added in block order (+ bias), so the
-//      logits are reproducible bit for bit; then one thread per token selects
-//      the top K and computes the gates.
+//      logits are reproducible bit for bit; then four lanes per token select
+//      the top K and compute the gates.
 //   2. route_block_rank: per block of 256 tokens, a per-warp bitmask of the
 //      tokens choosing each expert gives every route its rank among earlier
 //      routes to the same expert inside the block, and the block's count per
@@ -56,9 +56,6 @@ __device__ __forceinline__ bool beats(float a, int ia, float b, int ib) {
 // distinct rows hit distinct banks).  Splitting j into blocks gives 4 times
 // the warps of a single chain per logit.
 //
-// route_topk: one CTA per 32 tokens adds the block sums in order (+ bias)
-// into shared memory, then one thread per token selects the top K and
-// computes the gates.
 constexpr int kLogitJC = 32;
 constexpr int kLogitBlock = 512;  // j per block sum (a multiple of kLogitJC)
 constexpr int kLogitStages = 3;
@@ -178,57 +175,115 @@ route_logit_blocks(int T, int d, int N, const uint16_t *__restrict__ x,
     }
 }
 
-constexpr int kTopkTB = 32;
+constexpr int kTopkTB = 32;     // tokens per CTA
+constexpr int kTopkPlanes = 4;  // block-sum planes loaded before any is added
 
+// Shared-memory row stride of the logits: at least N + 1 and 4 mod 32, so the
+// 32 lanes of a selecting warp (8 tokens x 4 lanes, lane s reading expert
+// s + 4i) fall on 32 distinct banks.
+__host__ __device__ constexpr int topk_row_stride(int N) {
+    return N + 1 + (4 - (N + 1) % 32 + 32) % 32;
+}
+
+// Inserts (v, ie) into a list sorted best first; an entry that does not beat
+// the last one leaves the list unchanged.  Every index is a constant.
+template <int MAXK>
+__device__ __forceinline__ void topk_insert(float (&tv)[MAXK], int (&ti)[MAXK], float v, int ie) {
+    if (!beats(v, ie, tv[MAXK - 1], ti[MAXK - 1])) return;
+#pragma unroll
+    for (int q = 0; q < MAXK; ++q) {
+        const bool sw = beats(v, ie, tv[q], ti[q]);
+        const float sv = tv[q];
+        const int si = ti[q];
+        tv[q] = sw ? v : sv;
+        ti[q] = sw ? ie : si;
+        v = sw ? sv : v;
+        ie = sw ? si : ie;
+    }
+}
+
+// Replaces this lane's sorted list by the best MAXK of its union with the
+// list of lane ^ mask (both lanes end with the same list).  The better of
+// entry q and the partner's entry MAXK - 1 - q holds the best MAXK of the
+// union as a bitonic sequence; the bitonic merge network then sorts it.
+template <int MAXK>
+__device__ __forceinline__ void topk_merge(float (&tv)[MAXK], int (&ti)[MAXK], int mask) {
+    float pv[MAXK];
+    int pi[MAXK];
+#pragma unroll
+    for (int q = 0; q < MAXK; ++q) {
+        pv[q] = __shfl_xor_sync(0xFFFFFFFFu, tv[q], mask);
+        pi[q] = __shfl_xor_sync(0xFFFFFFFFu, ti[q], mask);
+    }
+#pragma unroll
+    for (int q = 0; q < MAXK; ++q) {
+        const bool take = beats(pv[MAXK - 1 - q], pi[MAXK - 1 - q], tv[q], ti[q]);
+        tv[q] = take ? pv[MAXK - 1 - q] : tv[q];
+        ti[q] = take ? pi[MAXK - 1 - q] : ti[q];
+    }
+#pragma unroll
+    for (int s = MAXK / 2; s > 0; s >>= 1) {
+#pragma unroll
+        for (int q = 0; q < MAXK; ++q) {
+            if (q & s) continue;
+            const bool sw = beats(tv[q + s], ti[q + s], tv[q], ti[q]);
+            const float a = tv[q], b = tv[q + s];
+            const int ia = ti[q], ib = ti[q + s];
+            tv[q] = sw ? b : a;
+            ti[q] = sw ? ib : ia;
+            tv[q + s] = sw ? a : b;
+            ti[q + s] = sw ? ia : ib;
+        }
+    }
+}
+// route_topk: one CTA (4 warps) per 32 tokens.  The block sums of the tile
+// are contiguous in each block's [T][N] plane; every thread loads its float4
+// groups from kTopkPlanes planes before adding any of them, then adds them in
+// block order (+ bias) into shared memory.  Selection: 4 lanes per token, lane
+// s keeping the best MAXK of experts s, s + 4, s + 8, ... (logit descending,
+// lower expert first on ties, NaN as -inf; unfilled entries are -inf with an
+// index past every expert, so any expert beats them); two merges over lane
+// shuffles give all four lanes the best MAXK of the token, whose first K are
+// the top K.  The order is strict and total, so the result does not depend on
+// how the experts were split.  Gates: softmax over the K, shifted by the
+// largest, summed over k ascending.
 template <int MAXK>
 __global__ void __launch_bounds__(128)
 route_topk(int T, int N, int K, int nb, const float *__restrict__ part,
            const float *__restrict__ bias, int32_t *__restrict__ topk_idx,
            float *__restrict__ topk_gate) {
     extern __shared__ __align__(16) uint8_t smem_t[];
-    const int LDS = N + 1;  // padded logit row: one thread per token reads its row
+    const int LDS = topk_row_stride(N);
     float *lg = reinterpret_cast<float *>(smem_t);  // [kTopkTB][LDS]
     const int tid = threadIdx.x;
     const int t0 = blockIdx.x * kTopkTB;
     const int tn = min(kTopkTB, T - t0);
-    // the tile's block sums are contiguous in each block's [T][N] array: read
-    // them as float4 (when N allows) with four groups in flight per thread
     const int64_t tile = (int64_t)t0 * N, n = (int64_t)tn * N;
     const int64_t plane = (int64_t)T * N;
     if ((N & 3) == 0) {
-        for (int64_t g0 = tid; g0 < n / 4; g0 += 4 * blockDim.x) {
-            float4 v[4];
+        const float4 *p0 = reinterpret_cast<const float4 *>(part + tile);
+        for (int64_t g = tid; g < n / 4; g += blockDim.x) {
+            float4 v = __ldcs(p0 + g);
+            for (int b = 1; b < nb; b += kTopkPlanes) {
+                float4 w[kTopkPlanes];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int64_t g = g0 + u * blockDim.x;
-                if (g < n / 4) v[u] = __ldcs(reinterpret_cast<const float4 *>(part + tile) + g);
-            }
-            for (int b = 1; b < nb; ++b) {
-                float4 w[4];
+                for (int c = 0; c < kTopkPlanes; ++c)
+                    if (b + c < nb)
+                        w[c] = __ldcs(reinterpret_cast<const float4 *>(part + (b + c) * plane + tile) + g);
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int64_t g = g0 + u * blockDim.x;
-                    if (g < n / 4)
-                        w[u] = __ldcs(reinterpret_cast<const float4 *>(part + b * plane + tile) + g);
-                }
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    v[u].x = __fadd_rn(v[u].x, w[u].x);
-                    v[u].y = __fadd_rn(v[u].y, w[u].y);
-                    v[u].z = __fadd_rn(v[u].z, w[u].z);
-                    v[u].w = __fadd_rn(v[u].w, w[u].w);
+                for (int c = 0; c < kTopkPlanes; ++c) {
+                    if (b + c >= nb) break;
+                    v.x = __fadd_rn(v.x, w[c].x);
+                    v.y = __fadd_rn(v.y, w[c].y);
+                    v.z = __fadd_rn(v.z, w[c].z);
+                    v.w = __fadd_rn(v.w, w[c].w);
                 }
             }
+            const float vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int64_t g = g0 + u * blockDim.x;
-                if (g >= n / 4) continue;
-                const float vv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    const int i = (int)(4 * g + h), tt = i / N, e = i - tt * N;
-                    lg[tt * LDS + e] = bias ? __fadd_rn(vv[h], bias[e]) : vv[h];
-                }
+            for (int h = 0; h < 4; ++h) {
+                const int i = (int)(4 * g + h), tt = i / N, e = i - tt * N;
+                lg[tt * LDS + e] = bias ? __fadd_rn(vv[h], bias[e]) : vv[h];
             }
         }
     } else {
@@ -242,62 +297,41 @@ route_topk(int T, int N, int K, int nb, const float *__restrict__ part,
     }
     __syncthreads();
 
-    // top-K and gates, one thread per token: the logits stream past a
-    // sorted list of the best K so far (logit descending, lower expert first
-    // on ties, NaN as -inf); a logit that beats the K-th is swapped down into
-    // place.  The list sits at the end of a MAXK-entry register array whose
-    // first MAXK - K entries hold sentinels that nothing beats, so the K-th
-    // is always the last entry and every index is a constant.
-    for (int tt = tid; tt < tn; tt += blockDim.x) {
-        const int t = t0 + tt;
-        if (t >= T) break;
-        const float *l = lg + tt * LDS;
-        const int first = MAXK - K;
-        float tv[MAXK];
-        int ti[MAXK];
+    const int lane = tid & 31, sub = lane & 3;
+    const int tt = (tid >> 5) * 8 + (lane >> 2);
+    const int nloc = tt < tn ? N : 0;  // lanes past the tile only join the shuffles
+    const float *l = lg + tt * LDS;
+    float tv[MAXK];
+    int ti[MAXK];
 #pragma unroll
-        for (int q = 0; q < MAXK; ++q) {
-            const bool real = q >= first;
-            tv[q] = real ? -INFINITY : INFINITY;
-            ti[q] = real ? 0x7FFFFFFF : -1;
-        }
-        auto insert = [&](float v, int ie) {
-            if (!beats(v, ie, tv[MAXK - 1], ti[MAXK - 1])) return;
+    for (int q = 0; q < MAXK; ++q) {
+        tv[q] = -INFINITY;
+        ti[q] = 0x7FFFFFFF;
+    }
+    int e = sub;
+    for (; e + 12 < nloc; e += 16) {
+        float v[4];
 #pragma unroll
-            for (int q = 0; q < MAXK; ++q) {
-                const bool sw = beats(v, ie, tv[q], ti[q]);
-                const float sv = tv[q];
-                const int si = ti[q];
-                tv[q] = sw ? v : sv;
-                ti[q] = sw ? ie : si;
-                v = sw ? sv : v;
-                ie = sw ? si : ie;
-            }
-        };
-        int e = 0;
-        for (; e + 8 <= N; e += 8) {
-            float v[8];
+        for (int u = 0; u < 4; ++u) v[u] = canon(l[e + 4 * u]);
 #pragma unroll
-            for (int u = 0; u < 8; ++u) v[u] = canon(l[e + u]);
+        for (int u = 0; u < 4; ++u) topk_insert(tv, ti, v[u], e + 4 * u);
+    }
+    for (; e < nloc; e += 4) topk_insert(tv, ti, canon(l[e]), e);
+    topk_merge(tv, ti, 1);
+    topk_merge(tv, ti, 2);
+    if (nloc == 0) return;
+    const int t = t0 + tt;
+    const float top = tv[0];
+    float sum = 0.0f;
 #pragma unroll
-            for (int u = 0; u < 8; ++u) insert(v[u], e + u);
-        }
-        for (; e < N; ++e) insert(canon(l[e]), e);
-        float top = 0.0f;
+    for (int q = 0; q < MAXK; ++q)
+        if (q < K) sum += (tv[q] == top) ? 1.0f : expf(tv[q] - top);
 #pragma unroll
-        for (int q = 0; q < MAXK; ++q)
-            if (q == first) top = tv[q];
-        float sum = 0.0f;
-#pragma unroll
-        for (int q = 0; q < MAXK; ++q)
-            if (q >= first) sum += (tv[q] == top) ? 1.0f : expf(tv[q] - top);
-#pragma unroll
-        for (int q = 0; q < MAXK; ++q) {
-            if (q >= first) {
-                const float ex = (tv[q] == top) ? 1.0f : expf(tv[q] - top);
-                topk_idx[(int64_t)t * K + (q - first)] = ti[q];
-                topk_gate[(int64_t)t * K + (q - first)] = ex / sum;
-            }
+    for (int q = 0; q < MAXK; ++q) {
+        if (q < K && (q & 3) == sub) {
+            const float ex = (tv[q] == top) ? 1.0f : expf(tv[q] - top);
+            topk_idx[(int64_t)t * K + q] = ti[q];
+            topk_gate[(int64_t)t * K + q] = ex / sum;
         }
     }
 }
@@ -418,9 +452,9 @@ moe_status launch_logits(const moe_shape *s, const uint16_t *x, const float *w, 
             cudaFuncSetAttribute(route_logit_blocks<1, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)LogitTile<1, 8>::SMEM) != cudaSuccess ||
             cudaFuncSetAttribute(route_topk<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)(sizeof(float) * kTopkTB * (kMaxN + 1))) != cudaSuccess ||
+                                 (int)(sizeof(float) * kTopkTB * topk_row_stride(kMaxN))) != cudaSuccess ||
             cudaFuncSetAttribute(route_topk<kMaxK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)(sizeof(float) * kTopkTB * (kMaxN + 1))) != cudaSuccess)
+                                 (int)(sizeof(float) * kTopkTB * topk_row_stride(kMaxN))) != cudaSuccess)
             return MOE_ERR_CUDA;
         configured = true;
     }
@@ -436,7 +470,7 @@ moe_status launch_logits(const moe_shape *s, const uint16_t *x, const float *w, 
     }
     moe_status r = launch_status();
     if (r != MOE_OK) return r;
-    const size_t tsmem = sizeof(float) * kTopkTB * (s->N + 1);
+    const size_t tsmem = sizeof(float) * kTopkTB * topk_row_stride(s->N);
     auto *topk = s->K <= 8 ? route_topk<8> : route_topk<kMaxK>;
     topk<<<(s->T + kTopkTB - 1) / kTopkTB, 128, tsmem, st>>>(s->T, s->N, s->K, nb, part, b, idx,
                                                            gate);
