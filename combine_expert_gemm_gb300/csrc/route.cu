@@ -43,9 +43,11 @@ __device__ __forceinline__ bool beats(float a, int ia, float b, int ib) {
 //
 // route_logit_blocks: the dot product over j is cut into 512-wide blocks (one
 // fp32 chain per block; the block sums are added in block order, the order
-// the logits are defined by).  CTA (token tile, block b) computes the block
-// sums of 128 tokens x all experts (passes of EC experts) and writes them to
-// part[b][t][e].  4 warps, each 32 tokens x EC experts; lane = tx + 8 ty (tx in
+// the logits are defined by).  CTA (token tile, block b, pass z) computes
+// the block sums of 128 tokens x the z-th group of EC experts and writes them
+// to part[b][t][e]; the passes sit in the grid rather than in a loop, so that
+// a layer with many experts gets many short CTAs instead of a second, nearly
+// empty wave of long ones.  4 warps, each 32 tokens x EC experts; lane = tx + 8 ty (tx in
 // 0..7, ty in 0..3) owns tokens ty + 4i (i = 0..7) and experts tx + 8b (b <
 // EPL): 8 EPL chains, advanced two tokens at a time by the packed fp32x2 fma.
 // EPL = 8 (64 experts per pass) when N > 32, else 4: each widened pair of x
@@ -95,7 +97,7 @@ route_logit_blocks(int T, int d, int N, const uint16_t *__restrict__ x,
     const int nchunks = (jlen + JC - 1) / JC;
     float *pb = part + (size_t)b * T * N;
 
-    for (int ec0 = 0; ec0 < N; ec0 += EC) {
+    for (int ec0 = blockIdx.z * EC; ec0 < N; ec0 += EC * (int)gridDim.z) {
         auto issue = [&](int c) {
             if (c < nchunks) {
                 uint8_t *st = smem_l + (size_t)(c % kLogitStages) * kLogitStage;
@@ -460,11 +462,13 @@ moe_status launch_logits(const moe_shape *s, const uint16_t *x, const float *w, 
     }
     const int nb = logit_blocks(s->d);
     if (s->N <= 32) {
-        const dim3 grid((s->T + LogitTile<1, 4>::TB - 1) / LogitTile<1, 4>::TB, nb);
+        const dim3 grid((s->T + LogitTile<1, 4>::TB - 1) / LogitTile<1, 4>::TB, nb,
+                        (s->N + LogitTile<1, 4>::EC - 1) / LogitTile<1, 4>::EC);
         route_logit_blocks<1, 4><<<grid, kLogitThreads, LogitTile<1, 4>::SMEM, st>>>(s->T, s->d, s->N, x,
                                                                              w, part);
     } else {
-        const dim3 grid((s->T + LogitTile<1, 8>::TB - 1) / LogitTile<1, 8>::TB, nb);
+        const dim3 grid((s->T + LogitTile<1, 8>::TB - 1) / LogitTile<1, 8>::TB, nb,
+                        (s->N + LogitTile<1, 8>::EC - 1) / LogitTile<1, 8>::EC);
         route_logit_blocks<1, 8><<<grid, kLogitThreads, LogitTile<1, 8>::SMEM, st>>>(s->T, s->d, s->N, x,
                                                                              w, part);
     }
