@@ -458,14 +458,11 @@ moe_status launch_gemm_pair(const CUtensorMap &a, const CUtensorMap &b0, const C
                             const int32_t *offset, const int32_t *row_token, uint16_t *out,
                             uint16_t *gs, uint16_t *us, int *status, cudaStream_t st) {
     const size_t smem = smem_bytes_pair(N);
-    static size_t configured = 0;
-    if (smem > configured) {
-        if (cudaFuncSetAttribute(grouped_gemm_pair<EPI, GATHER>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem_bytes_pair(kMaxN)) != cudaSuccess)
-            return MOE_ERR_CUDA;
-        configured = smem_bytes_pair(kMaxN);
-    }
+    static PerDeviceOnce smem_attr;
+    if (!device_once(smem_attr, [] {
+            return set_smem_limit(grouped_gemm_pair<EPI, GATHER>, smem_bytes_pair(kMaxN));
+        }))
+        return MOE_ERR_CUDA;
     constexpr int BN_OUT = EPI == EPI_SWIGLU ? MMA_N / 2 : MMA_N;
     const int64_t max_units = (int64_t)((max_row_tiles + 1) / 2 + N) * ((Nout + BN_OUT - 1) / BN_OUT);
     const int64_t pairs = std::min<int64_t>(num_sms() / 2, std::max<int64_t>(max_units, 1));

@@ -419,15 +419,12 @@ template <int MODE>
 moe_status launch_dgrad_pair(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap &b0,
                              const CUtensorMap &b1, const CUtensorMap &o0, const CUtensorMap &o1,
                              const Params &p, int max_units, cudaStream_t st) {
-    static size_t configured = 0;
     const size_t smem = smem_bytes_pair(p.N);
-    if (smem > configured) {
-        if (cudaFuncSetAttribute(grouped_dgrad_pair<MODE>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem_bytes_pair(kMaxN)) != cudaSuccess)
-            return MOE_ERR_CUDA;
-        configured = smem_bytes_pair(kMaxN);
-    }
+    static PerDeviceOnce smem_attr;
+    if (!device_once(smem_attr, [] {
+            return set_smem_limit(grouped_dgrad_pair<MODE>, smem_bytes_pair(kMaxN));
+        }))
+        return MOE_ERR_CUDA;
     const int pairs = std::min(num_sms() / 2, std::max(max_units, 1));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(2 * pairs));
@@ -751,14 +748,10 @@ template <int MODE>
 moe_status launch_wgrad_pair(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap &b0,
                              const CUtensorMap &o0, const CUtensorMap &o1, const Params &p,
                              int max_units, cudaStream_t st) {
-    static bool configured = false;
     const size_t smem = smem_bytes_wgrad_pair();
-    if (!configured) {
-        if (cudaFuncSetAttribute(grouped_wgrad_pair<MODE>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-            return MOE_ERR_CUDA;
-        configured = true;
-    }
+    static PerDeviceOnce smem_attr;
+    if (!device_once(smem_attr, [smem] { return set_smem_limit(grouped_wgrad_pair<MODE>, smem); }))
+        return MOE_ERR_CUDA;
     const int pairs = std::min(num_sms() / 2, std::max(max_units, 1));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(2 * pairs));

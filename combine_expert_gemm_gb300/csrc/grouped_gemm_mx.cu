@@ -358,14 +358,11 @@ moe_status launch_gemm_mx(const CUtensorMap &a, const CUtensorMap &b0, const CUt
                           int N, int Kdim, int Nout, int max_row_tiles, const int32_t *count,
                           const int32_t *offset, uint8_t *out_q, uint8_t *out_sf, int *status,
                           cudaStream_t st) {
-    static bool configured = false;
-    if (!configured) {
-        if (cudaFuncSetAttribute(grouped_gemm_mx_pair<EPI>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem_bytes_mx(kMaxN)) != cudaSuccess)
-            return MOE_ERR_CUDA;
-        configured = true;
-    }
+    static PerDeviceOnce smem_attr;
+    if (!device_once(smem_attr, [] {
+            return set_smem_limit(grouped_gemm_mx_pair<EPI>, smem_bytes_mx(kMaxN));
+        }))
+        return MOE_ERR_CUDA;
     constexpr int BN_OUT = EPI == XEPI_SWIGLU ? XN / 2 : XN;
     const int64_t max_units = (int64_t)((max_row_tiles + 1) / 2 + N) * ((Nout + BN_OUT - 1) / BN_OUT);
     const int64_t pairs = std::min<int64_t>(num_sms() / 2, std::max<int64_t>(max_units, 1));

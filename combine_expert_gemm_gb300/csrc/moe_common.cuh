@@ -9,6 +9,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "../../include/moe.h"
@@ -50,12 +51,15 @@ inline moe_status launch_status() {
 }
 
 inline int num_sms() {
-    static int n = 0;
+    static std::atomic<int> cache[64];  // per device; 0 = not read yet
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) dev = 0;
+    std::atomic<int> *c = dev < 64 ? &cache[dev] : nullptr;
+    int n = c ? c->load(std::memory_order_relaxed) : 0;
     if (n == 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        if (n <= 0) n = 1;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 1;
+        if (c) c->store(n, std::memory_order_relaxed);
     }
     return n;
 }
@@ -66,6 +70,38 @@ moe_status launch_router_dx(const moe_shape *s, const moe_bf16 *dx_disp, const i
                             const float *w_router, const int32_t *topk_idx,
                             const float *topk_gate, const float *dgate, float *dlogit, float *dx,
                             bool add, cudaStream_t stream);
+
+// ---- host: one-time kernel attributes ------------------------------------
+
+// A kernel attribute such as the dynamic shared-memory limit belongs to the
+// device that was current when it was set.  device_once(o, fn) runs fn (which
+// returns true on success) once per device for the state o, also when several
+// host threads make their first call at the same time; devices past 63 are
+// refused.
+struct PerDeviceOnce {
+    std::atomic<uint64_t> done{0};  // bit d: fn succeeded on device d
+    std::mutex mu;
+};
+
+template <typename Fn>
+inline bool device_once(PerDeviceOnce &o, Fn &&fn) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    const uint64_t bit = 1ull << dev;
+    if (o.done.load(std::memory_order_acquire) & bit) return true;
+    std::lock_guard<std::mutex> lock(o.mu);
+    if (o.done.load(std::memory_order_relaxed) & bit) return true;
+    if (!fn()) return false;
+    o.done.fetch_or(bit, std::memory_order_release);
+    return true;
+}
+
+// Raises kernel's dynamic shared-memory limit to bytes on the current device.
+template <typename K>
+inline bool set_smem_limit(K *kernel, size_t bytes) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) ==
+           cudaSuccess;
+}
 
 // ---- host: TMA descriptors -----------------------------------------------
 

@@ -447,19 +447,15 @@ __global__ void route_assign(int T, int N, int K, int cap, const int32_t *__rest
 
 moe_status launch_logits(const moe_shape *s, const uint16_t *x, const float *w, const float *b,
                          int32_t *idx, float *gate, float *part, cudaStream_t st) {
-    static bool configured = false;
-    if (!configured) {
-        if (cudaFuncSetAttribute(route_logit_blocks<1, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)LogitTile<1, 4>::SMEM) != cudaSuccess ||
-            cudaFuncSetAttribute(route_logit_blocks<1, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)LogitTile<1, 8>::SMEM) != cudaSuccess ||
-            cudaFuncSetAttribute(route_topk<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)(sizeof(float) * kTopkTB * topk_row_stride(kMaxN))) != cudaSuccess ||
-            cudaFuncSetAttribute(route_topk<kMaxK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)(sizeof(float) * kTopkTB * topk_row_stride(kMaxN))) != cudaSuccess)
-            return MOE_ERR_CUDA;
-        configured = true;
-    }
+    static PerDeviceOnce smem_attr;
+    if (!device_once(smem_attr, [] {
+            const size_t topk_smem = sizeof(float) * kTopkTB * topk_row_stride(kMaxN);
+            return set_smem_limit(route_logit_blocks<1, 4>, LogitTile<1, 4>::SMEM) &&
+                   set_smem_limit(route_logit_blocks<1, 8>, LogitTile<1, 8>::SMEM) &&
+                   set_smem_limit(route_topk<8>, topk_smem) &&
+                   set_smem_limit(route_topk<kMaxK>, topk_smem);
+        }))
+        return MOE_ERR_CUDA;
     const int nb = logit_blocks(s->d);
     if (s->N <= 32) {
         const dim3 grid((s->T + LogitTile<1, 4>::TB - 1) / LogitTile<1, 4>::TB, nb,
@@ -509,14 +505,12 @@ moe_status route_enqueue(const moe_shape *s, const moe_bf16 *x, const float *w_r
         r = launch_logits(s, x, w_router, bias, topk_idx, topk_gate, part, st);
         if (r != MOE_OK) return r;
         const size_t smem = sizeof(uint32_t) * 2 * (kRankBlock / 32) * (size_t)s->N;
-        static bool configured = false;
-        if (smem > 48 * 1024 && !configured) {
-            if (cudaFuncSetAttribute(route_block_rank, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     2 * (kRankBlock / 32) * kMaxN * (int)sizeof(uint32_t)) !=
-                cudaSuccess)
-                return MOE_ERR_CUDA;
-            configured = true;
-        }
+        static PerDeviceOnce smem_attr;
+        if (smem > 48 * 1024 && !device_once(smem_attr, [] {
+                return set_smem_limit(route_block_rank,
+                                      2 * (kRankBlock / 32) * kMaxN * sizeof(uint32_t));
+            }))
+            return MOE_ERR_CUDA;
         route_block_rank<<<nblk, kRankBlock, smem, st>>>(s->T, s->N, s->K, topk_idx, route_row,
                                                           block_count);
         if ((r = launch_status()) != MOE_OK) return r;

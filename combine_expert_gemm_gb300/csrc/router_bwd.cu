@@ -303,13 +303,9 @@ inline int rb_chunks(int T) {
 moe_status launch_router_dw(const moe_shape *s, const moe_bf16 *x, const int32_t *topk_idx,
                             const float *dlogit, float *dw_router, float *dbias, void *ws,
                             cudaStream_t stream) {
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(router_dw_tile, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        227 * 1024);
-    });
-    if (attr_err != cudaSuccess) return MOE_ERR_CUDA;
+    static PerDeviceOnce smem_attr;
+    if (!device_once(smem_attr, [] { return set_smem_limit(router_dw_tile, 227 * 1024); }))
+        return MOE_ERR_CUDA;
     const int C = rb_chunks(s->T);
     float *pdw = dw_router, *pdb = dbias;
     if (C > 1) {
