@@ -177,8 +177,9 @@ route_logit_blocks(int T, int d, int N, const uint16_t *__restrict__ x,
     }
 }
 
-constexpr int kTopkTB = 32;     // tokens per CTA
+constexpr int kTopkTB = 8;      // tokens per CTA (one warp)
 constexpr int kTopkPlanes = 4;  // block-sum planes loaded before any is added
+constexpr int kTopkGroups = 4;  // float4 groups per lane loaded before any is added
 
 // Shared-memory row stride of the logits: at least N + 1 and 4 mod 32, so the
 // 32 lanes of a selecting warp (8 tokens x 4 lanes, lane s reading expert
@@ -187,46 +188,49 @@ __host__ __device__ constexpr int topk_row_stride(int N) {
     return N + 1 + (4 - (N + 1) % 32 + 32) % 32;
 }
 
-// Inserts (v, ie) into a list sorted best first; an entry that does not beat
-// the last one leaves the list unchanged.  Every index is a constant.
-template <int MAXK>
-__device__ __forceinline__ void topk_insert(float (&tv)[MAXK], int (&ti)[MAXK], float v, int ie) {
-    if (!beats(v, ie, tv[MAXK - 1], ti[MAXK - 1])) return;
+// Sorts M (value, index) pairs best first (logit descending, lower expert
+// first on ties) with a bitonic network: the compare-exchanges of a stage are
+// independent, and every index is a constant.
+template <int M>
+__device__ __forceinline__ void topk_sort(float (&v)[M], int (&ix)[M]) {
 #pragma unroll
-    for (int q = 0; q < MAXK; ++q) {
-        const bool sw = beats(v, ie, tv[q], ti[q]);
-        const float sv = tv[q];
-        const int si = ti[q];
-        tv[q] = sw ? v : sv;
-        ti[q] = sw ? ie : si;
-        v = sw ? sv : v;
-        ie = sw ? si : ie;
+    for (int k = 2; k <= M; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+#pragma unroll
+            for (int i = 0; i < M; ++i) {
+                const int l = i ^ j;
+                if (l <= i) continue;
+                const bool sw = (i & k) == 0 ? beats(v[l], ix[l], v[i], ix[i])
+                                             : beats(v[i], ix[i], v[l], ix[l]);
+                const float a = v[i], b = v[l];
+                const int ia = ix[i], ib = ix[l];
+                v[i] = sw ? b : a;
+                ix[i] = sw ? ib : ia;
+                v[l] = sw ? a : b;
+                ix[l] = sw ? ia : ib;
+            }
+        }
     }
 }
 
-// Replaces this lane's sorted list by the best MAXK of its union with the
-// list of lane ^ mask (both lanes end with the same list).  The better of
-// entry q and the partner's entry MAXK - 1 - q holds the best MAXK of the
-// union as a bitonic sequence; the bitonic merge network then sorts it.
-template <int MAXK>
-__device__ __forceinline__ void topk_merge(float (&tv)[MAXK], int (&ti)[MAXK], int mask) {
-    float pv[MAXK];
-    int pi[MAXK];
+// Replaces the sorted list (tv, ti) by the best M of its union with the
+// sorted list (pv, pi): the better of entry q and entry M - 1 - q of the other
+// list holds the best M of the union as a bitonic sequence, which the bitonic
+// merge network then sorts.
+template <int M>
+__device__ __forceinline__ void topk_merge_list(float (&tv)[M], int (&ti)[M], const float (&pv)[M],
+                                                const int (&pi)[M]) {
 #pragma unroll
-    for (int q = 0; q < MAXK; ++q) {
-        pv[q] = __shfl_xor_sync(0xFFFFFFFFu, tv[q], mask);
-        pi[q] = __shfl_xor_sync(0xFFFFFFFFu, ti[q], mask);
+    for (int q = 0; q < M; ++q) {
+        const bool take = beats(pv[M - 1 - q], pi[M - 1 - q], tv[q], ti[q]);
+        tv[q] = take ? pv[M - 1 - q] : tv[q];
+        ti[q] = take ? pi[M - 1 - q] : ti[q];
     }
 #pragma unroll
-    for (int q = 0; q < MAXK; ++q) {
-        const bool take = beats(pv[MAXK - 1 - q], pi[MAXK - 1 - q], tv[q], ti[q]);
-        tv[q] = take ? pv[MAXK - 1 - q] : tv[q];
-        ti[q] = take ? pi[MAXK - 1 - q] : ti[q];
-    }
+    for (int s = M / 2; s > 0; s >>= 1) {
 #pragma unroll
-    for (int s = MAXK / 2; s > 0; s >>= 1) {
-#pragma unroll
-        for (int q = 0; q < MAXK; ++q) {
+        for (int q = 0; q < M; ++q) {
             if (q & s) continue;
             const bool sw = beats(tv[q + s], ti[q + s], tv[q], ti[q]);
             const float a = tv[q], b = tv[q + s];
@@ -238,19 +242,36 @@ __device__ __forceinline__ void topk_merge(float (&tv)[MAXK], int (&ti)[MAXK], i
         }
     }
 }
-// route_topk: one CTA (4 warps) per 32 tokens.  The block sums of the tile
-// are contiguous in each block's [T][N] plane; every thread loads its float4
-// groups from kTopkPlanes planes before adding any of them, then adds them in
-// block order (+ bias) into shared memory.  Selection: 4 lanes per token, lane
+
+// The same with the list of lane ^ mask (both lanes end with the same list).
+template <int M>
+__device__ __forceinline__ void topk_merge(float (&tv)[M], int (&ti)[M], int mask) {
+    float pv[M];
+    int pi[M];
+#pragma unroll
+    for (int q = 0; q < M; ++q) {
+        pv[q] = __shfl_xor_sync(0xFFFFFFFFu, tv[q], mask);
+        pi[q] = __shfl_xor_sync(0xFFFFFFFFu, ti[q], mask);
+    }
+    topk_merge_list(tv, ti, pv, pi);
+}
+
+// route_topk: one CTA of one warp per 8 tokens (many small CTAs spread evenly
+// over the SMs).  The block sums of the tile are contiguous in each block's
+// [T][N] plane; every lane loads kTopkGroups float4 groups from kTopkPlanes
+// planes before adding any of them (one memory round trip for d <= 2048),
+// then adds them in block order (+ bias) into shared memory.  Selection: 4 lanes per token, lane
 // s keeping the best MAXK of experts s, s + 4, s + 8, ... (logit descending,
 // lower expert first on ties, NaN as -inf; unfilled entries are -inf with an
-// index past every expert, so any expert beats them); two merges over lane
-// shuffles give all four lanes the best MAXK of the token, whose first K are
-// the top K.  The order is strict and total, so the result does not depend on
+// index past every expert, so any expert beats them).  The lane takes its
+// experts MAXK at a time, sorts them with a bitonic network and merges them
+// into its list, so no step waits on a data-dependent branch; two merges over
+// lane shuffles then give all four lanes the best MAXK of the token, whose
+// first K are the top K.  The order is strict and total, so the result does not depend on
 // how the experts were split.  Gates: softmax over the K, shifted by the
 // largest, summed over k ascending.
 template <int MAXK>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(32)
 route_topk(int T, int N, int K, int nb, const float *__restrict__ part,
            const float *__restrict__ bias, int32_t *__restrict__ topk_idx,
            float *__restrict__ topk_gate) {
@@ -263,29 +284,43 @@ route_topk(int T, int N, int K, int nb, const float *__restrict__ part,
     const int64_t tile = (int64_t)t0 * N, n = (int64_t)tn * N;
     const int64_t plane = (int64_t)T * N;
     if ((N & 3) == 0) {
-        const float4 *p0 = reinterpret_cast<const float4 *>(part + tile);
-        for (int64_t g = tid; g < n / 4; g += blockDim.x) {
-            float4 v = __ldcs(p0 + g);
-            for (int b = 1; b < nb; b += kTopkPlanes) {
-                float4 w[kTopkPlanes];
+        // kTopkGroups groups x kTopkPlanes planes in flight per lane
+        for (int64_t g0 = tid; g0 < n / 4; g0 += kTopkGroups * blockDim.x) {
+            float4 v[kTopkGroups][kTopkPlanes];
+#pragma unroll
+            for (int u = 0; u < kTopkGroups; ++u) {
+                const int64_t g = g0 + u * blockDim.x;
 #pragma unroll
                 for (int c = 0; c < kTopkPlanes; ++c)
-                    if (b + c < nb)
-                        w[c] = __ldcs(reinterpret_cast<const float4 *>(part + (b + c) * plane + tile) + g);
-#pragma unroll
-                for (int c = 0; c < kTopkPlanes; ++c) {
-                    if (b + c >= nb) break;
-                    v.x = __fadd_rn(v.x, w[c].x);
-                    v.y = __fadd_rn(v.y, w[c].y);
-                    v.z = __fadd_rn(v.z, w[c].z);
-                    v.w = __fadd_rn(v.w, w[c].w);
-                }
+                    if (g < n / 4 && c < nb)
+                        v[u][c] = __ldcs(reinterpret_cast<const float4 *>(part + c * plane + tile) + g);
             }
-            const float vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                const int i = (int)(4 * g + h), tt = i / N, e = i - tt * N;
-                lg[tt * LDS + e] = bias ? __fadd_rn(vv[h], bias[e]) : vv[h];
+            for (int u = 0; u < kTopkGroups; ++u) {
+                const int64_t g = g0 + u * blockDim.x;
+                if (g >= n / 4) continue;
+                float4 a = v[u][0];
+#pragma unroll
+                for (int c = 1; c < kTopkPlanes; ++c) {
+                    if (c >= nb) break;
+                    a.x = __fadd_rn(a.x, v[u][c].x);
+                    a.y = __fadd_rn(a.y, v[u][c].y);
+                    a.z = __fadd_rn(a.z, v[u][c].z);
+                    a.w = __fadd_rn(a.w, v[u][c].w);
+                }
+                for (int c = kTopkPlanes; c < nb; ++c) {  // d > 2048
+                    const float4 w = __ldcs(reinterpret_cast<const float4 *>(part + c * plane + tile) + g);
+                    a.x = __fadd_rn(a.x, w.x);
+                    a.y = __fadd_rn(a.y, w.y);
+                    a.z = __fadd_rn(a.z, w.z);
+                    a.w = __fadd_rn(a.w, w.w);
+                }
+                const float vv[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const int i = (int)(4 * g + h), tt = i / N, e = i - tt * N;
+                    lg[tt * LDS + e] = bias ? __fadd_rn(vv[h], bias[e]) : vv[h];
+                }
             }
         }
     } else {
@@ -300,7 +335,7 @@ route_topk(int T, int N, int K, int nb, const float *__restrict__ part,
     __syncthreads();
 
     const int lane = tid & 31, sub = lane & 3;
-    const int tt = (tid >> 5) * 8 + (lane >> 2);
+    const int tt = lane >> 2;
     const int nloc = tt < tn ? N : 0;  // lanes past the tile only join the shuffles
     const float *l = lg + tt * LDS;
     float tv[MAXK];
@@ -310,15 +345,30 @@ route_topk(int T, int N, int K, int nb, const float *__restrict__ part,
         tv[q] = -INFINITY;
         ti[q] = 0x7FFFFFFF;
     }
-    int e = sub;
-    for (; e + 12 < nloc; e += 16) {
-        float v[4];
+    // this lane's experts sub + 4i, i < nper, in blocks of MAXK
+    const int nper = nloc > sub ? (nloc - sub + 3) / 4 : 0;
+    for (int i0 = 0; i0 < nper; i0 += MAXK) {
+        float bv[MAXK];
+        int bi[MAXK];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) v[u] = canon(l[e + 4 * u]);
+        for (int u = 0; u < MAXK; ++u) {
+            const bool ok = i0 + u < nper;
+            const int e = sub + 4 * (i0 + u);
+            const float raw = l[ok ? e : 0];
+            bv[u] = ok ? canon(raw) : -INFINITY;
+            bi[u] = ok ? e : 0x7FFFFFFF;
+        }
+        topk_sort(bv, bi);
+        if (i0 == 0) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u) topk_insert(tv, ti, v[u], e + 4 * u);
+            for (int q = 0; q < MAXK; ++q) {
+                tv[q] = bv[q];
+                ti[q] = bi[q];
+            }
+        } else {
+            topk_merge_list(tv, ti, bv, bi);
+        }
     }
-    for (; e < nloc; e += 4) topk_insert(tv, ti, canon(l[e]), e);
     topk_merge(tv, ti, 1);
     topk_merge(tv, ti, 2);
     if (nloc == 0) return;
@@ -472,8 +522,8 @@ moe_status launch_logits(const moe_shape *s, const uint16_t *x, const float *w, 
     if (r != MOE_OK) return r;
     const size_t tsmem = sizeof(float) * kTopkTB * topk_row_stride(s->N);
     auto *topk = s->K <= 8 ? route_topk<8> : route_topk<kMaxK>;
-    topk<<<(s->T + kTopkTB - 1) / kTopkTB, 128, tsmem, st>>>(s->T, s->N, s->K, nb, part, b, idx,
-                                                           gate);
+    topk<<<(s->T + kTopkTB - 1) / kTopkTB, 32, tsmem, st>>>(s->T, s->N, s->K, nb, part, b, idx,
+                                                          gate);
     return launch_status();
 }
 
