@@ -111,6 +111,11 @@ def _ptr(t, dtype=None, name="tensor"):
         raise TypeError(f"{name}: expected a torch.Tensor")
     if t.device.type != "cuda":
         raise ValueError(f"{name}: must be a CUDA tensor")
+    # the kernels run on the current device: memory of another GPU would be
+    # read through a pointer that is not this device's
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{name}: on {t.device}, but the current device is "
+                         f"cuda:{torch.cuda.current_device()}")
     if dtype is not None and t.dtype != dtype:
         raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
     if not t.is_contiguous():

@@ -229,3 +229,25 @@ def test_mxfp8_entry_points_argument_errors(moe):
     bad = list(c5); bad[1] = mis                       # y_scale misaligned
     assert lib.moe_combine_mxfp8(ctypes.byref(s), *bad, None) == 2
     assert lib.moe_combine_mxfp8(ctypes.byref(_shape(moe, d=136)), *c5, None) == 5
+
+
+def test_binding_refuses_tensors_of_another_device(moe, monkeypatch):
+    """The binding passes raw pointers to kernels on the current device, so a
+    tensor that lives on another GPU is refused before any call."""
+    import torch
+
+    class OnDevice(torch.Tensor):
+        index = 0
+
+        @property
+        def device(self):
+            return torch.device("cuda", type(self).index)
+
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 0)
+    t = torch.Tensor._make_subclass(OnDevice, torch.zeros(4, dtype=torch.int32))
+    assert moe._ptr(t, torch.int32, "route_row") == t.data_ptr()
+    OnDevice.index = 1
+    with pytest.raises(ValueError, match="route_row: on cuda:1"):
+        moe._ptr(t, torch.int32, "route_row")
+    with pytest.raises(ValueError, match="must be a CUDA tensor"):
+        moe._ptr(torch.zeros(4), None, "x")
