@@ -38,6 +38,7 @@ namespace {
 // Waits, with the bounded wait every kernel uses, on an mbarrier whose phase
 // nothing completes; the wait gives up after limit_ns and records the timeout.
 __global__ void selftest_wait_timeout(int *status, unsigned long long limit_ns) {
+    pdl_enter();
     __shared__ uint64_t bar;
     __shared__ int abort;
     if (threadIdx.x == 0) {
@@ -54,6 +55,6 @@ __global__ void selftest_wait_timeout(int *status, unsigned long long limit_ns) 
 MOE_API moe_status moe_selftest_wait_timeout(void *ws, uint64_t limit_ns, cudaStream_t stream) {
     if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return MOE_ERR_WORKSPACE;
     if (limit_ns == 0 || limit_ns > 100000000ull) return MOE_ERR_INVALID_ARG;
-    selftest_wait_timeout<<<1, 32, 0, stream>>>(static_cast<int *>(ws), limit_ns);
+    launch_pdl(selftest_wait_timeout, 1, 32, 0, stream, static_cast<int *>(ws), limit_ns);
     return launch_status();
 }

@@ -234,6 +234,7 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tm_a, const __grid_constan
                   const int32_t *__restrict__ count, const int32_t *__restrict__ offset,
                   const int32_t *__restrict__ row_token, uint16_t *__restrict__ out,
                   uint16_t *__restrict__ g_save, uint16_t *__restrict__ u_save, int *status) {
+    pdl_enter();
     constexpr int BN_OUT = EPI == EPI_SWIGLU ? MMA_N / 2 : MMA_N;
     constexpr int PM = 2 * BM;  // rows per pair tile
     extern __shared__ uint8_t smem_raw[];
@@ -471,13 +472,14 @@ moe_status launch_gemm_pair(const CUtensorMap &a, const CUtensorMap &b0, const C
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    set_pdl_attr(attr[1]);
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     if (cudaLaunchKernelEx(&cfg, grouped_gemm_pair<EPI, GATHER>, a, b0, b1, o, og, ou, N, Kdim,
                            Nout, count, offset, row_token, out, gs, us, status) != cudaSuccess)
         return MOE_ERR_CUDA;
@@ -489,6 +491,7 @@ moe_status launch_gemm_pair(const CUtensorMap &a, const CUtensorMap &b0, const C
 __global__ void __launch_bounds__(256)
 invert_route_rows(int64_t routes, int K, const int32_t *__restrict__ route_row,
                   int32_t *__restrict__ row_token) {
+    pdl_enter();
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= routes) return;
     const int32_t r = route_row[i];
@@ -592,8 +595,8 @@ MOE_API moe_status moe_expert_ffn_gather(const moe_shape *s, const moe_bf16 *x,
         return MOE_ERR_CUDA;
     int *status = static_cast<int *>(ws);
     const int64_t routes = (int64_t)s->T * s->K;
-    invert_route_rows<<<(unsigned)((routes + 255) / 256), 256, 0, stream>>>(routes, s->K, route_row,
-                                                                          row_token);
+    launch_pdl(invert_route_rows, (unsigned)((routes + 255) / 256), 256, 0, stream, routes, s->K,
+               route_row, row_token);
     if ((r = launch_status()) != MOE_OK) return r;
     const int64_t rows = std::min<int64_t>(R, routes);
     const int max_row_tiles = (int)((rows + BM - 1) / BM + s->N);

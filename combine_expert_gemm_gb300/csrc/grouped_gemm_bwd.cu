@@ -222,6 +222,7 @@ grouped_dgrad_pair(const __grid_constant__ CUtensorMap tm_a0, const __grid_const
                    const __grid_constant__ CUtensorMap tm_b0, const __grid_constant__ CUtensorMap tm_b1,
                    const __grid_constant__ CUtensorMap tm_o0, const __grid_constant__ CUtensorMap tm_o1,
                    const Params p) {
+    pdl_enter();
     static_assert(MODE == DGRAD_DH || MODE == DGRAD_DX, "dgrad only");
     constexpr int PM = 2 * BM;
     extern __shared__ uint8_t smem_raw[];
@@ -431,13 +432,14 @@ moe_status launch_dgrad_pair(const CUtensorMap &a0, const CUtensorMap &a1, const
     cfg.blockDim = dim3(ModeT<MODE>::threads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    set_pdl_attr(attr[1]);
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     if (cudaLaunchKernelEx(&cfg, grouped_dgrad_pair<MODE>, a0, a1, b0, b1, o0, o1, p) != cudaSuccess)
         return MOE_ERR_CUDA;
     return launch_status();
@@ -486,6 +488,7 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
 grouped_wgrad_pair(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
                    const __grid_constant__ CUtensorMap tm_b0, const __grid_constant__ CUtensorMap tm_o0,
                    const __grid_constant__ CUtensorMap tm_o1, const Params p) {
+    pdl_enter();
     static_assert(MODE == WGRAD_DOWN || MODE == WGRAD_GATEUP, "wgrad only");
     constexpr int PM = 2 * BM;
     extern __shared__ uint8_t smem_raw[];
@@ -758,13 +761,14 @@ moe_status launch_wgrad_pair(const CUtensorMap &a0, const CUtensorMap &a1, const
     cfg.blockDim = dim3(WG_THREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    set_pdl_attr(attr[1]);
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     if (cudaLaunchKernelEx(&cfg, grouped_wgrad_pair<MODE>, a0, a1, b0, o0, o1, p) != cudaSuccess)
         return MOE_ERR_CUDA;
     return launch_status();

@@ -100,6 +100,7 @@ grouped_gemm_mx_pair(const __grid_constant__ CUtensorMap tm_a, const __grid_cons
                      const __grid_constant__ CUtensorMap tm_sfb1, int N, int Kdim, int Nout,
                      const int32_t *__restrict__ count, const int32_t *__restrict__ offset,
                      uint8_t *__restrict__ out_q, uint8_t *__restrict__ out_sf, int *status) {
+    pdl_enter();
     constexpr int BN_OUT = EPI == XEPI_SWIGLU ? XN / 2 : XN;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -371,13 +372,14 @@ moe_status launch_gemm_mx(const CUtensorMap &a, const CUtensorMap &b0, const CUt
     cfg.blockDim = dim3(X_THREADS);
     cfg.dynamicSmemBytes = smem_bytes_mx(N);
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    set_pdl_attr(attr[1]);
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     if (cudaLaunchKernelEx(&cfg, grouped_gemm_mx_pair<EPI>, a, b0, b1, sfa, sfb0, sfb1, N, Kdim,
                            Nout, count, offset, out_q, out_sf, status) != cudaSuccess)
         return MOE_ERR_CUDA;

@@ -10,6 +10,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <utility>
 #include <mutex>
 
 #include "../../include/moe.h"
@@ -43,6 +44,41 @@ inline moe_status check_shape(const moe_shape *s) {
 inline int64_t buffer_rows(const moe_shape *s) {
     const int64_t a = (int64_t)s->N * s->cap, b = (int64_t)s->T * s->K;
     return a < b ? a : b;
+}
+
+// ---- programmatic dependent launch ----------------------------------------
+//
+// Every kernel of the library is launched with programmatic stream
+// serialization allowed (launch_pdl, or the same attribute beside a cluster
+// dimension).  Its first statement is pdl_enter(): wait until the grid before
+// it in the stream has completed and its memory is visible, then let the next
+// grid launch.  The next grid's CTAs are thus scheduled, up to their own
+// wait, while this grid runs, which hides the launch gap between kernels.
+// The wait comes before any memory access and before any early return, so a
+// grid never completes ahead of its predecessor.
+__device__ __forceinline__ void pdl_enter() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+inline void set_pdl_attr(cudaLaunchAttribute &a) {
+    a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    a.val.programmaticStreamSerializationAllowed = 1;
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    set_pdl_attr(attr[0]);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 inline moe_status launch_status() {

@@ -67,6 +67,7 @@ __device__ __forceinline__ void bf16x4(uint2 w, float &a0, float &a1, float &a2,
 __global__ void __launch_bounds__(kMxThreads)
 mx_quantize_weight_rows(int64_t rows, int k, const uint2 *__restrict__ w, uint32_t *__restrict__ q,
                         uint8_t *__restrict__ sf) {
+    pdl_enter();
     const int lane = threadIdx.x & 31;
     const int groups = k / 128;
     const int64_t items = rows * groups;
@@ -136,6 +137,7 @@ dispatch_mx_rows(int T, int d, int K, int N, const uint4 *__restrict__ x,
                  const int32_t *__restrict__ route_row, const int32_t *__restrict__ topk_idx,
                  const int32_t *__restrict__ count, const int32_t *__restrict__ offset,
                  uint4 *__restrict__ xq, uint8_t *__restrict__ xsf) {
+    pdl_enter();
     extern __shared__ int32_t pad_block[];
     const int lane = threadIdx.x & 31;
     if ((threadIdx.x >> 5) == 0) pad_block_prefix(N, count, pad_block, lane);
@@ -210,6 +212,7 @@ __global__ void __launch_bounds__(kMxThreads)
 combine_mx_rows(int T, int d, int K, const uint4 *__restrict__ yq, const uint8_t *__restrict__ ys,
                 const int32_t *__restrict__ route_row, const float *__restrict__ gate,
                 uint4 *__restrict__ y) {
+    pdl_enter();
     const int lane = threadIdx.x & 31;
     const int64_t q16 = d / 16;
     const int64_t y8 = d / 8;
@@ -280,8 +283,8 @@ MOE_API moe_status moe_mx_quantize_weights(int32_t E, int32_t rows, int32_t k, c
     if (n == 0 || k == 0) return MOE_OK;
     if (!w || !q || !sf) return MOE_ERR_INVALID_ARG;
     if (!aligned16(w) || !aligned16(q) || !aligned16(sf)) return MOE_ERR_ALIGNMENT;
-    mx_quantize_weight_rows<<<mx_grid(n * (k / 128)), kMxThreads, 0, stream>>>(
-        n, k, reinterpret_cast<const uint2 *>(w), reinterpret_cast<uint32_t *>(q), sf);
+    launch_pdl(mx_quantize_weight_rows, mx_grid(n * (k / 128)), kMxThreads, 0, stream, n, k,
+               reinterpret_cast<const uint2 *>(w), reinterpret_cast<uint32_t *>(q), sf);
     return launch_status();
 }
 
@@ -298,9 +301,9 @@ MOE_API moe_status moe_dispatch_mxfp8(const moe_shape *s, const moe_bf16 *x,
     if (!aligned16(x) || !aligned16(route_row) || !aligned16(topk_idx) || !aligned16(x_q) ||
         !aligned16(x_sf))
         return MOE_ERR_ALIGNMENT;
-    dispatch_mx_rows<<<mx_grid(s->T), kMxThreads, sizeof(int32_t) * s->N, stream>>>(
-        s->T, s->d, s->K, s->N, reinterpret_cast<const uint4 *>(x), route_row, topk_idx,
-        expert_count, expert_offset, reinterpret_cast<uint4 *>(x_q), x_sf);
+    launch_pdl(dispatch_mx_rows, mx_grid(s->T), kMxThreads, sizeof(int32_t) * s->N, stream, s->T,
+               s->d, s->K, s->N, reinterpret_cast<const uint4 *>(x), route_row, topk_idx,
+               expert_count, expert_offset, reinterpret_cast<uint4 *>(x_q), x_sf);
     return launch_status();
 }
 
@@ -317,8 +320,8 @@ MOE_API moe_status moe_combine_mxfp8(const moe_shape *s, const uint8_t *y_q, con
         !aligned16(y))
         return MOE_ERR_ALIGNMENT;
     auto *kern = s->K <= 8 ? combine_mx_rows<8> : combine_mx_rows<16>;
-    kern<<<mx_grid(s->T), kMxThreads, 0, stream>>>(s->T, s->d, s->K,
-                                                 reinterpret_cast<const uint4 *>(y_q), y_scale,
-                                                 route_row, topk_gate, reinterpret_cast<uint4 *>(y));
+    launch_pdl(kern, mx_grid(s->T), kMxThreads, 0, stream, s->T, s->d, s->K,
+               reinterpret_cast<const uint4 *>(y_q), y_scale, route_row, topk_gate,
+               reinterpret_cast<uint4 *>(y));
     return launch_status();
 }

@@ -83,6 +83,7 @@ template <int WE, int EPL>
 __global__ void __launch_bounds__(kLogitThreads)
 route_logit_blocks(int T, int d, int N, const uint16_t *__restrict__ x,
                    const float *__restrict__ w_r, float *__restrict__ part) {
+    pdl_enter();
     using L = LogitTile<WE, EPL>;
     constexpr int JC = kLogitJC, XR = kLogitXR, WR = kLogitWR, TB = L::TB, EC = L::EC;
     constexpr int kLogitStage = L::STAGE;
@@ -275,6 +276,7 @@ __global__ void __launch_bounds__(32)
 route_topk(int T, int N, int K, int nb, const float *__restrict__ part,
            const float *__restrict__ bias, int32_t *__restrict__ topk_idx,
            float *__restrict__ topk_gate) {
+    pdl_enter();
     extern __shared__ __align__(16) uint8_t smem_t[];
     const int LDS = topk_row_stride(N);
     float *lg = reinterpret_cast<float *>(smem_t);  // [kTopkTB][LDS]
@@ -394,6 +396,7 @@ route_topk(int T, int N, int K, int nb, const float *__restrict__ part,
 __global__ void __launch_bounds__(kRankBlock)
 route_block_rank(int T, int N, int K, const int32_t *__restrict__ topk_idx,
                  int32_t *__restrict__ route_row, int32_t *__restrict__ block_count) {
+    pdl_enter();
     extern __shared__ uint32_t sm[];
     uint32_t *mask = sm;                       // [8][N]: bit lane of warp w chose e
     uint32_t *wpre = sm + (kRankBlock / 32) * N;  // [8][N]: routes to e in earlier warps
@@ -434,6 +437,7 @@ __global__ void __launch_bounds__(1024)
 route_scan(int nblk, int N, int cap, int32_t *__restrict__ block_count,
            int32_t *__restrict__ expert_count, int32_t *__restrict__ expert_offset,
            int32_t *__restrict__ expert_demand) {
+    pdl_enter();
     __shared__ int32_t warp_sum[32];
     const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
     int32_t cnt = 0;
@@ -487,6 +491,7 @@ __global__ void route_assign(int T, int N, int K, int cap, const int32_t *__rest
                              const int32_t *__restrict__ block_base,
                              const int32_t *__restrict__ expert_offset,
                              int32_t *__restrict__ route_row) {
+    pdl_enter();
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= (int64_t)T * K) return;
     const int t = (int)(i / K);
@@ -510,20 +515,20 @@ moe_status launch_logits(const moe_shape *s, const uint16_t *x, const float *w, 
     if (s->N <= 32) {
         const dim3 grid((s->T + LogitTile<1, 4>::TB - 1) / LogitTile<1, 4>::TB, nb,
                         (s->N + LogitTile<1, 4>::EC - 1) / LogitTile<1, 4>::EC);
-        route_logit_blocks<1, 4><<<grid, kLogitThreads, LogitTile<1, 4>::SMEM, st>>>(s->T, s->d, s->N, x,
-                                                                             w, part);
+        launch_pdl(route_logit_blocks<1, 4>, grid, kLogitThreads, LogitTile<1, 4>::SMEM, st, s->T,
+                   s->d, s->N, x, w, part);
     } else {
         const dim3 grid((s->T + LogitTile<1, 8>::TB - 1) / LogitTile<1, 8>::TB, nb,
                         (s->N + LogitTile<1, 8>::EC - 1) / LogitTile<1, 8>::EC);
-        route_logit_blocks<1, 8><<<grid, kLogitThreads, LogitTile<1, 8>::SMEM, st>>>(s->T, s->d, s->N, x,
-                                                                             w, part);
+        launch_pdl(route_logit_blocks<1, 8>, grid, kLogitThreads, LogitTile<1, 8>::SMEM, st, s->T,
+                   s->d, s->N, x, w, part);
     }
     moe_status r = launch_status();
     if (r != MOE_OK) return r;
     const size_t tsmem = sizeof(float) * kTopkTB * topk_row_stride(s->N);
     auto *topk = s->K <= 8 ? route_topk<8> : route_topk<kMaxK>;
-    topk<<<(s->T + kTopkTB - 1) / kTopkTB, 32, tsmem, st>>>(s->T, s->N, s->K, nb, part, b, idx,
-                                                          gate);
+    launch_pdl(topk, (s->T + kTopkTB - 1) / kTopkTB, 32, tsmem, st, s->T, s->N, s->K, nb, part, b,
+               idx, gate);
     return launch_status();
 }
 
@@ -561,18 +566,18 @@ moe_status route_enqueue(const moe_shape *s, const moe_bf16 *x, const float *w_r
                                       2 * (kRankBlock / 32) * kMaxN * sizeof(uint32_t));
             }))
             return MOE_ERR_CUDA;
-        route_block_rank<<<nblk, kRankBlock, smem, st>>>(s->T, s->N, s->K, topk_idx, route_row,
-                                                          block_count);
+        launch_pdl(route_block_rank, nblk, kRankBlock, smem, st, s->T, s->N, s->K, topk_idx,
+                   route_row, block_count);
         if ((r = launch_status()) != MOE_OK) return r;
     }
-    route_scan<<<1, 1024, 0, st>>>(nblk, s->N, s->cap, block_count, expert_count, expert_offset,
-                                   expert_demand);
+    launch_pdl(route_scan, 1, 1024, 0, st, nblk, s->N, s->cap, block_count, expert_count,
+               expert_offset, expert_demand);
     if ((r = launch_status()) != MOE_OK) return r;
     if (s->T > 0) {
         const int64_t routes = (int64_t)s->T * s->K;
         const int grid = (int)((routes + 255) / 256);
-        route_assign<<<grid, 256, 0, st>>>(s->T, s->N, s->K, s->cap, topk_idx, block_count,
-                                           expert_offset, route_row);
+        launch_pdl(route_assign, grid, 256, 0, st, s->T, s->N, s->K, s->cap, topk_idx, block_count,
+                   expert_offset, route_row);
         r = launch_status();
     }
     return r;

@@ -120,6 +120,7 @@ __global__ void __launch_bounds__(RB_THREADS, 2)
 router_dw_tile(int T, int d, int N, int K, int nchunk, const uint16_t *__restrict__ x,
                const int32_t *__restrict__ topk_idx, const float *__restrict__ dlogit,
                float *__restrict__ pdw, float *__restrict__ pdb) {
+    pdl_enter();
     extern __shared__ __align__(16) uint8_t rb_smem[];
     const RbSmem s = rb_carve(rb_smem, N, K);
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
@@ -253,6 +254,7 @@ constexpr int RS_GROUPS = 8;
 __global__ void __launch_bounds__(32 * RS_GROUPS)
 router_dw_sum(int64_t n4, int N, int nchunk, const float4 *__restrict__ pdw,
               const float *__restrict__ pdb, float4 *__restrict__ dw, float *__restrict__ dbias) {
+    pdl_enter();
     __shared__ float4 part[RS_GROUPS][32];
     __shared__ float bpart[RS_GROUPS][32];
     const int lane = threadIdx.x & 31, g = threadIdx.x >> 5;
@@ -313,15 +315,15 @@ moe_status launch_router_dw(const moe_shape *s, const moe_bf16 *x, const int32_t
         pdb = dbias ? pdw + (size_t)C * s->N * s->d : nullptr;
     }
     const dim3 grid(C, (s->d + RB_SLAB - 1) / RB_SLAB);
-    router_dw_tile<<<grid, RB_THREADS, rb_smem_bytes(s->N, s->K), stream>>>(
-        s->T, s->d, s->N, s->K, C, x, topk_idx, dlogit, pdw, pdb);
+    launch_pdl(router_dw_tile, grid, RB_THREADS, rb_smem_bytes(s->N, s->K), stream, s->T, s->d,
+               s->N, s->K, C, x, topk_idx, dlogit, pdw, pdb);
     moe_status r = launch_status();
     if (r != MOE_OK || C == 1) return r;
     const int64_t n4 = (int64_t)s->N * s->d / 4;
     const int64_t blocks = (std::max<int64_t>(n4, s->N) + 31) / 32;
-    router_dw_sum<<<(unsigned)blocks, 32 * RS_GROUPS, 0, stream>>>(n4, s->N, C,
-                                                        reinterpret_cast<const float4 *>(pdw), pdb,
-                                                        reinterpret_cast<float4 *>(dw_router), dbias);
+    launch_pdl(router_dw_sum, (unsigned)blocks, 32 * RS_GROUPS, 0, stream, n4, s->N, C,
+               reinterpret_cast<const float4 *>(pdw), pdb, reinterpret_cast<float4 *>(dw_router),
+               dbias);
     return launch_status();
 }
 

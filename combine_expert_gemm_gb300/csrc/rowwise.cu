@@ -36,6 +36,7 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
 __global__ void __launch_bounds__(kThreads)
 dispatch_rows(int T, int nchunk, int K, const uint4 *__restrict__ x,
               const int32_t *__restrict__ route_row, uint4 *__restrict__ x_disp) {
+    pdl_enter();
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
     if (t >= T) return;
@@ -68,6 +69,7 @@ __global__ void __launch_bounds__(kThreads, MAXK <= 8 ? 4 : 2)
 combine_rows(int T, int nchunk, int K, const uint4 *__restrict__ y_disp,
              const int32_t *__restrict__ route_row, const float *__restrict__ gate,
              uint4 *__restrict__ y) {
+    pdl_enter();
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
     if (t >= T) return;
@@ -110,6 +112,7 @@ combine_bwd_rows(int T, int nchunk, int K, const uint4 *__restrict__ dy,
                  const uint4 *__restrict__ y_disp, const int32_t *__restrict__ route_row,
                  const float *__restrict__ gate, uint4 *__restrict__ dy_disp,
                  float *__restrict__ dgate) {
+    pdl_enter();
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
     if (t >= T) return;
@@ -175,6 +178,7 @@ dispatch_bwd_rows(int T, int nchunk, int K, int N, const uint4 *__restrict__ dx_
                   const float4 *__restrict__ w_r, const int32_t *__restrict__ topk_idx,
                   const float *__restrict__ gate, const float *__restrict__ dgate,
                   float *__restrict__ dlogit) {
+    pdl_enter();
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
     if (t >= T) return;
@@ -288,9 +292,8 @@ MOE_API moe_status moe_dispatch(const moe_shape *s, const moe_bf16 *x, const int
     if (s->T == 0 || s->cap == 0) return MOE_OK;  // no row can be written
     if (!x || !route_row || !x_disp) return MOE_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(route_row) || !aligned16(x_disp)) return MOE_ERR_ALIGNMENT;
-    dispatch_rows<<<grid_for(s->T), kThreads, 0, stream>>>(
-        s->T, s->d / 8, s->K, reinterpret_cast<const uint4 *>(x), route_row,
-        reinterpret_cast<uint4 *>(x_disp));
+    launch_pdl(dispatch_rows, grid_for(s->T), kThreads, 0, stream, s->T, s->d / 8, s->K,
+               reinterpret_cast<const uint4 *>(x), route_row, reinterpret_cast<uint4 *>(x_disp));
     return launch_status();
 }
 
@@ -304,9 +307,9 @@ MOE_API moe_status moe_combine(const moe_shape *s, const moe_bf16 *y_disp,
     if (!aligned16(y_disp) || !aligned16(route_row) || !aligned16(topk_gate) || !aligned16(y))
         return MOE_ERR_ALIGNMENT;
     auto *kern = s->K <= 8 ? combine_rows<8> : combine_rows<16>;
-    kern<<<grid_for(s->T), kThreads, 0, stream>>>(s->T, s->d / 8, s->K,
-                                                 reinterpret_cast<const uint4 *>(y_disp),
-                                                 route_row, topk_gate, reinterpret_cast<uint4 *>(y));
+    launch_pdl(kern, grid_for(s->T), kThreads, 0, stream, s->T, s->d / 8, s->K,
+               reinterpret_cast<const uint4 *>(y_disp), route_row, topk_gate,
+               reinterpret_cast<uint4 *>(y));
     return launch_status();
 }
 
@@ -323,10 +326,9 @@ MOE_API moe_status moe_combine_backward(const moe_shape *s, const moe_bf16 *dy,
         !aligned16(dy_disp) || !aligned16(dgate))
         return MOE_ERR_ALIGNMENT;
     auto *kern = s->K <= 8 ? combine_bwd_rows<8> : combine_bwd_rows<16>;
-    kern<<<grid_for(s->T), kThreads, 0, stream>>>(
-        s->T, s->d / 8, s->K, reinterpret_cast<const uint4 *>(dy),
-        reinterpret_cast<const uint4 *>(y_disp), route_row, topk_gate,
-        reinterpret_cast<uint4 *>(dy_disp), dgate);
+    launch_pdl(kern, grid_for(s->T), kThreads, 0, stream, s->T, s->d / 8, s->K,
+               reinterpret_cast<const uint4 *>(dy), reinterpret_cast<const uint4 *>(y_disp),
+               route_row, topk_gate, reinterpret_cast<uint4 *>(dy_disp), dgate);
     return launch_status();
 }
 
@@ -339,10 +341,9 @@ MOE_API moe_status moe_dispatch_backward(const moe_shape *s, const moe_bf16 *dx_
     if (!route_row || !dx || (s->cap > 0 && !dx_disp)) return MOE_ERR_INVALID_ARG;
     if (!aligned16(dx_disp) || !aligned16(route_row) || !aligned16(dx)) return MOE_ERR_ALIGNMENT;
     auto *kern = s->K <= 8 ? dispatch_bwd_rows<8, DBWD_PLAIN> : dispatch_bwd_rows<16, DBWD_PLAIN>;
-    kern<<<grid_for(s->T), kThreads, 0, stream>>>(s->T, s->d / 8, s->K, s->N,
-                                                 reinterpret_cast<const uint4 *>(dx_disp), route_row,
-                                                 reinterpret_cast<float4 *>(dx), nullptr, nullptr,
-                                                 nullptr, nullptr, nullptr);
+    launch_pdl(kern, grid_for(s->T), kThreads, 0, stream, s->T, s->d / 8, s->K, s->N,
+               reinterpret_cast<const uint4 *>(dx_disp), route_row, reinterpret_cast<float4 *>(dx),
+               nullptr, nullptr, nullptr, nullptr, nullptr);
     return launch_status();
 }
 
@@ -362,10 +363,9 @@ moe_status launch_router_dx(const moe_shape *s, const moe_bf16 *dx_disp, const i
                          : dispatch_bwd_rows<16, DBWD_ROUTER_ADD>;
     else
         kern = s->K <= 8 ? dispatch_bwd_rows<8, DBWD_ROUTER> : dispatch_bwd_rows<16, DBWD_ROUTER>;
-    kern<<<grid_for(s->T), kThreads, 0, stream>>>(
-        s->T, s->d / 8, s->K, s->N, reinterpret_cast<const uint4 *>(dx_disp), route_row,
-        reinterpret_cast<float4 *>(dx), reinterpret_cast<const float4 *>(w_router), topk_idx,
-        topk_gate, dgate, dlogit);
+    launch_pdl(kern, grid_for(s->T), kThreads, 0, stream, s->T, s->d / 8, s->K, s->N,
+               reinterpret_cast<const uint4 *>(dx_disp), route_row, reinterpret_cast<float4 *>(dx),
+               reinterpret_cast<const float4 *>(w_router), topk_idx, topk_gate, dgate, dlogit);
     return launch_status();
 }
 }  // namespace moe
