@@ -138,7 +138,7 @@ route_logit_blocks(int T, int d, int N, const uint16_t *__restrict__ x,
             const uint16_t *xs = reinterpret_cast<const uint16_t *>(st) + tok0 * XR;
             const float *ws = reinterpret_cast<const float *>(st + TB * XR * 2) + exp0 * WR;
             const int jn = min(JC, jlen - c * JC);  // a multiple of 8
-#pragma unroll 2
+#pragma unroll 4
             for (int j = 0; j < jn; j += 4) {
                 uint2 xv[8];  // tokens tok0 + 4i, 4 bf16 at j .. j + 3
 #pragma unroll
