@@ -8,10 +8,11 @@
 // int32 cumulative offsets produced and kept on the device).  AWS Neuron
 // "Expert Parallelism (EP)", "Router Weights" (logits for every expert).
 //
-// Five launches, none of which waits on another CTA:
+// Five launches; no CTA spins on another, and each kernel waits only for the
+// grid before it (programmatic dependent launch):
 //   1. route_logit_blocks: fp32 block sums of the logits (per 512-wide block
 //      of j one fused multiply-add chain over j ascending), one CTA per
-//      (token tile, block);
+//      (token tile, block, group of 64 experts);
 //   1b. route_topk: the block sums added in block order (+ bias), so the
 //      logits are reproducible bit for bit; then four lanes per token select
 //      the top K and compute the gates.
@@ -47,9 +48,10 @@ __device__ __forceinline__ bool beats(float a, int ia, float b, int ib) {
 // the block sums of 128 tokens x the z-th group of EC experts and writes them
 // to part[b][t][e]; the passes sit in the grid rather than in a loop, so that
 // a layer with many experts gets many short CTAs instead of a second, nearly
-// empty wave of long ones.  4 warps, each 32 tokens x EC experts; lane = tx + 8 ty (tx in
-// 0..7, ty in 0..3) owns tokens ty + 4i (i = 0..7) and experts tx + 8b (b <
-// EPL): 8 EPL chains, advanced two tokens at a time by the packed fp32x2 fma.
+// empty wave of long ones.  4 warps, each 32 tokens x EC experts; lane =
+// tx + 8 ty (tx in 0..7, ty in 0..3) owns tokens ty + 4i (i = 0..7) and
+// experts tx + 8b (b < EPL): 8 EPL chains, advanced two tokens at a time by
+// the packed fp32x2 fma; the j loop over a chunk is unrolled four ways.
 // EPL = 8 (64 experts per pass) when N > 32, else 4: each widened pair of x
 // values then feeds 8 paired fmas instead of 4, which halves the conversion
 // and register-move instructions per fma (they, not memory, bound the loop).
