@@ -21,7 +21,8 @@
 //      routes to the same expert inside the block, and the block's count per
 //      expert.  Bitmask OR is order-free, so the ranks are deterministic.
 //   3. route_scan: one CTA scans the per-block counts for every expert
-//      (giving each block its base slot), clamps demand to capacity and scans
+//      (giving each block its base slot; up to 32 threads per expert, each
+//      over a contiguous chunk of blocks), clamps demand to capacity and scans
 //      the counts into the cumulative offsets.
 //   4. route_assign: slot = block base + rank; row = offset + slot, or -1 past
 //      capacity.
@@ -433,20 +434,53 @@ route_block_rank(int T, int N, int K, const int32_t *__restrict__ topk_idx,
     }
 }
 
-// One CTA of 1024 threads: thread e turns the per-block counts of expert e
-// into per-block base slots, then all threads scan the clamped counts.
+// Sums the counts of blocks [b0, b1) of expert e.
+__device__ __forceinline__ int32_t block_count_sum(const int32_t *__restrict__ block_count,
+                                                   int N, int e, int b0, int b1) {
+    int32_t s = 0;
+    int b = b0;
+    for (; b + 8 <= b1; b += 8) {
+        int32_t c[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) c[q] = block_count[(int64_t)(b + q) * N + e];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) s += c[q];
+    }
+    for (; b < b1; ++b) s += block_count[(int64_t)b * N + e];
+    return s;
+}
+
+// Threads per expert in route_scan: at most 32, at most 1024 / N, and at
+// least 4 blocks for each.
+__host__ __device__ inline int scan_lanes_per_expert(int nblk, int N) {
+    return max(1, min(min(32, kMaxN / N), nblk / 4));
+}
+
+// One CTA of 1024 threads.  Thread p * N + e (p < P, P threads per expert)
+// owns the contiguous chunk p of the per-block counts of expert e: it sums
+// its chunk, adds the sums of the chunks before it (in chunk order), and
+// rewrites its chunk's counts as base slots.  Every count is read in two
+// rounds of loads whatever the number of blocks, instead of one round per 8
+// blocks.  Then threads 0..N-1 scan the clamped counts over the experts.
 __global__ void __launch_bounds__(1024)
 route_scan(int nblk, int N, int cap, int32_t *__restrict__ block_count,
            int32_t *__restrict__ expert_count, int32_t *__restrict__ expert_offset,
            int32_t *__restrict__ expert_demand) {
     pdl_enter();
     __shared__ int32_t warp_sum[32];
-    const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
-    int32_t cnt = 0;
-    if (e < N) {
+    __shared__ int32_t chunk_sum[kMaxN];  // [P][N]
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int P = scan_lanes_per_expert(nblk, N);
+    const int chunk = (nblk + P - 1) / P;
+    const int p = tid / N, e = tid % N;
+    const int b0 = min(p * chunk, nblk), b1 = min(b0 + chunk, nblk);
+    if (p < P) chunk_sum[tid] = block_count_sum(block_count, N, e, b0, b1);
+    __syncthreads();
+    if (p < P) {
         int32_t run = 0;
-        int b = 0;
-        for (; b + 8 <= nblk; b += 8) {
+        for (int q = 0; q < p; ++q) run += chunk_sum[q * N + e];
+        int b = b0;
+        for (; b + 8 <= b1; b += 8) {
             int32_t c[8];
 #pragma unroll
             for (int q = 0; q < 8; ++q) c[q] = block_count[(int64_t)(b + q) * N + e];
@@ -456,14 +490,19 @@ route_scan(int nblk, int N, int cap, int32_t *__restrict__ block_count,
                 run += c[q];
             }
         }
-        for (; b < nblk; ++b) {
+        for (; b < b1; ++b) {
             const int32_t c = block_count[(int64_t)b * N + e];
             block_count[(int64_t)b * N + e] = run;
             run += c;
         }
-        expert_demand[e] = run;
-        cnt = min(run, cap);
-        expert_count[e] = cnt;
+    }
+    int32_t cnt = 0;
+    if (tid < N) {
+        int32_t demand = 0;
+        for (int q = 0; q < P; ++q) demand += chunk_sum[q * N + tid];
+        expert_demand[tid] = demand;
+        cnt = min(demand, cap);
+        expert_count[tid] = cnt;
     }
     // exclusive scan of cnt over e
     int32_t incl = cnt;
@@ -485,8 +524,8 @@ route_scan(int nblk, int N, int cap, int32_t *__restrict__ block_count,
     }
     __syncthreads();
     const int32_t base = warp > 0 ? warp_sum[warp - 1] : 0;
-    if (e < N) expert_offset[e] = base + incl - cnt;
-    if (e == N - 1) expert_offset[N] = base + incl;
+    if (tid < N) expert_offset[tid] = base + incl - cnt;
+    if (tid == N - 1) expert_offset[N] = base + incl;
 }
 
 __global__ void route_assign(int T, int N, int K, int cap, const int32_t *__restrict__ topk_idx,
