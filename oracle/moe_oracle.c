@@ -28,8 +28,8 @@
  *          for all experts from a replicated router weight).
  *
  * Readings where the pages are silent (each is listed in the design notes):
- *   - logits: fp32; per 512-wide block of j one fused multiply-add chain over
- *     j ascending, the block sums added in block order, then + bias;
+ *   - logits: fp32, one fused multiply-add chain from 0 over j ascending (the
+ *     plain left-to-right dot product), then + bias as a separate addition;
  *   - top-K: logit descending, lower expert index first on ties, NaN as -inf;
  *   - gates: softmax over the K selected logits (equal, in exact arithmetic, to
  *     a full softmax renormalised over the K selected); computed in fp64;
@@ -98,24 +98,18 @@ void oracle_bf16_from_f32(int64_t n, const float *v, uint16_t *out) {
 /* ------------------------------------------------------- R0: router logits ---
  * [NRN] "Router Weights": every token gets an affinity for every expert from
  * the replicated router weight, logit[t][e] = <x_t, W_r[e]> (+ bias[e]).
- * The pages fix no summation order.  Reading: fp32, the j range cut into
- * blocks of 512; within a block one fused multiply-add chain from 0 over j
- * ascending; the block sums added in ascending block order; then + bias.
+ * The pages fix no summation order.  Reading: the dot product as written,
+ * summed left to right in fp32 -- one fused multiply-add chain that starts
+ * at 0 and takes j = 0, 1, ..., d-1 in turn (x widened exactly from bf16) --
+ * then + bias[e] as one fp32 addition.
  */
-#define ORACLE_LOGIT_BLOCK 512
-
 void oracle_router_logits(int T, int d, int N, const uint16_t *x, const float *w_r,
                           const float *bias, float *logits) {
     for (int t = 0; t < T; ++t)
         for (int e = 0; e < N; ++e) {
             float acc = 0.0f;
-            for (int j0 = 0; j0 < d; j0 += ORACLE_LOGIT_BLOCK) {
-                const int j1 = j0 + ORACLE_LOGIT_BLOCK < d ? j0 + ORACLE_LOGIT_BLOCK : d;
-                float part = 0.0f;
-                for (int j = j0; j < j1; ++j)
-                    part = fmaf(bf16_to_f32(x[(int64_t)t * d + j]), w_r[(int64_t)e * d + j], part);
-                acc = j0 == 0 ? part : acc + part;
-            }
+            for (int j = 0; j < d; ++j)
+                acc = fmaf(bf16_to_f32(x[(int64_t)t * d + j]), w_r[(int64_t)e * d + j], acc);
             if (bias) acc = acc + bias[e];
             logits[(int64_t)t * N + e] = acc;
         }

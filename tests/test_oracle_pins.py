@@ -185,35 +185,52 @@ def test_logits_exact_on_integers_and_error_bound():
     bound = 512 * 2.0 ** -24 * (np.abs(xf) @ np.abs(w.astype(np.float64)).T)
     assert np.all(np.abs(got - exact) <= bound)
 
-    # d = 2000 (four blocks, the last ragged): within (512 + 4) u sum|x w|
+    # d = 2000: within the recursive-summation bound d u sum|x w| (each fused
+    # multiply-add rounds once, so d roundings in all)
     x = synth.normal_bf16(13, (T, 2000))
     w = synth.normal_f32(14, (N, 2000), 0.02)
     got = oracle.router_logits(x, w).astype(np.float64)
     xf = oracle.bf16_to_f32(x).astype(np.float64)
     exact = np.array([[math.fsum(xf[t] * w[e].astype(np.float64)) for e in range(N)]
                       for t in range(T)])
-    bound = 516 * 2.0 ** -24 * (np.abs(xf) @ np.abs(w.astype(np.float64)).T)
+    bound = 2000 * 2.0 ** -24 * (np.abs(xf) @ np.abs(w.astype(np.float64)).T)
     assert np.all(np.abs(got - exact) <= bound)
 
 
-def test_logits_blocks_of_512():
-    """The reading of the logit order: one fp32 chain per 512-wide block of j,
-    block sums added in order.  Block 0 holds a single product 2^24 and block
-    1 holds 512 unit products: the blocked sum is the exact 2^24 + 512, which
-    one chain over all j would lose (each +1 onto 2^24 rounds back to even)."""
+def test_logits_left_to_right_order():
+    """The logit is the dot product summed left to right from 0 (j = 0 first).
+    With the product 2^24 first and 1023 unit products after it, every +1 meets
+    2^24, lies exactly halfway between two fp32 neighbours and rounds back to
+    the even 2^24, so the sum stays 2^24; a sum cut into blocks (say of 512)
+    would keep the later blocks' ones exactly and end above 2^24.  The same
+    products in the reverse order sum exactly to 1023 before meeting 2^24,
+    giving 2^24 + 1023, which rounds to 2^24 + 1024."""
     d = 1024
-    x = np.zeros((1, d), np.float32)
-    w = np.zeros((1, d), np.float32)
-    x[0, 7], w[0, 7] = 4096.0, 4096.0
-    x[0, 512:], w[0, 512:] = 1.0, 1.0
-    got = oracle.router_logits(synth.f32_to_bf16_bits(x), w)
-    assert got[0, 0] == np.float32(2.0 ** 24 + 512)
-    # the same products inside one block meet 2^24 one at a time
-    x2 = np.zeros((1, 512), np.float32)
-    w2 = np.zeros((1, 512), np.float32)
-    x2[0, 0], w2[0, 0] = 4096.0, 4096.0
-    x2[0, 1:], w2[0, 1:] = 1.0, 1.0
-    assert oracle.router_logits(synth.f32_to_bf16_bits(x2), w2)[0, 0] == np.float32(2.0 ** 24)
+    x = np.ones((2, d), np.float32)
+    w = np.ones((1, d), np.float32)
+    x[0, 0] = 4096.0
+    w[0, 0] = 4096.0
+    x[1, d - 1] = 4096.0  # token 1: the large product comes last ...
+    w2 = np.ones((1, d), np.float32)
+    w2[0, d - 1] = 4096.0
+    got = oracle.router_logits(synth.f32_to_bf16_bits(x[:1]), w)
+    assert got[0, 0] == np.float32(2.0 ** 24)
+    got = oracle.router_logits(synth.f32_to_bf16_bits(x[1:]), w2)
+    assert got[0, 0] == np.float32(2.0 ** 24 + 1024)
+
+
+def test_logits_fused_multiply_add():
+    """Each step is one fused multiply-add (a single rounding of x*w + acc):
+    x = 1 + 2^-7 (exact in bf16) times w = 1 + 2^-23 is 1 + 2^-7 + 2^-23 +
+    2^-30, whose fp32 rounding drops 2^-30.  Adding -(1 + 2^-7 + 2^-23) as the
+    second product (x = -1, w = 1 + 2^-7 + 2^-23) therefore leaves the exact
+    2^-30 after a fused step, where a separately rounded product would leave 0.
+    The chain runs the small product first so that the large one is the fused
+    step: acc = fma(x1, w1, fma(x0, w0, 0)) = fma(x1, w1, rn(x0 w0))."""
+    x = synth.f32_to_bf16_bits(np.array([[-1.0, 1.0 + 2.0 ** -7]], np.float32))
+    w = np.array([[1.0 + 2.0 ** -7 + 2.0 ** -23, 1.0 + 2.0 ** -23]], np.float32)
+    got = oracle.router_logits(x, w)
+    assert got[0, 0] == np.float32(2.0 ** -30)
 
 
 def _brute_slots(idx, N, cap):
