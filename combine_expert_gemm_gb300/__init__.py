@@ -19,7 +19,7 @@ from .build import LIB
 
 __all__ = ["Shape", "MoEError", "lib", "route", "dispatch", "expert_ffn", "combine",
            "combine_backward", "dispatch_backward", "read_device_error",
-           "route_workspace_bytes", "expert_ffn_workspace_bytes", "capacity", "LayerBuffers",
+           "route_workspace_bytes", "route_logits", "expert_ffn_workspace_bytes", "capacity", "LayerBuffers",
            "layer_forward", "expert_ffn_backward", "expert_ffn_backward_workspace_bytes",
            "BackwardBuffers", "layer_backward", "MxWeights", "MxLayerBuffers", "mx_act_scale_bytes",
            "mx_quantize_weights", "dispatch_mxfp8", "expert_ffn_mxfp8", "combine_mxfp8",
@@ -55,6 +55,7 @@ _SZ = ctypes.c_size_t
 _SIG = {
     "moe_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "moe_route_workspace_bytes": ([_SP], _SZ),
+    "moe_route_logits_offset": ([_SP], _SZ),
     "moe_expert_ffn_workspace_bytes": ([_SP], _SZ),
     "moe_route": ([_SP] + [_P] * 9 + [_P, _SZ, _P], ctypes.c_int),
     "moe_dispatch": ([_SP, _P, _P, _P, _P], ctypes.c_int),
@@ -133,6 +134,16 @@ _bf16, _f32, _i32 = torch.bfloat16, torch.float32, torch.int32
 
 def route_workspace_bytes(shape):
     return int(_lib.moe_route_workspace_bytes(ctypes.byref(shape)))
+
+
+def route_logits(shape, ws):
+    """The router logits [T, N] fp32 that the last moe_route call on the
+    workspace ``ws`` (a uint8 CUDA tensor) left there: a view, not a copy."""
+    off = int(_lib.moe_route_logits_offset(ctypes.byref(shape)))
+    if off == 0:
+        raise MoEError(1, "moe_route_logits_offset")
+    n = shape.T * shape.N * 4
+    return ws[off:off + n].view(torch.float32).view(shape.T, shape.N)
 
 
 def expert_ffn_workspace_bytes(shape):
@@ -300,6 +311,10 @@ class LayerBuffers:
         self.u_save = torch.empty((R, h), dtype=_bf16, **e) if save_for_backward else None
         self.y_disp = torch.empty((R, d), dtype=_bf16, **e)
         self.y = torch.empty((T, d), dtype=_bf16, **e)
+
+    def route_logits(self):
+        """The router logits [T, N] fp32 of the last forward (a view into route_ws)."""
+        return route_logits(self.shape, self.route_ws)
 
 
 def layer_forward(buf, x, w_router, bias, w_gate, w_up, w_down, stream=None, fused_dispatch=False):

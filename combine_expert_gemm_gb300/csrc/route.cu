@@ -8,14 +8,15 @@
 // int32 cumulative offsets produced and kept on the device).  AWS Neuron
 // "Expert Parallelism (EP)", "Router Weights" (logits for every expert).
 //
-// Five launches; no CTA spins on another, and each kernel waits only for the
-// grid before it (programmatic dependent launch):
-//   1. route_logit_blocks: fp32 block sums of the logits (per 512-wide block
-//      of j one fused multiply-add chain over j ascending), one CTA per
-//      (token tile, block, group of 64 experts);
-//   1b. route_topk: the block sums added in block order (+ bias), so the
-//      logits are reproducible bit for bit; then four lanes per token select
-//      the top K and compute the gates.
+// Six launches; no CTA spins on another, and each kernel waits only for the
+// grid before it (programmatic dependent launch, except for route_logits):
+//   1. route_wt_pack: W_r rewritten as groups of experts, transposed, so one
+//      j of a group is contiguous;
+//   1a. route_logits: one fp32 fused multiply-add chain per (token, expert)
+//      over j ascending, + bias, written to the workspace (the logits the
+//      oracle defines, bit for bit);
+//   1b. route_topk: four lanes per token select the top K from the logits
+//      and compute the gates.
 //   2. route_block_rank: per block of 256 tokens, a per-warp bitmask of the
 //      tokens choosing each expert gives every route its rank among earlier
 //      routes to the same expert inside the block, and the block's count per
@@ -41,149 +42,172 @@ __device__ __forceinline__ bool beats(float a, int ia, float b, int ib) {
     return a > b || (a == b && ia < ib);
 }
 
-// Router logits in two launches.
+// Router logits: one fp32 fused multiply-add chain per (token, expert) over
+// j = 0 .. d-1 in order, then + bias[e] -- the dot product summed left to
+// right.  Two launches:
 //
-// route_logit_blocks: the dot product over j is cut into 512-wide blocks (one
-// fp32 chain per block; the block sums are added in block order, the order
-// the logits are defined by).  CTA (token tile, block b, pass z) computes
-// the block sums of 128 tokens x the z-th group of EC experts and writes them
-// to part[b][t][e]; the passes sit in the grid rather than in a loop, so that
-// a layer with many experts gets many short CTAs instead of a second, nearly
-// empty wave of long ones.  4 warps, each 32 tokens x EC experts; lane =
-// tx + 8 ty (tx in 0..7, ty in 0..3) owns tokens ty + 4i (i = 0..7) and
-// experts tx + 8b (b < EPL): 8 EPL chains, advanced two tokens at a time by
-// the packed fp32x2 fma; the j loop over a chunk is unrolled four ways.
-// EPL = 8 (64 experts per pass) when N > 32, else 4: each widened pair of x
-// values then feeds 8 paired fmas instead of 4, which halves the conversion
-// and register-move instructions per fma (they, not memory, bound the loop).
-// x (bf16) and W_r (fp32) stream through a 3-stage cp.async ring of 32-wide
-// j-chunks in their natural layouts (rows padded so that a warp load's
-// distinct rows hit distinct banks).  Splitting j into blocks gives 4 times
-// the warps of a single chain per logit.
+// route_wt_pack: W_r [N][d] is rewritten as expert groups of EG experts,
+// each [d][EG] (transposed, experts past N zero), so that the EG weights of
+// one j are 4*EG contiguous bytes and a chunk of j rows of a group is one
+// contiguous block.
 //
-constexpr int kLogitJC = 32;
-constexpr int kLogitBlock = 512;  // j per block sum (a multiple of kLogitJC)
-constexpr int kLogitStages = 3;
-constexpr int kLogitThreads = 128;
-constexpr int kLogitXR = kLogitJC + 8;  // bf16 per padded x row
-constexpr int kLogitWR = kLogitJC + 4;  // fp32 per padded W row
+// route_logits: CTA (token tile, expert group) runs TT tokens x EG experts
+// over all of d.  x (bf16, natural layout) and the group's W chunk stream
+// through a cp.async ring of JC-wide j-chunks.  Lane (lt, le) of a warp owns
+// tokens lt + LT*i (i < TPT) and experts 4*le + 4*LE*q + {0..3} (q < EPT/4):
+// TPT*EPT chains, advanced two tokens at a time by the packed fp32x2 fma
+// (tokens 2p and 2p+1 of the lane share one expert weight).  What bounds the
+// loop is the shared-memory data path (every 16-byte load delivers 512 bytes
+// to a warp's registers, broadcast or not), so x stays bf16 there -- each
+// 16-byte load brings 8 j of one token, widened in registers -- and each
+// value loaded feeds TPT or EPT fmas.  The chains of one logit never leave
+// their thread and take j in order, so every chain is the oracle's chain.
+constexpr int kLogitJC = 32;      // j per chunk
+constexpr int kLogitStages = 3;   // cp.async ring depth
 
-// WE warps along the experts, 4 / WE along the tokens; EPL experts per lane:
-// 128 tokens x 64 experts per pass (EPL = 8), or 128 x 32 (EPL = 4) for
-// N <= 32
-template <int WE, int EPL = 4>
-struct LogitTile {
-    static constexpr int WT = 4 / WE;
-    static constexpr int TB = 32 * WT;
-    static constexpr int EC = 8 * EPL * WE;
-    static constexpr int STAGE = TB * kLogitXR * 2 + EC * kLogitWR * 4;
+template <int TPT_, int EPT_, int LE_, int NW_>
+struct LogitCfg {
+    static constexpr int TPT = TPT_, EPT = EPT_, LE = LE_, NW = NW_;
+    static constexpr int LT = 32 / LE;
+    static constexpr int EG = LE * EPT;               // experts per CTA
+    static constexpr int TW = LT * TPT;               // tokens per warp
+    static constexpr int TT = TW * NW;                // tokens per CTA
+    static constexpr int NT = 32 * NW;
+    static constexpr int XR = kLogitJC * 2 + 16;      // bytes per staged x row (padded)
+    static constexpr int XS = TT * XR;
+    static constexpr int WS = kLogitJC * EG * 4;
+    static constexpr int STAGE = XS + WS;
     static constexpr size_t SMEM = (size_t)kLogitStages * STAGE;
+    static_assert(EPT % 4 == 0 && TPT % 2 == 0 && 32 % LE == 0, "lane tile");
+    static_assert(LT <= 8, "x rows of a warp load must fall on distinct bank groups");
 };
 
-inline int logit_blocks(int d) { return (d + kLogitBlock - 1) / kLogitBlock; }
+// Tiles.  With 8 x 8 chains per lane each value a lane loads feeds 8 fmas
+// (about 0.75 bytes of shared-memory traffic per fma, inside the data path's
+// budget at the fma peak), but a layer with few logits then has too few warps
+// to hide latency: below 2^20 logits the 4 x 4 tile (16 chains per lane, 4
+// times the warps) is faster although each value feeds only 4 fmas.
+using LogitWide = LogitCfg<8, 8, 8, 2>;    // 64 tokens x 64 experts per CTA, N > 32
+using LogitNarrow = LogitCfg<8, 8, 4, 2>;  // 128 tokens x 32 experts per CTA, N <= 32
+using LogitSmall = LogitCfg<4, 4, 8, 4>;   // 64 tokens x 32 experts per CTA
+constexpr int64_t kLogitBigTile = (int64_t)1 << 20;  // T * N from which the 8 x 8 tiles run
 
-template <int WE, int EPL>
-__global__ void __launch_bounds__(kLogitThreads)
-route_logit_blocks(int T, int d, int N, const uint16_t *__restrict__ x,
-                   const float *__restrict__ w_r, float *__restrict__ part) {
+template <int EG>
+__global__ void __launch_bounds__(256)
+route_wt_pack(int d, int N, const float *__restrict__ w_r, float *__restrict__ wt) {
     pdl_enter();
-    using L = LogitTile<WE, EPL>;
-    constexpr int JC = kLogitJC, XR = kLogitXR, WR = kLogitWR, TB = L::TB, EC = L::EC;
-    constexpr int kLogitStage = L::STAGE;
+    __shared__ float tile[32][EG + 1];
+    const int g = blockIdx.y, j0 = blockIdx.x * 32;
+    for (int i = threadIdx.x; i < EG * 32; i += 256) {
+        const int e = i / 32, j = i % 32, ex = g * EG + e;
+        tile[j][e] = (ex < N && j0 + j < d) ? w_r[(int64_t)ex * d + j0 + j] : 0.0f;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < EG * 32; i += 256) {
+        const int j = i / EG, e = i % EG;
+        if (j0 + j < d) wt[((int64_t)g * d + j0 + j) * EG + e] = tile[j][e];
+    }
+}
+
+template <class C>
+__global__ void __launch_bounds__(C::NT)
+route_logits(int T, int d, int N, const uint16_t *__restrict__ x, const float *__restrict__ wt,
+             const float *__restrict__ bias, float *__restrict__ logits) {
+    pdl_enter();
+    constexpr int JC = kLogitJC, EG = C::EG, TT = C::TT, NT = C::NT, XR = C::XR;
+    constexpr int TPT = C::TPT, EPT = C::EPT;
     extern __shared__ __align__(16) uint8_t smem_l[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int tx = lane & 7, ty = lane >> 3;
-    const int tok0 = (warp % L::WT) * 32 + ty;   // + 4i
-    const int exp0 = (warp / L::WT) * (8 * EPL) + tx;   // + 8b
-    const int t0 = blockIdx.x * TB;
-    const int b = blockIdx.y;
-    const int jb0 = b * kLogitBlock, jlen = min(kLogitBlock, d - jb0);  // a multiple of 8
-    const int nchunks = (jlen + JC - 1) / JC;
-    float *pb = part + (size_t)b * T * N;
+    const int le = lane % C::LE, lt = lane / C::LE;
+    const int t0 = blockIdx.x * TT, g = blockIdx.y;
+    const float *wg = wt + (int64_t)g * d * EG;
+    const int nchunks = (d + JC - 1) / JC;
 
-    for (int ec0 = blockIdx.z * EC; ec0 < N; ec0 += EC * (int)gridDim.z) {
-        auto issue = [&](int c) {
-            if (c < nchunks) {
-                uint8_t *st = smem_l + (size_t)(c % kLogitStages) * kLogitStage;
-                uint16_t *xs = reinterpret_cast<uint16_t *>(st);
-                float *ws = reinterpret_cast<float *>(st + TB * XR * 2);
-                const int j0 = jb0 + c * JC, jn = min(JC, jlen - c * JC);
-                for (int i = tid; i < TB * (JC / 8); i += kLogitThreads) {
-                    const int r = i / (JC / 8), q = (i % (JC / 8)) * 8;
-                    if (t0 + r < T && q < jn)
-                        cp_async16(xs + r * XR + q, x + (int64_t)(t0 + r) * d + j0 + q);
-                }
-                for (int i = tid; i < EC * (JC / 4); i += kLogitThreads) {
-                    const int r = i / (JC / 4), q = (i % (JC / 4)) * 4;
-                    if (ec0 + r < N && q < jn)
-                        cp_async16(ws + r * WR + q, w_r + (int64_t)(ec0 + r) * d + j0 + q);
-                }
+    auto issue = [&](int c) {
+        if (c < nchunks) {
+            uint8_t *st = smem_l + (c % kLogitStages) * C::STAGE;
+            const int j0 = c * JC, jn = min(JC, d - j0);  // a multiple of 8
+            for (int i = tid; i < TT * (JC / 8); i += NT) {
+                const int r = i / (JC / 8), q = (i % (JC / 8)) * 8;
+                if (t0 + r < T && q < jn)
+                    cp_async16(st + r * XR + q * 2, x + (int64_t)(t0 + r) * d + j0 + q);
             }
-            cp_async_commit();
-        };
+            float *ws = reinterpret_cast<float *>(st + C::XS);
+            const float *src = wg + (int64_t)j0 * EG;
+            for (int i = tid; i < jn * EG / 4; i += NT) cp_async16(ws + 4 * i, src + 4 * i);
+        }
+        cp_async_commit();
+    };
 
-        // acc[p][e]: chains (token tok0 + 8p, expert e) and (token tok0 + 8p + 4,
-        // expert e) of this lane, e = exp0 + 8 * (0..3)
-        float2 acc[4][EPL];
+    // acc[p][e]: (token lt + LT*2p, token lt + LT*(2p+1)) x expert e of the lane
+    float2 acc[TPT / 2][EPT];
 #pragma unroll
-        for (int p = 0; p < 4; ++p)
+    for (int p = 0; p < TPT / 2; ++p)
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) acc[p][e] = make_float2(0.0f, 0.0f);
+        for (int e = 0; e < EPT; ++e) acc[p][e] = make_float2(0.0f, 0.0f);
 
-        __syncthreads();  // the previous pass is done with every stage
 #pragma unroll
-        for (int c = 0; c < kLogitStages - 1; ++c) issue(c);
-        for (int c = 0; c < nchunks; ++c) {
-            cp_async_wait<kLogitStages - 2>();
-            __syncthreads();
-            issue(c + kLogitStages - 1);
-            const uint8_t *st = smem_l + (size_t)(c % kLogitStages) * kLogitStage;
-            const uint16_t *xs = reinterpret_cast<const uint16_t *>(st) + tok0 * XR;
-            const float *ws = reinterpret_cast<const float *>(st + TB * XR * 2) + exp0 * WR;
-            const int jn = min(JC, jlen - c * JC);  // a multiple of 8
-#pragma unroll 4
-            for (int j = 0; j < jn; j += 4) {
-                uint2 xv[8];  // tokens tok0 + 4i, 4 bf16 at j .. j + 3
+    for (int c = 0; c < kLogitStages - 1; ++c) issue(c);
+    for (int c = 0; c < nchunks; ++c) {
+        cp_async_wait<kLogitStages - 2>();
+        __syncthreads();  // chunk c has landed; every thread is done with chunk c - 1
+        issue(c + kLogitStages - 1);
+        const uint8_t *st = smem_l + (c % kLogitStages) * C::STAGE;
+        const uint8_t *xs = st + (warp * C::TW + lt) * XR;
+        const float *ws = reinterpret_cast<const float *>(st + C::XS) + 4 * le;
+        const int jn = min(JC, d - c * JC);
+        for (int j = 0; j < jn; j += 8) {
+            uint4 xv[TPT];  // tokens lt + LT*i, bf16 at j .. j + 7
 #pragma unroll
-                for (int i = 0; i < 8; ++i) xv[i] = *reinterpret_cast<const uint2 *>(xs + 4 * i * XR + j);
-                float4 wv[EPL];
+            for (int i = 0; i < TPT; ++i)
+                xv[i] = *reinterpret_cast<const uint4 *>(xs + i * C::LT * XR + j * 2);
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) wv[e] = *reinterpret_cast<const float4 *>(ws + 8 * e * WR + j);
+            for (int jj = 0; jj < 8; ++jj) {
+                float4 wv[EPT / 4];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
+                for (int q = 0; q < EPT / 4; ++q)
+                    wv[q] = *reinterpret_cast<const float4 *>(ws + (j + jj) * EG + 4 * C::LE * q);
 #pragma unroll
-                    for (int p = 0; p < 4; ++p) {
-                        const uint32_t a = (q < 2) ? xv[2 * p].x : xv[2 * p].y;
-                        const uint32_t bb = (q < 2) ? xv[2 * p + 1].x : xv[2 * p + 1].y;
-                        const float2 xp = (q & 1) ? make_float2(bf16_hi(a), bf16_hi(bb))
-                                                  : make_float2(bf16_lo(a), bf16_lo(bb));
+                for (int p = 0; p < TPT / 2; ++p) {
+                    const uint4 &a = xv[2 * p], &b = xv[2 * p + 1];
+                    const uint32_t wa = jj < 2 ? a.x : jj < 4 ? a.y : jj < 6 ? a.z : a.w;
+                    const uint32_t wb = jj < 2 ? b.x : jj < 4 ? b.y : jj < 6 ? b.z : b.w;
+                    const float2 xp = (jj & 1) ? make_float2(bf16_hi(wa), bf16_hi(wb))
+                                               : make_float2(bf16_lo(wa), bf16_lo(wb));
 #pragma unroll
-                        for (int e = 0; e < EPL; ++e) {
-                            const float w = q == 0 ? wv[e].x : q == 1 ? wv[e].y : q == 2 ? wv[e].z : wv[e].w;
-                            acc[p][e] = __ffma2_rn(xp, make_float2(w, w), acc[p][e]);
-                        }
+                    for (int q = 0; q < EPT / 4; ++q) {
+                        const float w4[4] = {wv[q].x, wv[q].y, wv[q].z, wv[q].w};
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            acc[p][4 * q + u] =
+                                __ffma2_rn(xp, make_float2(w4[u], w4[u]), acc[p][4 * q + u]);
                     }
                 }
             }
         }
-        cp_async_wait<0>();
+    }
+    cp_async_wait<0>();
 #pragma unroll
-        for (int p = 0; p < 4; ++p) {
-            const int ta = t0 + tok0 + 8 * p, tb = ta + 4;
+    for (int p = 0; p < TPT / 2; ++p) {
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) {
-                const int ex = ec0 + exp0 + 8 * e;
-                if (ex >= N) continue;
-                if (ta < T) pb[(int64_t)ta * N + ex] = acc[p][e].x;
-                if (tb < T) pb[(int64_t)tb * N + ex] = acc[p][e].y;
-            }
+        for (int h = 0; h < 2; ++h) {
+            const int t = t0 + warp * C::TW + lt + C::LT * (2 * p + h);
+            if (t >= T) continue;
+            float *out = logits + (int64_t)t * N;
+#pragma unroll
+            for (int q = 0; q < EPT / 4; ++q)
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int e = g * EG + 4 * le + 4 * C::LE * q + u;
+                    const float v = h ? acc[p][4 * q + u].y : acc[p][4 * q + u].x;
+                    if (e < N) out[e] = bias ? __fadd_rn(v, bias[e]) : v;
+                }
         }
     }
 }
 
 constexpr int kTopkTB = 8;      // tokens per CTA (one warp)
-constexpr int kTopkPlanes = 4;  // block-sum planes loaded before any is added
-constexpr int kTopkGroups = 4;  // float4 groups per lane loaded before any is added
+constexpr int kTopkGroups = 8;  // float4 groups per lane loaded before any is stored
 
 // Shared-memory row stride of the logits: at least N + 1 and 4 mod 32, so the
 // 32 lanes of a selecting warp (8 tokens x 4 lanes, lane s reading expert
@@ -261,23 +285,21 @@ __device__ __forceinline__ void topk_merge(float (&tv)[M], int (&ti)[M], int mas
 }
 
 // route_topk: one CTA of one warp per 8 tokens (many small CTAs spread evenly
-// over the SMs).  The block sums of the tile are contiguous in each block's
-// [T][N] plane; every lane loads kTopkGroups float4 groups from kTopkPlanes
-// planes before adding any of them (one memory round trip for d <= 2048),
-// then adds them in block order (+ bias) into shared memory.  Selection: 4 lanes per token, lane
-// s keeping the best MAXK of experts s, s + 4, s + 8, ... (logit descending,
-// lower expert first on ties, NaN as -inf; unfilled entries are -inf with an
-// index past every expert, so any expert beats them).  The lane takes its
-// experts MAXK at a time, sorts them with a bitonic network and merges them
-// into its list, so no step waits on a data-dependent branch; two merges over
-// lane shuffles then give all four lanes the best MAXK of the token, whose
-// first K are the top K.  The order is strict and total, so the result does not depend on
-// how the experts were split.  Gates: softmax over the K, shifted by the
-// largest, summed over k ascending.
+// over the SMs).  The tile's logits are contiguous; every lane loads
+// kTopkGroups float4 groups before storing any to shared memory (one memory
+// round trip for N <= 128).  Selection: 4 lanes per token, lane s keeping
+// the best MAXK of experts s, s + 4, s + 8, ... (logit descending, lower
+// expert first on ties, NaN as -inf; unfilled entries are -inf with an index
+// past every expert, so any expert beats them).  The lane takes its experts
+// MAXK at a time, sorts them with a bitonic network and merges them into its
+// list, so no step waits on a data-dependent branch; two merges over lane
+// shuffles then give all four lanes the best MAXK of the token, whose first K
+// are the top K.  The order is strict and total, so the result does not
+// depend on how the experts were split.  Gates: softmax over the K, shifted
+// by the largest, summed over k ascending.
 template <int MAXK>
 __global__ void __launch_bounds__(32)
-route_topk(int T, int N, int K, int nb, const float *__restrict__ part,
-           const float *__restrict__ bias, int32_t *__restrict__ topk_idx,
+route_topk(int T, int N, int K, const float *__restrict__ logits, int32_t *__restrict__ topk_idx,
            float *__restrict__ topk_gate) {
     pdl_enter();
     extern __shared__ __align__(16) uint8_t smem_t[];
@@ -287,54 +309,30 @@ route_topk(int T, int N, int K, int nb, const float *__restrict__ part,
     const int t0 = blockIdx.x * kTopkTB;
     const int tn = min(kTopkTB, T - t0);
     const int64_t tile = (int64_t)t0 * N, n = (int64_t)tn * N;
-    const int64_t plane = (int64_t)T * N;
     if ((N & 3) == 0) {
-        // kTopkGroups groups x kTopkPlanes planes in flight per lane
         for (int64_t g0 = tid; g0 < n / 4; g0 += kTopkGroups * blockDim.x) {
-            float4 v[kTopkGroups][kTopkPlanes];
+            float4 v[kTopkGroups];
 #pragma unroll
             for (int u = 0; u < kTopkGroups; ++u) {
                 const int64_t g = g0 + u * blockDim.x;
-#pragma unroll
-                for (int c = 0; c < kTopkPlanes; ++c)
-                    if (g < n / 4 && c < nb)
-                        v[u][c] = __ldcs(reinterpret_cast<const float4 *>(part + c * plane + tile) + g);
+                if (g < n / 4) v[u] = __ldcs(reinterpret_cast<const float4 *>(logits + tile) + g);
             }
 #pragma unroll
             for (int u = 0; u < kTopkGroups; ++u) {
                 const int64_t g = g0 + u * blockDim.x;
                 if (g >= n / 4) continue;
-                float4 a = v[u][0];
-#pragma unroll
-                for (int c = 1; c < kTopkPlanes; ++c) {
-                    if (c >= nb) break;
-                    a.x = __fadd_rn(a.x, v[u][c].x);
-                    a.y = __fadd_rn(a.y, v[u][c].y);
-                    a.z = __fadd_rn(a.z, v[u][c].z);
-                    a.w = __fadd_rn(a.w, v[u][c].w);
-                }
-                for (int c = kTopkPlanes; c < nb; ++c) {  // d > 2048
-                    const float4 w = __ldcs(reinterpret_cast<const float4 *>(part + c * plane + tile) + g);
-                    a.x = __fadd_rn(a.x, w.x);
-                    a.y = __fadd_rn(a.y, w.y);
-                    a.z = __fadd_rn(a.z, w.z);
-                    a.w = __fadd_rn(a.w, w.w);
-                }
-                const float vv[4] = {a.x, a.y, a.z, a.w};
+                const float vv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
                 for (int h = 0; h < 4; ++h) {
                     const int i = (int)(4 * g + h), tt = i / N, e = i - tt * N;
-                    lg[tt * LDS + e] = bias ? __fadd_rn(vv[h], bias[e]) : vv[h];
+                    lg[tt * LDS + e] = vv[h];
                 }
             }
         }
     } else {
         for (int i = tid; i < n; i += blockDim.x) {
             const int tt = i / N, e = i - tt * N;
-            float v = part[tile + i];
-            for (int b = 1; b < nb; ++b) v = __fadd_rn(v, part[b * plane + tile + i]);
-            if (bias) v = __fadd_rn(v, bias[e]);
-            lg[tt * LDS + e] = v;
+            lg[tt * LDS + e] = logits[tile + i];
         }
     }
     __syncthreads();
@@ -541,35 +539,53 @@ __global__ void route_assign(int T, int N, int K, int cap, const int32_t *__rest
     route_row[i] = slot < cap ? expert_offset[e] + slot : -1;
 }
 
+// Experts per group of the packed router weight (the tile's EG).
+inline int logit_group(const moe_shape *s) {
+    if ((int64_t)s->T * s->N < kLogitBigTile) return LogitSmall::EG;
+    return s->N > 32 ? LogitWide::EG : LogitNarrow::EG;
+}
+
+// route_logits is one wave of CTAs, placed all at once when the grid starts.
+// It is launched in plain stream order, not early beside the grid before it
+// (programmatic dependent launch): CTAs placed while the SMs still hold
+// another grid's CTAs pile onto the free SMs, and the kernel then runs at the
+// pace of its most crowded SM (measured 2 to 3 times slower).
+template <class C>
+moe_status launch_logits_cfg(const moe_shape *s, const uint16_t *x, const float *w,
+                             const float *b, float *logits, float *wt, cudaStream_t st) {
+    const int G = (s->N + C::EG - 1) / C::EG;
+    launch_pdl(route_wt_pack<C::EG>, dim3((s->d + 31) / 32, G), 256, 0, st, s->d, s->N, w, wt);
+    moe_status r = launch_status();
+    if (r != MOE_OK) return r;
+    route_logits<C><<<dim3((s->T + C::TT - 1) / C::TT, G), C::NT, C::SMEM, st>>>(s->T, s->d, s->N,
+                                                                             x, wt, b, logits);
+    return launch_status();
+}
+
 moe_status launch_logits(const moe_shape *s, const uint16_t *x, const float *w, const float *b,
-                         int32_t *idx, float *gate, float *part, cudaStream_t st) {
+                         int32_t *idx, float *gate, float *logits, float *wt, cudaStream_t st) {
     static PerDeviceOnce smem_attr;
     if (!device_once(smem_attr, [] {
             const size_t topk_smem = sizeof(float) * kTopkTB * topk_row_stride(kMaxN);
-            return set_smem_limit(route_logit_blocks<1, 4>, LogitTile<1, 4>::SMEM) &&
-                   set_smem_limit(route_logit_blocks<1, 8>, LogitTile<1, 8>::SMEM) &&
+            return set_smem_limit(route_logits<LogitWide>, LogitWide::SMEM) &&
+                   set_smem_limit(route_logits<LogitNarrow>, LogitNarrow::SMEM) &&
+                   set_smem_limit(route_logits<LogitSmall>, LogitSmall::SMEM) &&
                    set_smem_limit(route_topk<8>, topk_smem) &&
                    set_smem_limit(route_topk<kMaxK>, topk_smem);
         }))
         return MOE_ERR_CUDA;
-    const int nb = logit_blocks(s->d);
-    if (s->N <= 32) {
-        const dim3 grid((s->T + LogitTile<1, 4>::TB - 1) / LogitTile<1, 4>::TB, nb,
-                        (s->N + LogitTile<1, 4>::EC - 1) / LogitTile<1, 4>::EC);
-        launch_pdl(route_logit_blocks<1, 4>, grid, kLogitThreads, LogitTile<1, 4>::SMEM, st, s->T,
-                   s->d, s->N, x, w, part);
-    } else {
-        const dim3 grid((s->T + LogitTile<1, 8>::TB - 1) / LogitTile<1, 8>::TB, nb,
-                        (s->N + LogitTile<1, 8>::EC - 1) / LogitTile<1, 8>::EC);
-        launch_pdl(route_logit_blocks<1, 8>, grid, kLogitThreads, LogitTile<1, 8>::SMEM, st, s->T,
-                   s->d, s->N, x, w, part);
-    }
-    moe_status r = launch_status();
+    moe_status r;
+    if ((int64_t)s->T * s->N < kLogitBigTile)
+        r = launch_logits_cfg<LogitSmall>(s, x, w, b, logits, wt, st);
+    else if (s->N > 32)
+        r = launch_logits_cfg<LogitWide>(s, x, w, b, logits, wt, st);
+    else
+        r = launch_logits_cfg<LogitNarrow>(s, x, w, b, logits, wt, st);
     if (r != MOE_OK) return r;
     const size_t tsmem = sizeof(float) * kTopkTB * topk_row_stride(s->N);
     auto *topk = s->K <= 8 ? route_topk<8> : route_topk<kMaxK>;
-    launch_pdl(topk, (s->T + kTopkTB - 1) / kTopkTB, 32, tsmem, st, s->T, s->N, s->K, nb, part, b,
-               idx, gate);
+    launch_pdl(topk, (s->T + kTopkTB - 1) / kTopkTB, 32, tsmem, st, s->T, s->N, s->K, logits, idx,
+               gate);
     return launch_status();
 }
 
@@ -580,11 +596,18 @@ inline size_t route_block_count_bytes(const moe_shape *s) {
     return (nblk * (size_t)s->N * sizeof(int32_t) + 255) & ~(size_t)255;
 }
 
-// status word (256 B), the per-block count array, then the logit block sums
-// [ceil(d / 512)][T][N] fp32
+inline size_t round256(size_t n) { return (n + 255) & ~(size_t)255; }
+
+inline size_t route_logits_bytes(const moe_shape *s) {
+    return round256((size_t)s->T * s->N * sizeof(float));
+}
+
+// status word (256 B), the per-block count array, the logits [T][N] fp32,
+// then W_r packed by expert groups [ceil(N / EG)][d][EG] fp32
 size_t route_ws_bytes(const moe_shape *s) {
-    const size_t part = (size_t)logit_blocks(s->d) * s->T * s->N * sizeof(float);
-    return 256 + route_block_count_bytes(s) + ((part + 255) & ~(size_t)255);
+    const int eg = logit_group(s);
+    const size_t wt = (size_t)((s->N + eg - 1) / eg) * s->d * eg * sizeof(float);
+    return 256 + route_block_count_bytes(s) + route_logits_bytes(s) + round256(wt);
 }
 
 // Enqueues the routing kernels; `scratch` is the workspace past its status
@@ -595,10 +618,12 @@ moe_status route_enqueue(const moe_shape *s, const moe_bf16 *x, const float *w_r
                          int32_t *expert_demand, void *scratch, cudaStream_t st) {
     const int nblk = (s->T + kRankBlock - 1) / kRankBlock;
     int32_t *block_count = static_cast<int32_t *>(scratch);
-    float *part = reinterpret_cast<float *>(static_cast<char *>(scratch) + route_block_count_bytes(s));
+    char *after_counts = static_cast<char *>(scratch) + route_block_count_bytes(s);
+    float *logits = reinterpret_cast<float *>(after_counts);
+    float *wt = reinterpret_cast<float *>(after_counts + route_logits_bytes(s));
     moe_status r = MOE_OK;
     if (s->T > 0) {
-        r = launch_logits(s, x, w_router, bias, topk_idx, topk_gate, part, st);
+        r = launch_logits(s, x, w_router, bias, topk_idx, topk_gate, logits, wt, st);
         if (r != MOE_OK) return r;
         const size_t smem = sizeof(uint32_t) * 2 * (kRankBlock / 32) * (size_t)s->N;
         static PerDeviceOnce smem_attr;
@@ -633,6 +658,11 @@ MOE_API size_t moe_route_workspace_bytes(const moe_shape *s) {
     return route_ws_bytes(s);
 }
 
+MOE_API size_t moe_route_logits_offset(const moe_shape *s) {
+    if (check_shape(s) != MOE_OK) return 0;
+    return 256 + route_block_count_bytes(s);
+}
+
 MOE_API moe_status moe_route(const moe_shape *s, const moe_bf16 *x, const float *w_router,
                              const float *bias, int32_t *topk_idx, float *topk_gate,
                              int32_t *route_row, int32_t *expert_count, int32_t *expert_offset,
@@ -656,8 +686,10 @@ MOE_API moe_status moe_route(const moe_shape *s, const moe_bf16 *x, const float 
 // ------------------------------------------------------------------------
 // moe_route_noalloc: moe_route for callers that cannot allocate device memory.
 //
-// Its scratch (the device status word and the per-block count array) lives in
-// the fixed array below instead of a caller-provided workspace.  Every GPU
+// Its scratch -- the 256-byte status word (unused by routing), the per-block
+// counts, the fp32 logits [T][N] and the router weight regrouped by experts,
+// laid out as in moe_route's workspace -- lives in the fixed array below
+// instead of a caller-provided workspace.  Every GPU
 // that loads this library holds the array until the process exits.  In host
 // code `route_noalloc_scratch` names a host-side stand-in, not a device
 // address, so the address each kernel gets is looked up once per device with

@@ -87,6 +87,12 @@ const char *moe_status_string(moe_status s);
 /* Bytes of workspace moe_route needs for this shape (0 if the shape is invalid). */
 size_t moe_route_workspace_bytes(const moe_shape *s);
 
+/* Byte offset, inside the moe_route workspace, of the router logits [T, N]
+ * fp32 (row-major, bias included) that moe_route leaves there; a multiple of
+ * 256.  0 if the shape is invalid (the logits never start at 0: word 0 is the
+ * status word). */
+size_t moe_route_logits_offset(const moe_shape *s);
+
 /*
  * moe_route -- steps R0-R3: router logits, top-K, gates, slots, route map.
  * Report: Neuron "Router Weights" (logits over all N experts); Section 05
@@ -110,10 +116,13 @@ size_t moe_route_workspace_bytes(const moe_shape *s);
  *                capacity decision); dropped = sum(demand - count).
  *   ws, ws_bytes device workspace of at least moe_route_workspace_bytes(s)
  *                bytes, 256-byte aligned; word 0 is the device status word.
- * Logits are fp32: per 512-wide block of j one fused multiply-add chain over
- * j ascending, the block sums added in block order, then + bias (the pages
- * fix no order; this one is fixed, so top-K decisions are reproducible bit for
- * bit).
+ * Logits are fp32: one fused multiply-add chain per (token, expert) from 0
+ * over j = 0 .. d-1 in order (the dot product summed left to right), then
+ * + bias[e] as one fp32 addition.  The pages fix no order; this one is the
+ * plain reading, and it makes the logits, and with them every top-K
+ * decision, reproducible bit for bit.  The call leaves the logits [T, N] fp32
+ * in the workspace at byte moe_route_logits_offset(s), where they stay until
+ * the workspace is used again.
  */
 moe_status moe_route(const moe_shape *s, const moe_bf16 *x, const float *w_router,
                      const float *bias, int32_t *topk_idx, float *topk_gate, int32_t *route_row,
@@ -133,17 +142,20 @@ moe_status moe_route(const moe_shape *s, const moe_bf16 *x, const float *w_route
  * MOE_ROUTE_NOALLOC_SCRATCH_BYTES (64 MiB) inside this library; every GPU that
  * loads the library holds that array until the process exits.  The call
  * allocates nothing.  Shapes whose scratch (moe_route_workspace_bytes: the
- * per-block counts, 4 * ceil(T / 256) * N bytes, and the logit block sums,
- * 4 * ceil(d / 512) * T * N bytes) would exceed the array -- roughly
- * ceil(d / 512) * T * N > 16.7 million -- are rejected with
- * MOE_ERR_UNSUPPORTED before anything is enqueued.
+ * 256-byte status word, the per-block counts, 4 * ceil(T / 256) * N bytes,
+ * the logits, 4 * T * N bytes, and the router weight regrouped by experts,
+ * 4 * d * N bytes rounded up to whole groups of 32 or 64 experts) would
+ * exceed the array -- roughly T * N + d * N > 16.7 million -- are rejected
+ * with MOE_ERR_UNSUPPORTED before anything is enqueued.
  *
  * The first call on a device looks up the array's device address there
  * (cudaGetSymbolAddress, with that device current); make that first call
  * before any stream capture.  All calls on one device share the array, which
  * keeps the previous call's contents; nothing in it needs clearing.  Calls
  * that overlap on the GPU (e.g. on two streams at once) race on the array.
- * Device-side errors cannot be read back through moe_read_device_error here.
+ * Routing records no device-side error (its kernels have no waits and no
+ * data-dependent addresses outside the checked shape), in moe_route or here,
+ * so there is no status to read back.
  */
 #define MOE_ROUTE_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 moe_status moe_route_noalloc(const moe_shape *s, const moe_bf16 *x, const float *w_router,

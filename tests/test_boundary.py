@@ -74,6 +74,21 @@ def test_buffer_rows_is_the_smaller_bound(moe):
             assert s.R == rows
 
 
+def test_route_logits_offset_lies_inside_the_workspace(moe):
+    """The logits [T, N] fp32 sit 256-aligned past the status word and the
+    per-block counts, and end inside moe_route_workspace_bytes."""
+    lib = moe.lib()
+    for kw in [dict(), dict(T=1000, N=64, K=8), dict(T=257, d=136, N=33, K=5), dict(T=0),
+               dict(T=300, N=1024, K=16, d=64)]:
+        s = _shape(moe, **kw)
+        off = lib.moe_route_logits_offset(ctypes.byref(s))
+        nblk = (s.T + 255) // 256
+        assert off == 256 + ((4 * nblk * s.N + 255) // 256) * 256, kw
+        assert off % 256 == 0
+        assert off + 4 * s.T * s.N <= lib.moe_route_workspace_bytes(ctypes.byref(s)), kw
+    assert lib.moe_route_logits_offset(ctypes.byref(_shape(moe, K=0))) == 0
+
+
 def test_router_backward_argument_errors(moe):
     s = _shape(moe)
     lib = moe.lib()

@@ -1,6 +1,7 @@
 """GPU path versus the CPU oracle, through the C ABI.
 
-Bit-exact: top-K indices, route map, counts, offsets, demand, dispatched rows,
+Bit-exact: router logits, top-K indices, route map, counts, offsets, demand,
+dispatched rows,
 and the movement kernels given identical inputs (combine, combine backward
 payload, dispatch backward).  Within tolerance (rel 2e-2 / abs 1e-2, plus the
 same bound with the absolute term scaled to the data): gates (rel 1e-5),
@@ -36,7 +37,7 @@ SMALL = {
     "cap0": MoEConfig("cap0", T=100, d=64, N=8, K=2, h=64, cf_num=0, cf_den=1, seed=16),
     "N1024": MoEConfig("N1024", T=300, d=64, N=1024, K=16, h=64, cf_num=1, cf_den=1, seed=17),
     "N200": MoEConfig("N200", T=600, d=192, N=200, K=6, h=64, cf_num=2, cf_den=1, seed=18),
-    # three 512-wide logit blocks, the last one ragged (64 wide)
+    # 34 chunks of 32 j in each logit chain, the last one ragged (16 wide)
     "multi_block": MoEConfig("multi_block", T=333, d=1088, N=24, K=3, h=128, cf_num=5, cf_den=4,
                              seed=19),
 }
@@ -77,7 +78,21 @@ def _run_chain(moe, cfg, x, wr, bias, wg, wu, wd, save=False, poison=True):
     return buf
 
 
+def assert_same_f32(got, want, what):
+    """Bit-for-bit equality of fp32 arrays; NaN matches any NaN (the CPU and
+    the GPU may carry different NaN payloads)."""
+    g = np.ascontiguousarray(got, dtype=np.float32)
+    w = np.ascontiguousarray(want, dtype=np.float32)
+    assert g.shape == w.shape, what
+    both_nan = np.isnan(g) & np.isnan(w)
+    diff = (g.view(np.uint32) != w.view(np.uint32)) & ~both_nan
+    assert not diff.any(), (f"{what}: {int(diff.sum())} of {g.size} differ, first at "
+                            f"{np.argwhere(diff)[0].tolist()}")
+
+
 def _check_route(buf, ref):
+    logits = buf.route_logits().cpu().numpy()
+    assert_same_f32(logits, ref["logits"], "router logits")
     np.testing.assert_array_equal(buf.topk_idx.cpu().numpy(), ref["topk_idx"])
     np.testing.assert_array_equal(buf.route_row.cpu().numpy(), ref["route_row"])
     np.testing.assert_array_equal(buf.expert_count.cpu().numpy(), ref["expert_count"])
@@ -110,6 +125,62 @@ def test_layer_parity_small(moe, name):
         assert (ref["route_row"] < 0).any()
     if name == "cap0":
         assert np.all(bits(buf.y) == 0)
+
+
+def _route_only(moe, cfg, x, wr, bias):
+    """moe_route alone into fresh buffers (the experts' shape limits do not apply)."""
+    s = _shape(moe, cfg)
+    buf = moe.LayerBuffers(s, DEV)
+    moe.route(s, bf(x), f32(wr), None if bias is None else f32(bias), buf.topk_idx, buf.topk_gate,
+              buf.route_row, buf.expert_count, buf.expert_offset, buf.expert_demand, buf.route_ws)
+    return s, buf
+
+
+@pytest.mark.parametrize("T,d,N,K,cf", [(300, 136, 16, 4, (5, 4)), (257, 200, 40, 3, (1, 1)),
+                                        (70, 72, 8, 2, (3, 2)), (129, 8, 33, 5, (1, 1)),
+                                        # 2^20 logits and more: the 8 x 8 lane tiles, ragged
+                                        (16411, 200, 64, 4, (1, 1)), (33001, 72, 32, 2, (5, 4))])
+def test_route_dispatch_combine_any_d(moe, T, d, N, K, cf):
+    """Routing, dispatch and combine accept any d that is a multiple of 8: the
+    logit chains end inside a chunk of j and the row kernels on a partial
+    vector group.  Logits, route map and dispatched rows are bit-exact; the
+    combine of the dispatched rows (identity experts) is bit-exact too."""
+    cfg = MoEConfig("any_d", T=T, d=d, N=N, K=K, h=64, cf_num=cf[0], cf_den=cf[1], seed=T + d)
+    x, wr = synth.gen_x(cfg), synth.gen_router(cfg)
+    ref = oracle.route(x, wr, None, K, cfg.cap)
+    s, buf = _route_only(moe, cfg, x, wr, None)
+    buf.x_disp.view(torch.int16).fill_(SENT)
+    moe.dispatch(s, bf(x), buf.route_row, buf.x_disp)
+    moe.combine(s, buf.x_disp, buf.route_row, buf.topk_gate, buf.y)
+    torch.cuda.synchronize()
+    _check_route(buf, ref)
+    A = int(ref["expert_offset"][-1])
+    want_xd = oracle.dispatch(x, ref["route_row"], cfg.R, fill=SENT)
+    np.testing.assert_array_equal(bits(buf.x_disp), want_xd)
+    gate = buf.topk_gate.cpu().numpy()  # the GPU's gates, so the check is exact
+    np.testing.assert_array_equal(bits(buf.y), oracle.combine(want_xd[:max(A, 1)], ref["route_row"],
+                                                              gate))
+
+
+def test_route_nan_logits(moe):
+    """NaN logits rank as -inf (ties to the lower expert): tokens whose row
+    holds a NaN have only NaN logits and take experts 0..K-1 with equal gates;
+    an expert whose router row holds a NaN is never chosen over a number."""
+    cfg = MoEConfig("nan", T=200, d=96, N=12, K=3, h=64, cf_num=2, cf_den=1, seed=31)
+    x, wr = synth.gen_x(cfg), synth.gen_router(cfg)
+    x = x.copy()
+    wr = wr.copy()
+    x[[0, 17, 199], 5] = 0x7FC0      # bf16 quiet NaN
+    x[50, 0] = 0xFF80                # -inf times weights of both signs: NaN or -inf/+inf
+    wr[7, 40] = np.float32("nan")
+    ref = oracle.route(x, wr, None, cfg.K, cfg.cap)
+    assert np.isnan(ref["logits"][0]).all() and np.isnan(ref["logits"][:, 7]).all()
+    assert ref["topk_idx"][0].tolist() == [0, 1, 2]
+    assert not (ref["topk_idx"][1:17] == 7).any()
+    s, buf = _route_only(moe, cfg, x, wr, None)
+    torch.cuda.synchronize()
+    _check_route(buf, ref)
+    np.testing.assert_allclose(buf.topk_gate.cpu().numpy()[0], 1.0 / 3.0, rtol=1e-6)
 
 
 def test_movement_kernels_bit_exact(moe):
