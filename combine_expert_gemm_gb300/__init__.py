@@ -18,7 +18,8 @@ import torch
 from .build import LIB
 
 __all__ = ["Shape", "MoEError", "lib", "route", "dispatch", "expert_ffn", "combine",
-           "combine_backward", "dispatch_backward", "read_device_error",
+           "combine_backward", "dispatch_backward", "read_device_error", "dispatch_checked",
+           "combine_checked", "combine_backward_checked", "dispatch_backward_checked",
            "route_workspace_bytes", "route_logits", "expert_ffn_workspace_bytes", "capacity", "LayerBuffers",
            "layer_forward", "expert_ffn_backward", "expert_ffn_backward_workspace_bytes",
            "BackwardBuffers", "layer_backward", "MxWeights", "MxLayerBuffers", "mx_act_scale_bytes",
@@ -63,6 +64,10 @@ _SIG = {
     "moe_combine": ([_SP, _P, _P, _P, _P, _P], ctypes.c_int),
     "moe_combine_backward": ([_SP, _P, _P, _P, _P, _P, _P, _P], ctypes.c_int),
     "moe_dispatch_backward": ([_SP, _P, _P, _P, _P], ctypes.c_int),
+    "moe_dispatch_checked": ([_SP, _P, _P, _P, _P, _P], ctypes.c_int),
+    "moe_combine_checked": ([_SP, _P, _P, _P, _P, _P, _P], ctypes.c_int),
+    "moe_combine_backward_checked": ([_SP] + [_P] * 6 + [_P, _P], ctypes.c_int),
+    "moe_dispatch_backward_checked": ([_SP, _P, _P, _P, _P, _P], ctypes.c_int),
     "moe_read_device_error": ([_P, ctypes.POINTER(ctypes.c_int32), _P], ctypes.c_int),
     "moe_expert_ffn_backward_workspace_bytes": ([_SP], _SZ),
     "moe_expert_ffn_backward": ([_SP] + [_P] * 14 + [_P, _SZ, _P], ctypes.c_int),
@@ -217,6 +222,44 @@ def dispatch_backward(shape, dx_disp, route_row, dx, stream=None):
     _check(_lib.moe_dispatch_backward(ctypes.byref(shape), _ptr(dx_disp, _bf16, "dx_disp"),
                                       _ptr(route_row, _i32, "route_row"), _ptr(dx, _f32, "dx"),
                                       _stream(stream)), "moe_dispatch_backward")
+
+
+def _status_ptr(status_ws):
+    if status_ws.dtype != torch.uint8 or status_ws.numel() < 256:
+        raise ValueError("status_ws: a uint8 CUDA tensor of at least 256 bytes")
+    return _ptr(status_ws, None, "status_ws")
+
+
+def dispatch_checked(shape, x, route_row, x_disp, status_ws, stream=None):
+    """moe_dispatch with every route row compared with the buffer rows on the
+    device; a row past them is skipped and recorded in status_ws (include/moe.h)."""
+    _check(_lib.moe_dispatch_checked(ctypes.byref(shape), _ptr(x, _bf16, "x"),
+                                     _ptr(route_row, _i32, "route_row"),
+                                     _ptr(x_disp, _bf16, "x_disp"), _status_ptr(status_ws),
+                                     _stream(stream)), "moe_dispatch_checked")
+
+
+def combine_checked(shape, y_disp, route_row, topk_gate, y, status_ws, stream=None):
+    _check(_lib.moe_combine_checked(ctypes.byref(shape), _ptr(y_disp, _bf16, "y_disp"),
+                                    _ptr(route_row, _i32, "route_row"),
+                                    _ptr(topk_gate, _f32, "topk_gate"), _ptr(y, _bf16, "y"),
+                                    _status_ptr(status_ws), _stream(stream)), "moe_combine_checked")
+
+
+def combine_backward_checked(shape, dy, y_disp, route_row, topk_gate, dy_disp, dgate, status_ws,
+                             stream=None):
+    _check(_lib.moe_combine_backward_checked(
+        ctypes.byref(shape), _ptr(dy, _bf16, "dy"), _ptr(y_disp, _bf16, "y_disp"),
+        _ptr(route_row, _i32, "route_row"), _ptr(topk_gate, _f32, "topk_gate"),
+        _ptr(dy_disp, _bf16, "dy_disp"), _ptr(dgate, _f32, "dgate"), _status_ptr(status_ws),
+        _stream(stream)), "moe_combine_backward_checked")
+
+
+def dispatch_backward_checked(shape, dx_disp, route_row, dx, status_ws, stream=None):
+    _check(_lib.moe_dispatch_backward_checked(
+        ctypes.byref(shape), _ptr(dx_disp, _bf16, "dx_disp"), _ptr(route_row, _i32, "route_row"),
+        _ptr(dx, _f32, "dx"), _status_ptr(status_ws), _stream(stream)),
+        "moe_dispatch_backward_checked")
 
 
 def expert_ffn_backward_workspace_bytes(shape):

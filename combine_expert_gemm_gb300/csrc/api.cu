@@ -13,6 +13,7 @@ MOE_API const char *moe_status_string(moe_status s) {
         case MOE_ERR_CUDA: return "MOE_ERR_CUDA: a CUDA call or kernel launch failed";
         case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: shape outside what the kernels handle";
         case MOE_ERR_DEVICE_TIMEOUT: return "MOE_ERR_DEVICE_TIMEOUT: a bounded wait inside a kernel expired";
+        case MOE_ERR_DEVICE_ROUTE_RANGE: return "MOE_ERR_DEVICE_ROUTE_RANGE: a checked call skipped a route row outside the capacity buffers";
     }
     return "unknown moe_status";
 }

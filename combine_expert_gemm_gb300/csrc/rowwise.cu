@@ -12,6 +12,12 @@
 // shuffles.  All four kernels are HBM-bound.  The dispatch backward can also
 // add the router's share of dx (and write dlogit) in the same pass over the
 // token's rows.
+//
+// Checked variants (CHECK = true; the *_checked entry points): every route
+// row a kernel takes is first compared with the R rows of the capacity
+// buffers.  A row at or past R is recorded as MOE_ERR_DEVICE_ROUTE_RANGE in the caller's status word
+// and the route is skipped as if it were dropped, so no address outside the
+// buffers is formed.  The release instantiations compile the check out.
 #include "moe_common.cuh"
 
 namespace moe {
@@ -33,14 +39,28 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
                       pack_bf16x2(f[6], f[7]));
 }
 
+// A route row for a checked kernel: rows at or past R are recorded in the
+// status word and read as -1 (dropped).
+template <bool CHECK>
+__device__ __forceinline__ int32_t checked_row(int32_t r, int64_t R, int32_t *status) {
+    if (CHECK && r >= R) {
+        atomicCAS(status, 0, (int32_t)MOE_ERR_DEVICE_ROUTE_RANGE);
+        return -1;
+    }
+    return r;
+}
+
+template <bool CHECK>
 __global__ void __launch_bounds__(kThreads)
 dispatch_rows(int T, int nchunk, int K, const uint4 *__restrict__ x,
-              const int32_t *__restrict__ route_row, uint4 *__restrict__ x_disp) {
+              const int32_t *__restrict__ route_row, uint4 *__restrict__ x_disp, int64_t R,
+              int32_t *status) {
     pdl_enter();
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
     if (t >= T) return;
-    const int32_t my_row = lane < K ? route_row[(int64_t)t * K + lane] : -1;
+    const int32_t my_row =
+        lane < K ? checked_row<CHECK>(route_row[(int64_t)t * K + lane], R, status) : -1;
     const uint4 *src = x + (int64_t)t * nchunk;
     for (int c0 = 0; c0 < nchunk; c0 += 32 * kSeg) {
         uint4 v[kSeg];
@@ -64,16 +84,17 @@ dispatch_rows(int T, int nchunk, int K, const uint4 *__restrict__ x,
 
 // MAXK (8 or 16) bounds the route count K: the K route rows of a chunk are
 // all in flight at once, and a smaller bound keeps more warps resident.
-template <int MAXK>
+template <int MAXK, bool CHECK>
 __global__ void __launch_bounds__(kThreads, MAXK <= 8 ? 4 : 2)
 combine_rows(int T, int nchunk, int K, const uint4 *__restrict__ y_disp,
              const int32_t *__restrict__ route_row, const float *__restrict__ gate,
-             uint4 *__restrict__ y) {
+             uint4 *__restrict__ y, int64_t R, int32_t *status) {
     pdl_enter();
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
     if (t >= T) return;
-    const int32_t my_row = lane < K ? route_row[(int64_t)t * K + lane] : -1;
+    const int32_t my_row =
+        lane < K ? checked_row<CHECK>(route_row[(int64_t)t * K + lane], R, status) : -1;
     const float my_g = lane < K ? gate[(int64_t)t * K + lane] : 0.0f;
     int32_t rows[MAXK];
     float gs[MAXK];
@@ -106,17 +127,18 @@ combine_rows(int T, int nchunk, int K, const uint4 *__restrict__ y_disp,
 // Chunk-outer: for each 16-byte chunk of the token row, all K route rows are
 // read at once; the K partial dot products for dgate stay in registers and
 // are reduced across the warp at the end.
-template <int MAXK>
+template <int MAXK, bool CHECK>
 __global__ void __launch_bounds__(kThreads, MAXK <= 8 ? 3 : 2)
 combine_bwd_rows(int T, int nchunk, int K, const uint4 *__restrict__ dy,
                  const uint4 *__restrict__ y_disp, const int32_t *__restrict__ route_row,
                  const float *__restrict__ gate, uint4 *__restrict__ dy_disp,
-                 float *__restrict__ dgate) {
+                 float *__restrict__ dgate, int64_t R, int32_t *status) {
     pdl_enter();
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
     if (t >= T) return;
-    const int32_t my_row = lane < K ? route_row[(int64_t)t * K + lane] : -1;
+    const int32_t my_row =
+        lane < K ? checked_row<CHECK>(route_row[(int64_t)t * K + lane], R, status) : -1;
     const float my_g = lane < K ? gate[(int64_t)t * K + lane] : 0.0f;
     int32_t rows[MAXK];
     float gs[MAXK], part[MAXK];
@@ -171,13 +193,13 @@ combine_bwd_rows(int T, int nchunk, int K, const uint4 *__restrict__ dy,
 // bits as DBWD_PLAIN followed by DBWD_ROUTER_ADD.
 enum { DBWD_PLAIN = 0, DBWD_ROUTER = 1, DBWD_ROUTER_ADD = 2 };
 
-template <int MAXK, int MODE>
+template <int MAXK, int MODE, bool CHECK = false>
 __global__ void __launch_bounds__(kThreads, MODE == DBWD_PLAIN ? (MAXK <= 8 ? 4 : 2) : (MAXK <= 8 ? 2 : 1))
 dispatch_bwd_rows(int T, int nchunk, int K, int N, const uint4 *__restrict__ dx_disp,
                   const int32_t *__restrict__ route_row, float4 *__restrict__ dx,
                   const float4 *__restrict__ w_r, const int32_t *__restrict__ topk_idx,
                   const float *__restrict__ gate, const float *__restrict__ dgate,
-                  float *__restrict__ dlogit) {
+                  float *__restrict__ dlogit, int64_t R = 0, int32_t *status = nullptr) {
     pdl_enter();
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * kWarps + (threadIdx.x >> 5);
@@ -185,7 +207,8 @@ dispatch_bwd_rows(int T, int nchunk, int K, int N, const uint4 *__restrict__ dx_
     // lane k < K holds route k's row, expert and dlogit; the chunk loop
     // broadcasts them with shuffles (fewer live registers than arrays)
     int32_t my_row = -1;
-    if (MODE != DBWD_ROUTER_ADD && lane < K) my_row = route_row[(int64_t)t * K + lane];
+    if (MODE != DBWD_ROUTER_ADD && lane < K)
+        my_row = checked_row<CHECK>(route_row[(int64_t)t * K + lane], R, status);
     float my_dl = 0.f;
     int32_t my_e = -1;
     if (MODE != DBWD_PLAIN) {
@@ -280,6 +303,96 @@ dispatch_bwd_rows(int T, int nchunk, int K, int N, const uint4 *__restrict__ dx_
 
 inline int grid_for(int T) { return (T + kWarps - 1) / kWarps; }
 
+// Launchers shared by the release and the checked entry points; arguments are
+// checked by the callers.  status is the checked calls' status word (unused
+// when CHECK is false).
+template <bool CHECK>
+moe_status launch_dispatch(const moe_shape *s, const moe_bf16 *x, const int32_t *route_row,
+                           moe_bf16 *x_disp, int32_t *status, cudaStream_t stream) {
+    launch_pdl(dispatch_rows<CHECK>, grid_for(s->T), kThreads, 0, stream, s->T, s->d / 8, s->K,
+               reinterpret_cast<const uint4 *>(x), route_row, reinterpret_cast<uint4 *>(x_disp),
+               buffer_rows(s), status);
+    return launch_status();
+}
+
+template <bool CHECK>
+moe_status launch_combine(const moe_shape *s, const moe_bf16 *y_disp, const int32_t *route_row,
+                          const float *topk_gate, moe_bf16 *y, int32_t *status,
+                          cudaStream_t stream) {
+    auto *kern = s->K <= 8 ? combine_rows<8, CHECK> : combine_rows<16, CHECK>;
+    launch_pdl(kern, grid_for(s->T), kThreads, 0, stream, s->T, s->d / 8, s->K,
+               reinterpret_cast<const uint4 *>(y_disp), route_row, topk_gate,
+               reinterpret_cast<uint4 *>(y), buffer_rows(s), status);
+    return launch_status();
+}
+
+template <bool CHECK>
+moe_status launch_combine_bwd(const moe_shape *s, const moe_bf16 *dy, const moe_bf16 *y_disp,
+                              const int32_t *route_row, const float *topk_gate, moe_bf16 *dy_disp,
+                              float *dgate, int32_t *status, cudaStream_t stream) {
+    auto *kern = s->K <= 8 ? combine_bwd_rows<8, CHECK> : combine_bwd_rows<16, CHECK>;
+    launch_pdl(kern, grid_for(s->T), kThreads, 0, stream, s->T, s->d / 8, s->K,
+               reinterpret_cast<const uint4 *>(dy), reinterpret_cast<const uint4 *>(y_disp),
+               route_row, topk_gate, reinterpret_cast<uint4 *>(dy_disp), dgate, buffer_rows(s),
+               status);
+    return launch_status();
+}
+
+template <bool CHECK>
+moe_status launch_dispatch_bwd(const moe_shape *s, const moe_bf16 *dx_disp,
+                               const int32_t *route_row, float *dx, int32_t *status,
+                               cudaStream_t stream) {
+    auto *kern = s->K <= 8 ? dispatch_bwd_rows<8, DBWD_PLAIN, CHECK>
+                           : dispatch_bwd_rows<16, DBWD_PLAIN, CHECK>;
+    launch_pdl(kern, grid_for(s->T), kThreads, 0, stream, s->T, s->d / 8, s->K, s->N,
+               reinterpret_cast<const uint4 *>(dx_disp), route_row, reinterpret_cast<float4 *>(dx),
+               nullptr, nullptr, nullptr, nullptr, nullptr, buffer_rows(s), status);
+    return launch_status();
+}
+
+// The status word of a checked call: word 0 of a 256-byte-aligned workspace.
+inline int32_t *status_word(void *status_ws) { return static_cast<int32_t *>(status_ws); }
+inline bool status_ws_ok(const void *p) {
+    return p && (reinterpret_cast<uintptr_t>(p) & 255u) == 0;
+}
+
+// ---- argument checks shared by the release and checked entry points -------
+
+inline moe_status check_dispatch(const moe_shape *s, const moe_bf16 *x, const int32_t *route_row,
+                                 const moe_bf16 *x_disp) {
+    if (!x || !route_row || !x_disp) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(route_row) || !aligned16(x_disp)) return MOE_ERR_ALIGNMENT;
+    return MOE_OK;
+}
+
+inline moe_status check_combine(const moe_shape *s, const moe_bf16 *y_disp,
+                                const int32_t *route_row, const float *topk_gate,
+                                const moe_bf16 *y) {
+    if (!route_row || !topk_gate || !y || (s->cap > 0 && !y_disp)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(y_disp) || !aligned16(route_row) || !aligned16(topk_gate) || !aligned16(y))
+        return MOE_ERR_ALIGNMENT;
+    return MOE_OK;
+}
+
+inline moe_status check_combine_bwd(const moe_shape *s, const moe_bf16 *dy,
+                                    const moe_bf16 *y_disp, const int32_t *route_row,
+                                    const float *topk_gate, const moe_bf16 *dy_disp,
+                                    const float *dgate) {
+    if (!dy || !route_row || !topk_gate || !dgate || (s->cap > 0 && (!y_disp || !dy_disp)))
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16(dy) || !aligned16(y_disp) || !aligned16(route_row) || !aligned16(topk_gate) ||
+        !aligned16(dy_disp) || !aligned16(dgate))
+        return MOE_ERR_ALIGNMENT;
+    return MOE_OK;
+}
+
+inline moe_status check_dispatch_bwd(const moe_shape *s, const moe_bf16 *dx_disp,
+                                     const int32_t *route_row, const float *dx) {
+    if (!route_row || !dx || (s->cap > 0 && !dx_disp)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(dx_disp) || !aligned16(route_row) || !aligned16(dx)) return MOE_ERR_ALIGNMENT;
+    return MOE_OK;
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -290,11 +403,8 @@ MOE_API moe_status moe_dispatch(const moe_shape *s, const moe_bf16 *x, const int
     moe_status r = check_shape(s);
     if (r != MOE_OK) return r;
     if (s->T == 0 || s->cap == 0) return MOE_OK;  // no row can be written
-    if (!x || !route_row || !x_disp) return MOE_ERR_INVALID_ARG;
-    if (!aligned16(x) || !aligned16(route_row) || !aligned16(x_disp)) return MOE_ERR_ALIGNMENT;
-    launch_pdl(dispatch_rows, grid_for(s->T), kThreads, 0, stream, s->T, s->d / 8, s->K,
-               reinterpret_cast<const uint4 *>(x), route_row, reinterpret_cast<uint4 *>(x_disp));
-    return launch_status();
+    if ((r = check_dispatch(s, x, route_row, x_disp)) != MOE_OK) return r;
+    return launch_dispatch<false>(s, x, route_row, x_disp, nullptr, stream);
 }
 
 MOE_API moe_status moe_combine(const moe_shape *s, const moe_bf16 *y_disp,
@@ -303,14 +413,8 @@ MOE_API moe_status moe_combine(const moe_shape *s, const moe_bf16 *y_disp,
     moe_status r = check_shape(s);
     if (r != MOE_OK) return r;
     if (s->T == 0) return MOE_OK;
-    if (!route_row || !topk_gate || !y || (s->cap > 0 && !y_disp)) return MOE_ERR_INVALID_ARG;
-    if (!aligned16(y_disp) || !aligned16(route_row) || !aligned16(topk_gate) || !aligned16(y))
-        return MOE_ERR_ALIGNMENT;
-    auto *kern = s->K <= 8 ? combine_rows<8> : combine_rows<16>;
-    launch_pdl(kern, grid_for(s->T), kThreads, 0, stream, s->T, s->d / 8, s->K,
-               reinterpret_cast<const uint4 *>(y_disp), route_row, topk_gate,
-               reinterpret_cast<uint4 *>(y));
-    return launch_status();
+    if ((r = check_combine(s, y_disp, route_row, topk_gate, y)) != MOE_OK) return r;
+    return launch_combine<false>(s, y_disp, route_row, topk_gate, y, nullptr, stream);
 }
 
 MOE_API moe_status moe_combine_backward(const moe_shape *s, const moe_bf16 *dy,
@@ -320,16 +424,10 @@ MOE_API moe_status moe_combine_backward(const moe_shape *s, const moe_bf16 *dy,
     moe_status r = check_shape(s);
     if (r != MOE_OK) return r;
     if (s->T == 0) return MOE_OK;
-    if (!dy || !route_row || !topk_gate || !dgate || (s->cap > 0 && (!y_disp || !dy_disp)))
-        return MOE_ERR_INVALID_ARG;
-    if (!aligned16(dy) || !aligned16(y_disp) || !aligned16(route_row) || !aligned16(topk_gate) ||
-        !aligned16(dy_disp) || !aligned16(dgate))
-        return MOE_ERR_ALIGNMENT;
-    auto *kern = s->K <= 8 ? combine_bwd_rows<8> : combine_bwd_rows<16>;
-    launch_pdl(kern, grid_for(s->T), kThreads, 0, stream, s->T, s->d / 8, s->K,
-               reinterpret_cast<const uint4 *>(dy), reinterpret_cast<const uint4 *>(y_disp),
-               route_row, topk_gate, reinterpret_cast<uint4 *>(dy_disp), dgate);
-    return launch_status();
+    if ((r = check_combine_bwd(s, dy, y_disp, route_row, topk_gate, dy_disp, dgate)) != MOE_OK)
+        return r;
+    return launch_combine_bwd<false>(s, dy, y_disp, route_row, topk_gate, dy_disp, dgate, nullptr,
+                                     stream);
 }
 
 MOE_API moe_status moe_dispatch_backward(const moe_shape *s, const moe_bf16 *dx_disp,
@@ -338,13 +436,58 @@ MOE_API moe_status moe_dispatch_backward(const moe_shape *s, const moe_bf16 *dx_
     moe_status r = check_shape(s);
     if (r != MOE_OK) return r;
     if (s->T == 0) return MOE_OK;
-    if (!route_row || !dx || (s->cap > 0 && !dx_disp)) return MOE_ERR_INVALID_ARG;
-    if (!aligned16(dx_disp) || !aligned16(route_row) || !aligned16(dx)) return MOE_ERR_ALIGNMENT;
-    auto *kern = s->K <= 8 ? dispatch_bwd_rows<8, DBWD_PLAIN> : dispatch_bwd_rows<16, DBWD_PLAIN>;
-    launch_pdl(kern, grid_for(s->T), kThreads, 0, stream, s->T, s->d / 8, s->K, s->N,
-               reinterpret_cast<const uint4 *>(dx_disp), route_row, reinterpret_cast<float4 *>(dx),
-               nullptr, nullptr, nullptr, nullptr, nullptr);
-    return launch_status();
+    if ((r = check_dispatch_bwd(s, dx_disp, route_row, dx)) != MOE_OK) return r;
+    return launch_dispatch_bwd<false>(s, dx_disp, route_row, dx, nullptr, stream);
+}
+
+// ---- checked variants: route rows validated on the device ------------------
+
+MOE_API moe_status moe_dispatch_checked(const moe_shape *s, const moe_bf16 *x,
+                                        const int32_t *route_row, moe_bf16 *x_disp,
+                                        void *status_ws, cudaStream_t stream) {
+    moe_status r = check_shape(s);
+    if (r != MOE_OK) return r;
+    if (!status_ws_ok(status_ws)) return MOE_ERR_WORKSPACE;
+    if (s->T == 0 || s->cap == 0) return MOE_OK;
+    if ((r = check_dispatch(s, x, route_row, x_disp)) != MOE_OK) return r;
+    return launch_dispatch<true>(s, x, route_row, x_disp, status_word(status_ws), stream);
+}
+
+MOE_API moe_status moe_combine_checked(const moe_shape *s, const moe_bf16 *y_disp,
+                                       const int32_t *route_row, const float *topk_gate,
+                                       moe_bf16 *y, void *status_ws, cudaStream_t stream) {
+    moe_status r = check_shape(s);
+    if (r != MOE_OK) return r;
+    if (!status_ws_ok(status_ws)) return MOE_ERR_WORKSPACE;
+    if (s->T == 0) return MOE_OK;
+    if ((r = check_combine(s, y_disp, route_row, topk_gate, y)) != MOE_OK) return r;
+    return launch_combine<true>(s, y_disp, route_row, topk_gate, y, status_word(status_ws), stream);
+}
+
+MOE_API moe_status moe_combine_backward_checked(const moe_shape *s, const moe_bf16 *dy,
+                                                const moe_bf16 *y_disp, const int32_t *route_row,
+                                                const float *topk_gate, moe_bf16 *dy_disp,
+                                                float *dgate, void *status_ws,
+                                                cudaStream_t stream) {
+    moe_status r = check_shape(s);
+    if (r != MOE_OK) return r;
+    if (!status_ws_ok(status_ws)) return MOE_ERR_WORKSPACE;
+    if (s->T == 0) return MOE_OK;
+    if ((r = check_combine_bwd(s, dy, y_disp, route_row, topk_gate, dy_disp, dgate)) != MOE_OK)
+        return r;
+    return launch_combine_bwd<true>(s, dy, y_disp, route_row, topk_gate, dy_disp, dgate,
+                                    status_word(status_ws), stream);
+}
+
+MOE_API moe_status moe_dispatch_backward_checked(const moe_shape *s, const moe_bf16 *dx_disp,
+                                                 const int32_t *route_row, float *dx,
+                                                 void *status_ws, cudaStream_t stream) {
+    moe_status r = check_shape(s);
+    if (r != MOE_OK) return r;
+    if (!status_ws_ok(status_ws)) return MOE_ERR_WORKSPACE;
+    if (s->T == 0) return MOE_OK;
+    if ((r = check_dispatch_bwd(s, dx_disp, route_row, dx)) != MOE_OK) return r;
+    return launch_dispatch_bwd<true>(s, dx_disp, route_row, dx, status_word(status_ws), stream);
 }
 
 namespace moe {
@@ -356,7 +499,8 @@ moe_status launch_router_dx(const moe_shape *s, const moe_bf16 *dx_disp, const i
                             const float *topk_gate, const float *dgate, float *dlogit, float *dx,
                             bool add, cudaStream_t stream) {
     using Fn = void (*)(int, int, int, int, const uint4 *, const int32_t *, float4 *,
-                        const float4 *, const int32_t *, const float *, const float *, float *);
+                        const float4 *, const int32_t *, const float *, const float *, float *,
+                        int64_t, int32_t *);
     Fn kern;
     if (add)
         kern = s->K <= 8 ? dispatch_bwd_rows<8, DBWD_ROUTER_ADD>
@@ -365,7 +509,8 @@ moe_status launch_router_dx(const moe_shape *s, const moe_bf16 *dx_disp, const i
         kern = s->K <= 8 ? dispatch_bwd_rows<8, DBWD_ROUTER> : dispatch_bwd_rows<16, DBWD_ROUTER>;
     launch_pdl(kern, grid_for(s->T), kThreads, 0, stream, s->T, s->d / 8, s->K, s->N,
                reinterpret_cast<const uint4 *>(dx_disp), route_row, reinterpret_cast<float4 *>(dx),
-               reinterpret_cast<const float4 *>(w_router), topk_idx, topk_gate, dgate, dlogit);
+               reinterpret_cast<const float4 *>(w_router), topk_idx, topk_gate, dgate, dlogit,
+               buffer_rows(s), static_cast<int32_t *>(nullptr));
     return launch_status();
 }
 }  // namespace moe

@@ -38,7 +38,8 @@
  *     Rows from expert_offset[N] to R - 1 (the tail) are neither read nor
  *     written by any call and may hold anything, including NaN.
  *   - Host-side argument errors are returned before anything is enqueued.
- *     Errors seen on the device (a wait that timed out) are recorded in the
+ *     Errors seen on the device (a wait that timed out; in the *_checked
+ *     calls, a route row outside the buffers) are recorded in the
  *     workspace's status word; moe_read_device_error() reads it.
  *   - Results are deterministic: no floating-point atomics anywhere.
  */
@@ -62,7 +63,9 @@ typedef enum {
     MOE_ERR_WORKSPACE = 3,    /* workspace missing or smaller than the *_workspace_bytes query */
     MOE_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
     MOE_ERR_UNSUPPORTED = 5,  /* shape outside what the kernels handle (see each call) */
-    MOE_ERR_DEVICE_TIMEOUT = 6 /* device status word: a bounded wait inside a kernel expired */
+    MOE_ERR_DEVICE_TIMEOUT = 6, /* device status word: a bounded wait inside a kernel expired */
+    MOE_ERR_DEVICE_ROUTE_RANGE = 7 /* device status word: a *_checked call met a route row
+                                      >= R and skipped that route */
 } moe_status;
 
 /* Layer shape.  cap is chosen by the caller before its loop, e.g.
@@ -289,6 +292,36 @@ moe_status moe_combine_backward(const moe_shape *s, const moe_bf16 *dy, const mo
  */
 moe_status moe_dispatch_backward(const moe_shape *s, const moe_bf16 *dx_disp,
                                  const int32_t *route_row, float *dx, cudaStream_t stream);
+
+/*
+ * Checked variants of the four row movements, for debugging a route map that
+ * did not come from moe_route (Section 05, 5.4: a negative row marks a
+ * dropped route; every other row must name a row of the capacity buffers).
+ * Same arguments and results as moe_dispatch, moe_combine,
+ * moe_combine_backward and moe_dispatch_backward, plus status_ws: a device
+ * workspace of at least 256 bytes, 256-byte aligned, whose word 0 is the
+ * status word (zero it before the first call; moe_read_device_error reads
+ * and clears it).  The kernels compare every route row with
+ * R = moe_buffer_rows(s) before using it: a row >= R records
+ * MOE_ERR_DEVICE_ROUTE_RANGE in the status word and the route is skipped as
+ * if it were dropped (nothing is read or written through it), so the outputs
+ * equal those of the same route map with that entry set to -1.  The check
+ * costs one comparison per route; the release calls above run kernels with
+ * the check compiled out.  Host-side errors: as the release calls, plus
+ * MOE_ERR_WORKSPACE for a missing or misaligned status_ws.
+ */
+moe_status moe_dispatch_checked(const moe_shape *s, const moe_bf16 *x, const int32_t *route_row,
+                                moe_bf16 *x_disp, void *status_ws, cudaStream_t stream);
+moe_status moe_combine_checked(const moe_shape *s, const moe_bf16 *y_disp,
+                               const int32_t *route_row, const float *topk_gate, moe_bf16 *y,
+                               void *status_ws, cudaStream_t stream);
+moe_status moe_combine_backward_checked(const moe_shape *s, const moe_bf16 *dy,
+                                        const moe_bf16 *y_disp, const int32_t *route_row,
+                                        const float *topk_gate, moe_bf16 *dy_disp, float *dgate,
+                                        void *status_ws, cudaStream_t stream);
+moe_status moe_dispatch_backward_checked(const moe_shape *s, const moe_bf16 *dx_disp,
+                                         const int32_t *route_row, float *dx, void *status_ws,
+                                         cudaStream_t stream);
 
 /* Bytes of workspace moe_router_backward and moe_router_weight_backward need
  * (per-chunk partial sums of dW_r and dbias: at most 32 * N * (d + 1) floats;

@@ -89,6 +89,20 @@ def test_route_logits_offset_lies_inside_the_workspace(moe):
     assert lib.moe_route_logits_offset(ctypes.byref(_shape(moe, K=0))) == 0
 
 
+def test_checked_calls_want_a_status_workspace(moe):
+    """The checked row movements refuse a missing or misaligned status
+    workspace (MOE_ERR_WORKSPACE) before anything is enqueued."""
+    s = _shape(moe)
+    lib = moe.lib()
+    P = ctypes.c_void_p(256)
+    for bad in (None, ctypes.c_void_p(4096 + 16)):
+        assert lib.moe_dispatch_checked(ctypes.byref(s), P, P, P, bad, None) == 3
+        assert lib.moe_combine_checked(ctypes.byref(s), P, P, P, P, bad, None) == 3
+        assert lib.moe_combine_backward_checked(ctypes.byref(s), P, P, P, P, P, P, bad, None) == 3
+        assert lib.moe_dispatch_backward_checked(ctypes.byref(s), P, P, P, bad, None) == 3
+    assert b"ROUTE_RANGE" in lib.moe_status_string(7)
+
+
 def test_router_backward_argument_errors(moe):
     s = _shape(moe)
     lib = moe.lib()
