@@ -82,8 +82,12 @@ dispatch_rows(int T, int nchunk, int K, const uint4 *__restrict__ x,
     }
 }
 
-// MAXK (8 or 16) bounds the route count K: the K route rows of a chunk are
-// all in flight at once, and a smaller bound keeps more warps resident.
+// MAXK (8 or 16) bounds the route count K.  The token's accepted routes are
+// first compacted to lanes 0..nv-1 (k ascending); each pass then covers two
+// 16-byte chunks per lane and takes the accepted rows four at a time, so a
+// token with few accepted routes (a drop-heavy layer) still keeps 8 loads per
+// lane in flight.  The fp32 fma chain of every element runs over the
+// accepted routes in k order, as before the compaction.
 template <int MAXK, bool CHECK>
 __global__ void __launch_bounds__(kThreads, MAXK <= 8 ? 4 : 2)
 combine_rows(int T, int nchunk, int K, const uint4 *__restrict__ y_disp,
@@ -96,31 +100,60 @@ combine_rows(int T, int nchunk, int K, const uint4 *__restrict__ y_disp,
     const int32_t my_row =
         lane < K ? checked_row<CHECK>(route_row[(int64_t)t * K + lane], R, status) : -1;
     const float my_g = lane < K ? gate[(int64_t)t * K + lane] : 0.0f;
-    int32_t rows[MAXK];
-    float gs[MAXK];
+    // lane j < nv gets the j-th accepted route (k ascending)
+    int32_t rc = -1;
+    float gc = 0.0f;
+    int nv = 0;  // warp-uniform
 #pragma unroll
     for (int k = 0; k < MAXK; ++k) {
-        rows[k] = __shfl_sync(0xFFFFFFFFu, my_row, k);
-        gs[k] = __shfl_sync(0xFFFFFFFFu, my_g, k);
-    }
-    // the chunk loop is warp-uniform; no shuffles inside
-    for (int c0 = 0; c0 < nchunk; c0 += 32) {
-        const int c = c0 + lane;
-        if (c >= nchunk) break;
-        uint4 v[MAXK];
-#pragma unroll
-        for (int k = 0; k < MAXK; ++k)
-            if (k < K && rows[k] >= 0) v[k] = __ldcs(y_disp + (int64_t)rows[k] * nchunk + c);
-        float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-#pragma unroll
-        for (int k = 0; k < MAXK; ++k) {
-            if (k >= K || rows[k] < 0) continue;
-            float f[8];
-            unpack8(v[k], f);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = __fmaf_rn(gs[k], f[i], acc[i]);
+        const int32_t r = __shfl_sync(0xFFFFFFFFu, my_row, k);
+        const float g = __shfl_sync(0xFFFFFFFFu, my_g, k);
+        if (k < K && r >= 0) {
+            if (lane == nv) {
+                rc = r;
+                gc = g;
+            }
+            ++nv;
         }
-        y[(int64_t)t * nchunk + c] = pack8(acc);
+    }
+    // the chunk loop is warp-uniform (the shuffles need every lane)
+    for (int c0 = 0; c0 < nchunk; c0 += 64) {
+        const int ca = c0 + lane, cb = ca + 32;
+        float acc[2][8];
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[h][i] = 0.0f;
+#pragma unroll
+        for (int g0 = 0; g0 < MAXK; g0 += 4) {
+            if (g0 >= nv) break;
+            int32_t r[4];
+            float gg[4];
+            uint4 v[4][2];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                r[u] = __shfl_sync(0xFFFFFFFFu, rc, g0 + u);
+                gg[u] = __shfl_sync(0xFFFFFFFFu, gc, g0 + u);
+                if (g0 + u < nv) {
+                    const uint4 *src = y_disp + (int64_t)r[u] * nchunk;
+                    if (ca < nchunk) v[u][0] = __ldcs(src + ca);
+                    if (cb < nchunk) v[u][1] = __ldcs(src + cb);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (g0 + u >= nv) continue;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    float f[8];
+                    unpack8(v[u][h], f);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) acc[h][i] = __fmaf_rn(gg[u], f[i], acc[h][i]);
+                }
+            }
+        }
+        if (ca < nchunk) y[(int64_t)t * nchunk + ca] = pack8(acc[0]);
+        if (cb < nchunk) y[(int64_t)t * nchunk + cb] = pack8(acc[1]);
     }
 }
 
