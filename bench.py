@@ -525,7 +525,7 @@ def run_ours(args, cfg, rank, world):
     if fused_ms is not None:
         line["fused_dispatch_ffn"] = {
             "ms": fused_ms, "two_step_ms": ph_ms["dispatch"] + ph_ms["ffn"],
-            "note": "moe_expert_ffn_gather (x rows fetched by TMA gather4 in GEMM1) vs dispatch + expert_ffn"}
+            "note": "moe_expert_ffn_gather (x rows gathered by cp.async inside GEMM1) vs dispatch + expert_ffn"}
     if mx is not None:
         mms = mx["ms"]
         T, d, K = cfg.T, cfg.d, cfg.K

@@ -23,8 +23,9 @@
 //              a warp whose 32 rows are all valid writes each 32 x 32 output
 //              block to its 2 KB of shared memory (64-byte swizzle) and stores
 //              it with one TMA instruction; other warps store their valid rows.
-// With GATHER (moe_expert_ffn_gather) the F1 producer reads A rows straight
-// from x by route (tile::gather4 loads), so no dispatched copy is made.
+// With GATHER (moe_expert_ffn_gather) two more warps per CTA gather the A rows
+// straight from x by route (16-byte cp.async into the swizzled stage), so no
+// dispatched copy is made; // from x by route (tile::gather4 loads), so no dispatched copy is made.
 // Work list: every CTA derives, from expert_count in device memory, the tiles
 // of every expert (ceil(count/256) row tiles x output-column tiles) and walks
 // them round-robin.  Rows past an expert's count (the next expert's rows or
@@ -45,6 +46,10 @@ constexpr int ACC_COLS = 256;
 constexpr int TMEM_COLS = 512;
 constexpr int kEpiThreads = 256;  // 8 epilogue warps
 constexpr int kThreads = 64 + kEpiThreads;
+constexpr int kGatherWarps = 2;  // GATHER: warps 10-11 fetch the A rows
+constexpr int kGatherThreads = 32 * kGatherWarps;
+template <bool GATHER>
+constexpr int pair_threads() { return kThreads + (GATHER ? kGatherThreads : 0); }
 
 enum { EPI_SWIGLU = 0, EPI_STORE = 1 };
 
@@ -207,6 +212,7 @@ constexpr int P_EPI_WARPS = kEpiThreads / 32;
 struct alignas(8) PairBars {
     uint64_t full[P_STAGES];
     uint64_t empty[P_STAGES];
+    uint64_t gfull[P_STAGES];  // GATHER: this CTA's A rows of the stage landed
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint32_t tmem_base;
@@ -220,19 +226,35 @@ constexpr size_t smem_bytes_pair(int N) {
            sizeof(int32_t) * (N + 1) + 16;
 }
 
-// GATHER: A is not the packed buffer but the token rows themselves: the map
-// is over x [T, d] with a one-row box, and the producer fetches each packed
-// row r from x[row_token[r]] with tile::gather4 loads (four rows per load,
-// four producer lanes with 32 rows each).  Rows past the expert's count read
-// token 0; their accumulator rows are never stored.
+// GATHER: A is not the packed buffer but the token rows themselves.  The two
+// gather warps of each CTA fetch packed row r of its 128 from x[row_token[r]]
+// with 16-byte cp.async (thread t: rows t/8 + 8i, 16-byte chunk t%8 of the
+// k-block, written to the 128-byte swizzled position), so one warp
+// instruction moves four whole 128-byte rows; each thread's copies of a stage
+// arrive on the CTA's gfull barrier when they land, so the gather threads
+// never wait for their own copies and keep every free stage in flight.  Lane
+// 1 of warp 0 forwards each stage in order: it waits for gfull, fences the
+// rows to the async proxy (the tensor core reads them there) and arrives on
+// the leader's full barrier, which thus counts the leader's expect_tx (B by
+// TMA) and the two CTAs' forwards.  Rows past the expert's count read token
+// 0; their accumulator rows are never stored.
+__device__ __forceinline__ void cp_async16_s(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 template <int EPI, bool GATHER>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(pair_threads<GATHER>(), 1)
 grouped_gemm_pair(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b0,
                   const __grid_constant__ CUtensorMap tm_b1, const __grid_constant__ CUtensorMap tm_o,
                   const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_u,
                   int N, int Kdim, int Nout,
                   const int32_t *__restrict__ count, const int32_t *__restrict__ offset,
-                  const int32_t *__restrict__ row_token, uint16_t *__restrict__ out,
+                  const int32_t *__restrict__ row_token, const uint16_t *__restrict__ x_rows,
+                  uint16_t *__restrict__ out,
                   uint16_t *__restrict__ g_save, uint16_t *__restrict__ u_save, int *status) {
     pdl_enter();
     constexpr int BN_OUT = EPI == EPI_SWIGLU ? MMA_N / 2 : MMA_N;
@@ -254,8 +276,9 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tm_a, const __grid_constan
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < P_STAGES; ++s) {
-            mbar_init(smem_u32(&bars->full[s]), 1);
+            mbar_init(smem_u32(&bars->full[s]), GATHER ? 3 : 1);
             mbar_init(smem_u32(&bars->empty[s]), 1);
+            mbar_init(smem_u32(&bars->gfull[s]), kGatherThreads);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&bars->tfull[b]), 1);
@@ -303,15 +326,9 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tm_a, const __grid_constan
 
     if (warp == 0) {
         // -------------------------------------------- TMA producer (both CTAs)
-        // lane 0 drives the ring; with GATHER lanes 0-3 each fetch 32 of the
-        // CTA's 128 A rows
-        constexpr int PL = GATHER ? 4 : 1;
-        constexpr unsigned PMASK = (1u << PL) - 1u;
-        if (lane < PL) {
-            if (lane == 0) {
-                tma_prefetch_desc(&tm_a);
-                tma_prefetch_desc(rank && EPI == EPI_SWIGLU ? &tm_b1 : &tm_b0);
-            }
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_a);
+            tma_prefetch_desc(rank && EPI == EPI_SWIGLU ? &tm_b1 : &tm_b0);
             int stage = 0;
             uint32_t phase = 0;
             int issued = 0;
@@ -322,20 +339,8 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tm_a, const __grid_constan
                 const int b_row = EPI == EPI_SWIGLU ? t.e * Nout + t.n * BN_OUT
                                                     : t.e * Nout + t.n * BN_OUT + (int)rank * (MMA_N / 2);
                 const CUtensorMap *mb = rank && EPI == EPI_SWIGLU ? &tm_b1 : &tm_b0;
-                int tok[GATHER ? 32 : 1];
-                if (GATHER) {
-                    const int valid_end = offset[t.e] + count[t.e];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int r = a_row + lane * 32 + i;
-                        tok[i] = r < valid_end ? row_token[r] : 0;
-                    }
-                }
                 for (int kb = 0; kb < nk; ++kb) {
-                    bool got = true;
-                    if (lane == 0)
-                        got = mbar_wait(smem_u32(&bars->empty[stage]), phase ^ 1, status, abort);
-                    if (!__shfl_sync(PMASK, (int)got, 0)) {
+                    if (!mbar_wait(smem_u32(&bars->empty[stage]), phase ^ 1, status, abort)) {
                         ok = false;
                         break;
                     }
@@ -343,37 +348,45 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tm_a, const __grid_constan
                     const uint32_t full = cluster_map(own_full, 0);
                     const uint32_t sa = smem_u32(smem + (size_t)stage * P_STAGE_BYTES);
                     const uint32_t sb = sa + A_BYTES;
-                    if (lane == 0 && leader) mbar_arrive_expect_tx(own_full, 2 * P_STAGE_BYTES);
-                    if (GATHER) {
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            tma_gather4_pair(sa + (uint32_t)(lane * 32 + 4 * i) * 128, &tm_a, full,
-                                             kb * BK, tok[4 * i], tok[4 * i + 1], tok[4 * i + 2],
-                                             tok[4 * i + 3]);
-                    } else {
-                        tma_load_2d_pair(sa, &tm_a, full, kb * BK, a_row);
-                    }
-                    if (lane == 0) tma_load_2d_pair(sb, mb, full, kb * BK, b_row);
+                    if (leader)
+                        mbar_arrive_expect_tx(own_full, GATHER ? 2 * P_B_BYTES : 2 * P_STAGE_BYTES);
+                    if (!GATHER) tma_load_2d_pair(sa, &tm_a, full, kb * BK, a_row);
+                    tma_load_2d_pair(sb, mb, full, kb * BK, b_row);
                     ++issued;
                     if (++stage == P_STAGES) { stage = 0; phase ^= 1; }
                 }
             }
-            if (lane == 0) {
-                if (!ok && leader) {
-                    // the leader's full barriers count both CTAs' copies: let the
-                    // ones already issued land before the pair leaves
-                    for (int s = 0; s < P_STAGES; ++s) {
-                        volatile int no_abort = 0;
-                        mbar_wait(smem_u32(&bars->full[s]), phase ^ (s >= stage ? 1 : 0), status,
-                                  &no_abort);
-                    }
-                }
-                // every release of every stage (the leader's commits) has arrived
+            if (!ok && leader) {
+                // the leader's full barriers count both CTAs' copies: let the
+                // ones already issued land before the pair leaves
                 for (int s = 0; s < P_STAGES; ++s) {
-                    const int uses = issued / P_STAGES + (s < issued % P_STAGES ? 1 : 0);
-                    if (uses > 0)
-                        mbar_wait(smem_u32(&bars->empty[s]), (uint32_t)((uses - 1) & 1), status,
-                                  abort);
+                    volatile int no_abort = 0;
+                    mbar_wait(smem_u32(&bars->full[s]), phase ^ (s >= stage ? 1 : 0), status,
+                              &no_abort);
+                }
+            }
+            // every release of every stage (the leader's commits) has arrived
+            for (int s = 0; s < P_STAGES; ++s) {
+                const int uses = issued / P_STAGES + (s < issued % P_STAGES ? 1 : 0);
+                if (uses > 0)
+                    mbar_wait(smem_u32(&bars->empty[s]), (uint32_t)((uses - 1) & 1), status,
+                              abort);
+            }
+        } else if (GATHER && lane == 1) {
+            // forwarder: the gathered rows of each stage, in order, to the
+            // leader's full barrier once they have landed
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int g = unit0; g < total && ok; g += units) {
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!mbar_wait(smem_u32(&bars->gfull[stage]), phase, status, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    mbar_arrive_cluster(cluster_map(smem_u32(&bars->full[stage]), 0));
+                    if (++stage == P_STAGES) { stage = 0; phase ^= 1; }
                 }
             }
         }
@@ -391,7 +404,8 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tm_a, const __grid_constan
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * ACC_COLS);
                 for (int kb = 0; kb < nk; ++kb) {
-                    if (!mbar_wait(smem_u32(&bars->full[stage]), phase, status, abort)) {
+                    // GATHER: the peer's rows are released at cluster scope
+                    if (!mbar_wait<GATHER>(smem_u32(&bars->full[stage]), phase, status, abort)) {
                         ok = false;
                         break;
                     }
@@ -412,6 +426,40 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tm_a, const __grid_constan
                 if (++acc == 2) { acc = 0; acc_phase ^= 1; }
             }
         }
+    } else if (GATHER && warp >= 2 + P_EPI_WARPS) {
+        // ------------------------------------------- A-row gather (both CTAs)
+        const int gt = threadIdx.x - 32 * (2 + P_EPI_WARPS);  // 0..63
+        const int chunk = gt & 7;
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int g = unit0; g < total && ok; g += units) {
+            const TileMap t = map_pair(g);
+            const int a_row = offset[t.e] + t.m * PM + (int)rank * BM;
+            const int valid_end = offset[t.e] + count[t.e];
+            const uint16_t *src[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int r = a_row + gt / 8 + 8 * i;
+                src[i] = x_rows + (int64_t)(r < valid_end ? row_token[r] : 0) * Kdim + chunk * 8;
+            }
+            for (int kb = 0; kb < nk; ++kb) {
+                if (!mbar_wait(smem_u32(&bars->empty[stage]), phase ^ 1, status, abort)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t sa = smem_u32(smem + (size_t)stage * P_STAGE_BYTES);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int row = gt / 8 + 8 * i;
+                    cp_async16_s(sa + (uint32_t)row * 128 + (uint32_t)((chunk ^ (row & 7)) << 4),
+                                 src[i] + kb * BK);
+                }
+                cp_async_arrive_noinc(smem_u32(&bars->gfull[stage]));
+                if (++stage == P_STAGES) { stage = 0; phase ^= 1; }
+            }
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");
     } else {
         // ----------------------------------------------- epilogue (both CTAs)
         const int quad = warp & 3;
@@ -456,8 +504,9 @@ template <int EPI, bool GATHER>
 moe_status launch_gemm_pair(const CUtensorMap &a, const CUtensorMap &b0, const CUtensorMap &b1,
                             const CUtensorMap &o, const CUtensorMap &og, const CUtensorMap &ou,
                             int N, int Kdim, int Nout, int max_row_tiles, const int32_t *count,
-                            const int32_t *offset, const int32_t *row_token, uint16_t *out,
-                            uint16_t *gs, uint16_t *us, int *status, cudaStream_t st) {
+                            const int32_t *offset, const int32_t *row_token,
+                            const uint16_t *x_rows, uint16_t *out, uint16_t *gs, uint16_t *us,
+                            int *status, cudaStream_t st) {
     const size_t smem = smem_bytes_pair(N);
     static PerDeviceOnce smem_attr;
     if (!device_once(smem_attr, [] {
@@ -469,7 +518,7 @@ moe_status launch_gemm_pair(const CUtensorMap &a, const CUtensorMap &b0, const C
     const int64_t pairs = std::min<int64_t>(num_sms() / 2, std::max<int64_t>(max_units, 1));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(2 * pairs));
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(pair_threads<GATHER>());
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
@@ -481,7 +530,7 @@ moe_status launch_gemm_pair(const CUtensorMap &a, const CUtensorMap &b0, const C
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     if (cudaLaunchKernelEx(&cfg, grouped_gemm_pair<EPI, GATHER>, a, b0, b1, o, og, ou, N, Kdim,
-                           Nout, count, offset, row_token, out, gs, us, status) != cudaSuccess)
+                           Nout, count, offset, row_token, x_rows, out, gs, us, status) != cudaSuccess)
         return MOE_ERR_CUDA;
     return launch_status();
 }
@@ -544,11 +593,11 @@ MOE_API moe_status moe_expert_ffn(const moe_shape *s, const moe_bf16 *x_disp,
     const int max_row_tiles = (int)((rows + BM - 1) / BM + s->N);
     r = launch_gemm_pair<EPI_SWIGLU, false>(ma, mg, mu, oh, og, ou, s->N, s->d, s->h,
                                             max_row_tiles, expert_count, expert_offset, nullptr,
-                                            h_act, g_save, u_save, status, stream);
+                                            nullptr, h_act, g_save, u_save, status, stream);
     if (r != MOE_OK) return r;
     return launch_gemm_pair<EPI_STORE, false>(mh, md, md, oy, oy, oy, s->N, s->h, s->d,
                                               max_row_tiles, expert_count, expert_offset, nullptr,
-                                              y_disp, nullptr, nullptr, status, stream);
+                                              nullptr, y_disp, nullptr, nullptr, status, stream);
 }
 
 MOE_API size_t moe_expert_ffn_gather_workspace_bytes(const moe_shape *s) {
@@ -601,10 +650,11 @@ MOE_API moe_status moe_expert_ffn_gather(const moe_shape *s, const moe_bf16 *x,
     const int64_t rows = std::min<int64_t>(R, routes);
     const int max_row_tiles = (int)((rows + BM - 1) / BM + s->N);
     r = launch_gemm_pair<EPI_SWIGLU, true>(mx, mg, mu, oh, og, ou, s->N, s->d, s->h, max_row_tiles,
-                                           expert_count, expert_offset, row_token, h_act, g_save,
+                                           expert_count, expert_offset, row_token,
+                                           reinterpret_cast<const uint16_t *>(x), h_act, g_save,
                                            u_save, status, stream);
     if (r != MOE_OK) return r;
     return launch_gemm_pair<EPI_STORE, false>(mh, md, md, oy, oy, oy, s->N, s->h, s->d,
                                               max_row_tiles, expert_count, expert_offset, nullptr,
-                                              y_disp, nullptr, nullptr, status, stream);
+                                              nullptr, y_disp, nullptr, nullptr, status, stream);
 }

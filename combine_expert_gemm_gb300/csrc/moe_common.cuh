@@ -344,16 +344,34 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// The same test with acquire semantics at cluster scope, for a phase that
+// other CTAs of the cluster complete with release arrivals covering their
+// own shared-memory writes.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete.  Returns false (and
 // records MOE_ERR_DEVICE_TIMEOUT in *status) if it has not completed within
 // limit_ns (kWaitLimitNs by default), or at once if *abort is already set.
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int *status,
                                           volatile int *abort,
                                           unsigned long long limit_ns = kWaitLimitNs) {
-    if (mbar_try_wait(bar, parity)) return true;
+    auto test = [&] {
+        return CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+    };
+    if (test()) return true;
     unsigned long long t0 = global_ns();
     for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (test()) return true;
         if ((i & 63u) == 0) {
             if (*abort) return false;
             if (global_ns() - t0 > limit_ns) {
