@@ -207,9 +207,107 @@ dispatch_mx_rows(int T, int d, int K, int N, const uint4 *__restrict__ x,
 // Combine: one warp per token, a lane owns 16 consecutive columns of a
 // 512-column step; y[t] = bf16(sum_k gate_k * deq(row_k)) with an fp32 FMA
 // chain over k ascending (each dequantized value e4m3 * 2^(s - 127) is exact).
+// For K <= 4 the token's accepted routes are first compacted to lanes
+// 0..nv-1 (k ascending) and each pass covers two steps per lane, so 8 code
+// loads per lane are in flight with 4 accepted routes (the K > 4 kernel
+// below keeps one step of all K routes in flight instead: two steps of 8
+// rows would need more registers than the occupancy allows).
+__device__ __forceinline__ void mx_fma16(float (&acc)[16], float g, uint4 code, uint32_t sc) {
+    const float s = e8m0_value(sc);
+    const uint32_t w[4] = {code.x, code.y, code.z, code.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float2 lo = e4m3x2_to_f32((uint16_t)(w[j] & 0xFFFFu));
+        const float2 hi = e4m3x2_to_f32((uint16_t)(w[j] >> 16));
+        acc[4 * j] = fmaf(g, lo.x * s, acc[4 * j]);
+        acc[4 * j + 1] = fmaf(g, lo.y * s, acc[4 * j + 1]);
+        acc[4 * j + 2] = fmaf(g, hi.x * s, acc[4 * j + 2]);
+        acc[4 * j + 3] = fmaf(g, hi.y * s, acc[4 * j + 3]);
+    }
+}
+
+__device__ __forceinline__ void store_bf16x16(uint4 *dst, const float (&acc)[16]) {
+    dst[0] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                        pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+    dst[1] = make_uint4(pack_bf16x2(acc[8], acc[9]), pack_bf16x2(acc[10], acc[11]),
+                        pack_bf16x2(acc[12], acc[13]), pack_bf16x2(acc[14], acc[15]));
+}
+
 template <int MAXK>
 __global__ void __launch_bounds__(kMxThreads)
 combine_mx_rows(int T, int d, int K, const uint4 *__restrict__ yq, const uint8_t *__restrict__ ys,
+                const int32_t *__restrict__ route_row, const float *__restrict__ gate,
+                uint4 *__restrict__ y) {
+    pdl_enter();
+    const int lane = threadIdx.x & 31;
+    const int64_t q16 = d / 16;
+    const int64_t y8 = d / 8;
+    const int sc_row = d / 32;
+    for (int t = blockIdx.x * kMxWarps + (threadIdx.x >> 5); t < T; t += gridDim.x * kMxWarps) {
+        const int32_t my_row = lane < K ? route_row[(int64_t)t * K + lane] : -1;
+        const float my_g = lane < K ? gate[(int64_t)t * K + lane] : 0.0f;
+        // lane j < nv gets the j-th accepted route (k ascending)
+        int32_t rc = -1;
+        float gc = 0.0f;
+        int nv = 0;  // warp-uniform
+#pragma unroll
+        for (int k = 0; k < MAXK; ++k) {
+            const int32_t r = __shfl_sync(0xFFFFFFFFu, my_row, k);
+            const float g = __shfl_sync(0xFFFFFFFFu, my_g, k);
+            if (k < K && r >= 0) {
+                if (lane == nv) {
+                    rc = r;
+                    gc = g;
+                }
+                ++nv;
+            }
+        }
+        for (int c0 = 0; c0 < d; c0 += 2 * kDispStep) {  // warp-uniform
+            const int ca = c0 + lane * 16, cb = ca + kDispStep;
+            float acc[2][16];
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int i = 0; i < 16; ++i) acc[h][i] = 0.0f;
+#pragma unroll
+            for (int g0 = 0; g0 < MAXK; g0 += 4) {
+                if (g0 >= nv) break;
+                float gg[4];
+                uint4 code[4][2];
+                uint32_t sc[4][2];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int32_t r = __shfl_sync(0xFFFFFFFFu, rc, g0 + u);
+                    gg[u] = __shfl_sync(0xFFFFFFFFu, gc, g0 + u);
+                    if (g0 + u < nv) {
+                        if (ca < d) {
+                            code[u][0] = __ldcs(yq + (int64_t)r * q16 + ca / 16);
+                            sc[u][0] = ys[(int64_t)r * sc_row + ca / 32];
+                        }
+                        if (cb < d) {
+                            code[u][1] = __ldcs(yq + (int64_t)r * q16 + cb / 16);
+                            sc[u][1] = ys[(int64_t)r * sc_row + cb / 32];
+                        }
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    if (g0 + u >= nv) continue;
+                    if (ca < d) mx_fma16(acc[0], gg[u], code[u][0], sc[u][0]);
+                    if (cb < d) mx_fma16(acc[1], gg[u], code[u][1], sc[u][1]);
+                }
+            }
+            if (ca < d) store_bf16x16(y + (int64_t)t * y8 + ca / 8, acc[0]);
+            if (cb < d) store_bf16x16(y + (int64_t)t * y8 + cb / 8, acc[1]);
+        }
+    }
+}
+
+// Combine for K > 4: one 512-column step per pass, all K route rows of the
+// step in flight (the same fp32 FMA chain over k ascending).
+template <int MAXK>
+__global__ void __launch_bounds__(kMxThreads)
+combine_mx_rows_wide_k(int T, int d, int K, const uint4 *__restrict__ yq, const uint8_t *__restrict__ ys,
                 const int32_t *__restrict__ route_row, const float *__restrict__ gate,
                 uint4 *__restrict__ y) {
     pdl_enter();
@@ -319,7 +417,9 @@ MOE_API moe_status moe_combine_mxfp8(const moe_shape *s, const uint8_t *y_q, con
     if (!aligned16(y_q) || !aligned16(y_scale) || !aligned16(route_row) || !aligned16(topk_gate) ||
         !aligned16(y))
         return MOE_ERR_ALIGNMENT;
-    auto *kern = s->K <= 8 ? combine_mx_rows<8> : combine_mx_rows<16>;
+    auto *kern = s->K <= 4   ? combine_mx_rows<4>
+                 : s->K <= 8 ? combine_mx_rows_wide_k<8>
+                             : combine_mx_rows_wide_k<16>;
     launch_pdl(kern, mx_grid(s->T), kMxThreads, 0, stream, s->T, s->d, s->K,
                reinterpret_cast<const uint4 *>(y_q), y_scale, route_row, topk_gate,
                reinterpret_cast<uint4 *>(y));
