@@ -31,6 +31,12 @@
 // them round-robin.  Rows past an expert's count (the next expert's rows or
 // the tail) enter the MMA but are never stored; column tiles past the output
 // width are never stored either.  No host round trip, no per-expert launch.
+// Swap tiles: an expert's last row tile with at most 128 valid rows (all of a
+// small expert's rows, or a large expert's remainder) runs with the operands
+// exchanged -- A = 256 weight rows, B = the tile's token rows rounded up to 32
+// -- so the MMA computes those few columns instead of 256 rows; the
+// accumulator then holds the outputs transposed (lane = output column, TMEM
+// column = token) and they are stored token by token.
 #include <algorithm>
 
 #include "moe_common.cuh"
@@ -193,6 +199,97 @@ __device__ __forceinline__ void epilogue_tile_tma(uint32_t tbase, int half, int 
     }
 }
 
+// ---------------------------------------------------------- swap-AB tiles
+//
+// An expert's last tile with at most SWAP_MAX valid rows runs as M = 256
+// weight rows (128 per CTA) by N = n_sw token columns (the valid rows rounded
+// up to 32; the leader holds tokens 0..n_sw/2-1, the peer the rest).  F1: each
+// CTA's 128 A rows are the gate rows (0-63) and the up rows (64-127) of the
+// same 64 hidden units, loaded as two 64-row boxes; the up values of TMEM lane
+// quadrants 2-3 reach the gate lanes of quadrants 0-1 through the up warp's
+// staging block (a named barrier per warp pair).  F2: each CTA's A rows are
+// 128 rows of W_down (output features).  Few, large TMA boxes per stage
+// matter: the copy engine's cost is per request.
+constexpr int SWAP_MAX = 128;
+constexpr int SW_BOX = 32;  // token rows per B load of a swap tile
+
+__device__ __forceinline__ int swap_cols(int rows) { return (rows + 31) & ~31; }
+
+__device__ __forceinline__ uint16_t bf16_bits(float v) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// F1 epilogue of a swap tile for one warp of a gate/up warp pair: accumulator
+// columns (tokens) [c0, c1).  An up warp (quadrant 2-3) passes its values
+// through `xbuf` (its own 2 KB staging block); the gate warp (quadrant 0-1)
+// computes H = silu(G) * U for hidden unit `hid` and stores it per token.
+__device__ __forceinline__ void epilogue_swap_swiglu(uint32_t tbase, int c0, int c1,
+                                                     int rows_valid, int64_t row0, bool gate_warp,
+                                                     float *xbuf, int bar_id, int hid, int Nout,
+                                                     int lane, uint16_t *__restrict__ out,
+                                                     uint16_t *__restrict__ g_save,
+                                                     uint16_t *__restrict__ u_save) {
+    if (!gate_warp) {
+        if (lane == 0) bulk_wait_read<0>();  // an earlier TMA store from the block is done
+        __syncwarp();
+    }
+    for (int c = c0; c < c1; c += 16) {
+        uint32_t v[16];
+        tmem_ld16(tbase + c, v);
+        tmem_ld_wait();
+        reg_fence(v);
+        if (!gate_warp) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) xbuf[i * 32 + lane] = __uint_as_float(v[i]);
+            named_bar_sync(bar_id, 64);  // up values ready
+            named_bar_sync(bar_id, 64);  // gate warp done reading
+            continue;
+        }
+        float u[16];
+        named_bar_sync(bar_id, 64);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) u[i] = xbuf[i * 32 + lane];
+        named_bar_sync(bar_id, 64);
+        if (hid < Nout) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                if (c + i >= rows_valid) break;
+                const float g = __uint_as_float(v[i]);
+                const int64_t at = (row0 + c + i) * Nout + hid;
+                out[at] = bf16_bits(__fdividef(g, 1.0f + __expf(-g)) * u[i]);
+                if (g_save) {
+                    g_save[at] = bf16_bits(g);
+                    u_save[at] = bf16_bits(u[i]);
+                }
+            }
+        }
+    }
+}
+
+// F2 epilogue of a swap tile for one warp: output feature `feat` of this lane,
+// accumulator columns (tokens) [c0, c1).
+__device__ __forceinline__ void epilogue_swap_store(uint32_t tbase, int c0, int c1,
+                                                    int rows_valid, int64_t row0, int feat,
+                                                    int Nout, uint16_t *__restrict__ out) {
+    for (int c = c0; c < c1; c += 16) {
+        uint32_t v[16];
+        tmem_ld16(tbase + c, v);
+        tmem_ld_wait();
+        reg_fence(v);
+        if (feat < Nout) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                if (c + i >= rows_valid) break;
+                out[(row0 + c + i) * Nout + feat] = bf16_bits(__uint_as_float(v[i]));
+            }
+        }
+    }
+}
+
 // ------------------------------------------------------------ CTA-pair kernel
 //
 // Two CTAs of a cluster compute one 256-row x 256-column tile with
@@ -221,9 +318,11 @@ struct alignas(8) PairBars {
 
 constexpr int P_STG_BYTES = P_EPI_WARPS * 2048;  // one 32 x 32 bf16 store block per epilogue warp
 
+// ... + tile_start [N + 1] and the expert counts [N] (copied once, so that the
+// MMA issuer reads no global memory between tiles)
 constexpr size_t smem_bytes_pair(int N) {
     return 1024 + (size_t)P_STAGES * P_STAGE_BYTES + P_STG_BYTES + sizeof(PairBars) +
-           sizeof(int32_t) * (N + 1) + 16;
+           sizeof(int32_t) * (2 * N + 1) + 16;
 }
 
 // GATHER: A is not the packed buffer but the token rows themselves.  The two
@@ -246,11 +345,17 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
+// Swap tiles: tm_sa0 / tm_sa1 are the A maps of a swap tile (F1: W_gate and
+// W_up with 64-row boxes; F2: W_down with 128-row boxes, tm_sa1 unused) and
+// tm_sb the B map (the packed rows with 32-row boxes).  GATHER runs no swap
+// tiles.
 template <int EPI, bool GATHER>
 __global__ void __launch_bounds__(pair_threads<GATHER>(), 1)
 grouped_gemm_pair(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b0,
                   const __grid_constant__ CUtensorMap tm_b1, const __grid_constant__ CUtensorMap tm_o,
                   const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_u,
+                  const __grid_constant__ CUtensorMap tm_sa0, const __grid_constant__ CUtensorMap tm_sa1,
+                  const __grid_constant__ CUtensorMap tm_sb,
                   int N, int Kdim, int Nout,
                   const int32_t *__restrict__ count, const int32_t *__restrict__ offset,
                   const int32_t *__restrict__ row_token, const uint16_t *__restrict__ x_rows,
@@ -259,12 +364,14 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tm_a, const __grid_constan
     pdl_enter();
     constexpr int BN_OUT = EPI == EPI_SWIGLU ? MMA_N / 2 : MMA_N;
     constexpr int PM = 2 * BM;  // rows per pair tile
+    constexpr bool kSwap = !GATHER;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t *stage_out = smem + (size_t)P_STAGES * P_STAGE_BYTES;  // [8 warps][2 KB]
     PairBars *bars = reinterpret_cast<PairBars *>(stage_out + P_STG_BYTES);
     int32_t *tile_start = reinterpret_cast<int32_t *>(bars + 1);
+    int32_t *cnt = tile_start + N + 1;  // expert_count, copied
     volatile int *abort = &bars->abort;
     const uint32_t rank = cluster_rank();
     const bool leader = rank == 0;
@@ -292,7 +399,9 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tm_a, const __grid_constan
         int carry = 0;
         for (int base = 0; base < N; base += 32) {
             const int e = base + lane;
-            const int v = e < N ? ((count[e] + PM - 1) / PM) * ntn : 0;
+            const int c = e < N ? count[e] : 0;
+            if (e < N) cnt[e] = c;
+            const int v = ((c + PM - 1) / PM) * ntn;
             int incl = v;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
@@ -319,7 +428,7 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tm_a, const __grid_constan
             if (tile_start[mid] <= g) lo = mid;
             else hi = mid - 1;
         }
-        const int mt = (count[lo] + PM - 1) / PM;
+        const int mt = (cnt[lo] + PM - 1) / PM;
         const int local = g - tile_start[lo];
         return TileMap{lo, local % mt, local / mt};
     };
@@ -335,6 +444,10 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tm_a, const __grid_constan
             bool ok = true;
             for (int g = unit0; g < total && ok; g += units) {
                 const TileMap t = map_pair(g);
+                const int rows_valid = cnt[t.e] - t.m * PM;
+                const bool swap = kSwap && rows_valid <= SWAP_MAX;
+                const int n_sw = swap_cols(rows_valid);
+                const int sw_loads = (n_sw / 2 + SW_BOX - 1) / SW_BOX;
                 const int a_row = offset[t.e] + t.m * PM + (int)rank * BM;
                 const int b_row = EPI == EPI_SWIGLU ? t.e * Nout + t.n * BN_OUT
                                                     : t.e * Nout + t.n * BN_OUT + (int)rank * (MMA_N / 2);
@@ -348,10 +461,28 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tm_a, const __grid_constan
                     const uint32_t full = cluster_map(own_full, 0);
                     const uint32_t sa = smem_u32(smem + (size_t)stage * P_STAGE_BYTES);
                     const uint32_t sb = sa + A_BYTES;
-                    if (leader)
-                        mbar_arrive_expect_tx(own_full, GATHER ? 2 * P_B_BYTES : 2 * P_STAGE_BYTES);
-                    if (!GATHER) tma_load_2d_pair(sa, &tm_a, full, kb * BK, a_row);
-                    tma_load_2d_pair(sb, mb, full, kb * BK, b_row);
+                    if (swap) {
+                        if (leader)
+                            mbar_arrive_expect_tx(own_full, 2 * (A_BYTES + sw_loads * SW_BOX * BK * 2));
+                        if (EPI == EPI_SWIGLU) {
+                            const int hrow = t.e * Nout + t.n * BN_OUT + 64 * (int)rank;
+                            tma_load_2d_pair(sa, &tm_sa0, full, kb * BK, hrow);
+                            tma_load_2d_pair(sa + 64 * 128, &tm_sa1, full, kb * BK, hrow);
+                        } else {
+                            tma_load_2d_pair(sa, &tm_sa0, full, kb * BK,
+                                             t.e * Nout + t.n * MMA_N + BM * (int)rank);
+                        }
+                        const int trow = offset[t.e] + t.m * PM + (int)rank * (n_sw / 2);
+                        for (int i = 0; i < sw_loads; ++i)
+                            tma_load_2d_pair(sb + (uint32_t)(i * SW_BOX) * 128, &tm_sb, full,
+                                             kb * BK, trow + i * SW_BOX);
+                    } else {
+                        if (leader)
+                            mbar_arrive_expect_tx(own_full,
+                                                  GATHER ? 2 * P_B_BYTES : 2 * P_STAGE_BYTES);
+                        if (!GATHER) tma_load_2d_pair(sa, &tm_a, full, kb * BK, a_row);
+                        tma_load_2d_pair(sb, mb, full, kb * BK, b_row);
+                    }
                     ++issued;
                     if (++stage == P_STAGES) { stage = 0; phase ^= 1; }
                 }
@@ -400,6 +531,12 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tm_a, const __grid_constan
             uint32_t acc_phase = 0;
             bool ok = true;
             for (int g = unit0; g < total && ok; g += units) {
+                uint32_t tdesc = idesc;
+                if (kSwap) {
+                    const TileMap t = map_pair(g);
+                    const int rows_valid = cnt[t.e] - t.m * PM;
+                    if (rows_valid <= SWAP_MAX) tdesc = idesc_bf16_f32(PM, swap_cols(rows_valid));
+                }
                 if (!mbar_wait(smem_u32(&bars->tempty[acc]), acc_phase ^ 1, status, abort)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * ACC_COLS);
@@ -415,7 +552,7 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tm_a, const __grid_constan
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
                         tc_mma_bf16_pair(d_tmem, sw128_kmajor_desc(sa + kk * 32),
-                                         sw128_kmajor_desc(sb + kk * 32), idesc,
+                                         sw128_kmajor_desc(sb + kk * 32), tdesc,
                                          (kb | kk) != 0 ? 1u : 0u);
                     }
                     tc_commit_pair(smem_u32(&bars->empty[stage]));
@@ -436,7 +573,7 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tm_a, const __grid_constan
         for (int g = unit0; g < total && ok; g += units) {
             const TileMap t = map_pair(g);
             const int a_row = offset[t.e] + t.m * PM + (int)rank * BM;
-            const int valid_end = offset[t.e] + count[t.e];
+            const int valid_end = offset[t.e] + cnt[t.e];
             const uint16_t *src[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
@@ -469,13 +606,30 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tm_a, const __grid_constan
         uint32_t acc_phase = 0;
         for (int g = unit0; g < total; g += units) {
             const TileMap t = map_pair(g);
-            const int rows_valid = count[t.e] - t.m * PM;
+            const int rows_valid = cnt[t.e] - t.m * PM;
             const bool row_ok = row_in_tile < rows_valid;
             const int64_t row = (int64_t)offset[t.e] + t.m * PM + row_in_tile;
             if (!mbar_wait(smem_u32(&bars->tfull[acc]), acc_phase, status, abort)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + acc * ACC_COLS;
-            if (rows_valid - (row_in_tile - lane) >= 32)  // all 32 rows of this warp are valid
+            if (kSwap && rows_valid <= SWAP_MAX) {
+                const int n_sw = swap_cols(rows_valid);
+                const int c0 = half * (n_sw / 2), c1 = c0 + n_sw / 2;
+                const int64_t row0 = (int64_t)offset[t.e] + t.m * PM;
+                if (EPI == EPI_SWIGLU) {
+                    // gate warps (quadrants 0-1) pair with the up warps two below them
+                    const bool gate_warp = quad < 2;
+                    const int xwarp = gate_warp ? warp - 2 : warp;
+                    epilogue_swap_swiglu(tbase, c0, c1, rows_valid, row0, gate_warp,
+                                         reinterpret_cast<float *>(stage_out + (xwarp - 2) * 2048),
+                                         1 + (quad & 1) + 2 * half,
+                                         t.n * BN_OUT + 64 * (int)rank + 32 * (quad & 1) + lane,
+                                         Nout, lane, out, g_save, u_save);
+                } else {
+                    epilogue_swap_store(tbase, c0, c1, rows_valid, row0,
+                                        t.n * MMA_N + BM * (int)rank + 32 * quad + lane, Nout, out);
+                }
+            } else if (rows_valid - (row_in_tile - lane) >= 32)  // all 32 rows of this warp are valid
                 epilogue_tile_tma<EPI>(tbase, half, (int)(row - lane), t.n, Nout,
                                        stage_out + (warp - 2) * 2048, &tm_o, &tm_g, &tm_u,
                                        g_save != nullptr, lane);
@@ -503,6 +657,7 @@ grouped_gemm_pair(const __grid_constant__ CUtensorMap tm_a, const __grid_constan
 template <int EPI, bool GATHER>
 moe_status launch_gemm_pair(const CUtensorMap &a, const CUtensorMap &b0, const CUtensorMap &b1,
                             const CUtensorMap &o, const CUtensorMap &og, const CUtensorMap &ou,
+                            const CUtensorMap &sa0, const CUtensorMap &sa1, const CUtensorMap &sb,
                             int N, int Kdim, int Nout, int max_row_tiles, const int32_t *count,
                             const int32_t *offset, const int32_t *row_token,
                             const uint16_t *x_rows, uint16_t *out, uint16_t *gs, uint16_t *us,
@@ -529,8 +684,9 @@ moe_status launch_gemm_pair(const CUtensorMap &a, const CUtensorMap &b0, const C
     set_pdl_attr(attr[1]);
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    if (cudaLaunchKernelEx(&cfg, grouped_gemm_pair<EPI, GATHER>, a, b0, b1, o, og, ou, N, Kdim,
-                           Nout, count, offset, row_token, x_rows, out, gs, us, status) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, grouped_gemm_pair<EPI, GATHER>, a, b0, b1, o, og, ou, sa0, sa1,
+                           sb, N, Kdim, Nout, count, offset, row_token, x_rows, out, gs, us,
+                           status) != cudaSuccess)
         return MOE_ERR_CUDA;
     return launch_status();
 }
@@ -588,16 +744,23 @@ MOE_API moe_status moe_expert_ffn(const moe_shape *s, const moe_bf16 *x_disp,
         !make_map_bf16_store(&og, g_save ? g_save : h_act, s->h, R) ||
         !make_map_bf16_store(&ou, u_save ? u_save : h_act, s->h, R))
         return MOE_ERR_CUDA;
+    // swap tiles: weights by 64 (F1) or 128 (F2, md) rows, packed rows by 32
+    CUtensorMap sg, su, sx, sh;
+    if (!make_map(&sg, w_gate, s->d, (uint64_t)s->N * s->h, 64) ||
+        !make_map(&su, w_up, s->d, (uint64_t)s->N * s->h, 64) ||
+        !make_map(&sx, x_disp, s->d, R, SW_BOX) || !make_map(&sh, h_act, s->h, R, SW_BOX))
+        return MOE_ERR_CUDA;
     int *status = static_cast<int *>(ws);
     const int64_t rows = std::min<int64_t>(R, (int64_t)s->T * s->K);
     const int max_row_tiles = (int)((rows + BM - 1) / BM + s->N);
-    r = launch_gemm_pair<EPI_SWIGLU, false>(ma, mg, mu, oh, og, ou, s->N, s->d, s->h,
+    r = launch_gemm_pair<EPI_SWIGLU, false>(ma, mg, mu, oh, og, ou, sg, su, sx, s->N, s->d, s->h,
                                             max_row_tiles, expert_count, expert_offset, nullptr,
                                             nullptr, h_act, g_save, u_save, status, stream);
     if (r != MOE_OK) return r;
-    return launch_gemm_pair<EPI_STORE, false>(mh, md, md, oy, oy, oy, s->N, s->h, s->d,
-                                              max_row_tiles, expert_count, expert_offset, nullptr,
-                                              nullptr, y_disp, nullptr, nullptr, status, stream);
+    return launch_gemm_pair<EPI_STORE, false>(mh, md, md, oy, oy, oy, md, md, sh, s->N, s->h,
+                                              s->d, max_row_tiles, expert_count, expert_offset,
+                                              nullptr, nullptr, y_disp, nullptr, nullptr, status,
+                                              stream);
 }
 
 MOE_API size_t moe_expert_ffn_gather_workspace_bytes(const moe_shape *s) {
@@ -649,12 +812,16 @@ MOE_API moe_status moe_expert_ffn_gather(const moe_shape *s, const moe_bf16 *x,
     if ((r = launch_status()) != MOE_OK) return r;
     const int64_t rows = std::min<int64_t>(R, routes);
     const int max_row_tiles = (int)((rows + BM - 1) / BM + s->N);
-    r = launch_gemm_pair<EPI_SWIGLU, true>(mx, mg, mu, oh, og, ou, s->N, s->d, s->h, max_row_tiles,
+    CUtensorMap sh;
+    if (!make_map(&sh, h_act, s->h, R, SW_BOX)) return MOE_ERR_CUDA;
+    r = launch_gemm_pair<EPI_SWIGLU, true>(mx, mg, mu, oh, og, ou, mg, mu, mx, s->N, s->d, s->h,
+                                           max_row_tiles,
                                            expert_count, expert_offset, row_token,
                                            reinterpret_cast<const uint16_t *>(x), h_act, g_save,
                                            u_save, status, stream);
     if (r != MOE_OK) return r;
-    return launch_gemm_pair<EPI_STORE, false>(mh, md, md, oy, oy, oy, s->N, s->h, s->d,
-                                              max_row_tiles, expert_count, expert_offset, nullptr,
-                                              nullptr, y_disp, nullptr, nullptr, status, stream);
+    return launch_gemm_pair<EPI_STORE, false>(mh, md, md, oy, oy, oy, md, md, sh, s->N, s->h,
+                                              s->d, max_row_tiles, expert_count, expert_offset,
+                                              nullptr, nullptr, y_disp, nullptr, nullptr, status,
+                                              stream);
 }
