@@ -314,9 +314,8 @@ grouped_dgrad_pair(const __grid_constant__ CUtensorMap tm_a0, const __grid_const
                     const int kk = up ? kb - hb : kb;
                     const int brow = MODE == DGRAD_DH ? t.e * p.d + kb * BK : t.e * p.h + kk * BK;
                     tma_load_2d_pair(sa, up ? &tm_a1 : &tm_a0, full, kk * BK, a_row);
-                    for (int q = 0; q < 2; ++q)
-                        tma_load_2d_pair(sb + q * BLK, up ? &tm_b1 : &tm_b0, full, ncol + 64 * q,
-                                         brow);
+                    // both 64-column blocks of this CTA's half of B (make_map_mn2)
+                    tma_load_3d_pair(sb, up ? &tm_b1 : &tm_b0, full, 0, brow, ncol / 64);
                     ++issued;
                     if (++stage == P_STAGES) { stage = 0; phase ^= 1; }
                 }
@@ -557,19 +556,16 @@ grouped_wgrad_pair(const __grid_constant__ CUtensorMap tm_a0, const __grid_const
                     if (kb == nk - 1) {
                         const uint32_t bar = smem_u32(&bars->lastfull[stage]);
                         mbar_arrive_expect_tx(bar, P_STAGE_BYTES);
-                        for (int q = 0; q < 2; ++q) tma_load_2d(sa + q * BLK, ma, bar, mcol + 64 * q, row);
-                        for (int q = 0; q < 2; ++q)
-                            tma_load_2d(sb + q * BLK, &tm_b0, bar, ncol + 64 * q, row);
+                        tma_load_3d(sa, ma, bar, 0, row, mcol / 64);
+                        tma_load_3d(sb, &tm_b0, bar, 0, row, ncol / 64);
                         par_last ^= 1u << stage;
                         last_kind |= 1u << stage;
                     } else {
                         const uint32_t own_full = smem_u32(&bars->full[stage]);
                         const uint32_t full = cluster_map(own_full, 0);
                         if (leader) mbar_arrive_expect_tx(own_full, 2 * P_STAGE_BYTES);
-                        for (int q = 0; q < 2; ++q)
-                            tma_load_2d_pair(sa + q * BLK, ma, full, mcol + 64 * q, row);
-                        for (int q = 0; q < 2; ++q)
-                            tma_load_2d_pair(sb + q * BLK, &tm_b0, full, ncol + 64 * q, row);
+                        tma_load_3d_pair(sa, ma, full, 0, row, mcol / 64);
+                        tma_load_3d_pair(sb, &tm_b0, full, 0, row, ncol / 64);
                         par_full ^= 1u << stage;
                         last_kind &= ~(1u << stage);
                     }
@@ -620,8 +616,10 @@ grouped_wgrad_pair(const __grid_constant__ CUtensorMap tm_a0, const __grid_const
                     bool got;
                     if (kb == nk - 1) {
                         steps = (cnt - kb * BK + 15) / 16;
-                        got = mbar_wait(smem_u32(&bars->ready[stage]), stage_parity(par_ready, stage),
-                                        status, abort);
+                        // both fixers zeroed rows with ordinary stores and
+                        // arrived with release at cluster scope: acquire there
+                        got = mbar_wait<true>(smem_u32(&bars->ready[stage]),
+                                              stage_parity(par_ready, stage), status, abort);
                         par_ready ^= 1u << stage;
                     } else {
                         got = mbar_wait(smem_u32(&bars->full[stage]), stage_parity(par_full, stage),
@@ -838,12 +836,15 @@ MOE_API moe_status moe_expert_ffn_backward(
 
     CUtensorMap dy_k, wd_mn, dg_k, du_k, wg_mn, wu_mn, dy_mn, h_mn, dg_mn, du_mn, x_mn;
     const uint64_t Nd = (uint64_t)s->N * s->d, Nh = (uint64_t)s->N * s->h;
-    if (!make_map(&dy_k, dy_disp, s->d, R, BM) || !make_map(&wd_mn, w_down, s->h, Nd, 64) ||
-        !make_map(&dg_k, dG, s->h, R, BM) || !make_map(&du_k, dU, s->h, R, BM) ||
-        !make_map(&wg_mn, w_gate, s->d, Nh, 64) || !make_map(&wu_mn, w_up, s->d, Nh, 64) ||
-        !make_map(&dy_mn, dy_disp, s->d, R, 64) || !make_map(&h_mn, h_act, s->h, R, 64) ||
-        !make_map(&dg_mn, dG, s->h, R, 64) || !make_map(&du_mn, dU, s->h, R, 64) ||
-        !make_map(&x_mn, x_disp, s->d, R, 64))
+    // MN-major operands as 3-D two-block maps (d and h are multiples of 64
+    // here): each CTA's two 64-column blocks of a k-block arrive by one request
+    // instead of two, about 1% off the expert backward on the training layer
+    if (!make_map(&dy_k, dy_disp, s->d, R, BM) || !make_map(&dg_k, dG, s->h, R, BM) ||
+        !make_map(&du_k, dU, s->h, R, BM) || !make_map_mn2(&wd_mn, w_down, s->h, Nd, 64) ||
+        !make_map_mn2(&wg_mn, w_gate, s->d, Nh, 64) || !make_map_mn2(&wu_mn, w_up, s->d, Nh, 64) ||
+        !make_map_mn2(&dy_mn, dy_disp, s->d, R, 64) || !make_map_mn2(&h_mn, h_act, s->h, R, 64) ||
+        !make_map_mn2(&dg_mn, dG, s->h, R, 64) || !make_map_mn2(&du_mn, dU, s->h, R, 64) ||
+        !make_map_mn2(&x_mn, x_disp, s->d, R, 64))
         return MOE_ERR_CUDA;
     CUtensorMap o_dg, o_du, o_dx;
     if (!make_map_bf16_store(&o_dg, dG, s->h, R) || !make_map_bf16_store(&o_du, dU, s->h, R) ||
