@@ -44,6 +44,49 @@ constexpr int MMA_N = 256;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = MMA_N * BK * 2;
 constexpr int BLK = 64 * BK * 2;  // one MN-major 64 x 64 block: 8 KB
+
+// 3-D view of a row-major [rows, inner] bf16 matrix (inner a multiple
+// of 64) as [inner / 64 blocks][rows][64]: one box of 64 x box_rows x 2
+// blocks lands two 64-column blocks of box_rows rows, each 128-byte
+// swizzled, exactly where two boxes of make_map at columns x and x + 64 would
+// (the swizzle follows the smem row, and a block is a whole number of 8-row
+// groups), with one request instead of two.  A block index past the last
+// reads as zeros.  Returns false if inner is not a multiple of 64 or the
+// driver refuses the map.
+inline bool make_map_mn2(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows,
+                         uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || inner % 64 != 0) return false;
+    const cuuint64_t dims[3] = {64, rows, inner / 64};
+    const cuuint64_t strides[2] = {inner * 2, 128};
+    const cuuint32_t box[3] = {64, box_rows, 2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Loads of a 3-D map (make_map_mn2): block z and z + 1 of rows y.., into
+// this CTA's shared memory, completing on bar (this CTA's) or, for the pair
+// form, on the leader's barrier (a cluster address).
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int32_t x, int32_t y, int32_t z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap *map,
+                                                 uint32_t bar, int32_t x, int32_t y, int32_t z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
 constexpr int ACC_COLS = 256;
 constexpr int TMEM_COLS = 512;
 
