@@ -67,17 +67,9 @@ inline bool make_map_mn2(CUtensorMap *m, const void *base, uint64_t inner, uint6
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Loads of a 3-D map (make_map_mn2): block z and z + 1 of rows y.., into
-// this CTA's shared memory, completing on bar (this CTA's) or, for the pair
-// form, on the leader's barrier (a cluster address).
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
-                                            int32_t x, int32_t y, int32_t z) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
-        : "memory");
-}
+// Load of a 3-D map (make_map_mn2): blocks z and z + 1 of rows y.. into this
+// CTA's shared memory, completing on the pair leader's barrier (a cluster
+// address).
 __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap *map,
                                                  uint32_t bar, int32_t x, int32_t y, int32_t z) {
     asm volatile(
@@ -126,6 +118,8 @@ struct Params {
     const uint16_t *g_save, *u_save;  // DGRAD_DH epilogue inputs
     uint16_t *out0, *out1;            // DH: dG, dU; DX: dx_disp
     float *fout0, *fout1;             // wgrad: dW (down) or (gate, up)
+    CUtensorMap *map_slots;           // wgrad: kMapSlots x 2 bounded map copies per CTA
+    int rows;                         // R: rows of every row buffer (the maps' extent)
     int *status;
 };
 
@@ -492,30 +486,32 @@ moe_status launch_dgrad_pair(const CUtensorMap &a0, const CUtensorMap &a1, const
 // dW tiles of 256 output rows x 256 output columns, one tcgen05.mma
 // cta_group::2 per 16 rows of the expert: each CTA holds its own 128 output
 // rows of A and 128 output columns of B, both MN-major (two 64 x 64 blocks
-// each), 32 KB per k-block in the 6-stage ring.  Every k-block but a tile's
-// last completes on the leader's full barrier (both CTAs' copies, as in the
-// dgrad kernel).  A tile's last k-block may be ragged, so each CTA's copy of
-// it completes on that CTA's own barrier; a fixer warp in each CTA then
-// zeroes the invalid rows in its own shared memory, fences them to the async
-// proxy and reports the stage ready on the leader's barrier.  The fixers run
-// while the leader is still busy with the tile's earlier k-blocks, so the
-// repair stays off the MMA issue path.  Stage barriers alternate between the
-// two kinds of use, so each role tracks their phases per stage.
+// each), 32 KB per k-block in the 6-stage ring; both CTAs' copies complete on
+// the leader's full barrier, as in the dgrad kernel.  The reduction runs over
+// the expert's rows, and a tile's last k-block may reach into the next
+// expert's rows or the unwritten tail.  That block is loaded through copies
+// of the two maps whose row extent ends at the expert's last row, so the rows
+// past it arrive as zeros: the producer warp writes the copies into this
+// CTA's ring of kMapSlots global slots (tensormap.replace on a shared-memory
+// copy of the kernel's map, then a release copy to the tensormap proxy) and
+// acquires them before the load.  A slot is rewritten kMapSlots tiles later,
+// when the producer has long since waited for the stage its load filled.
 constexpr int WG_STAGES = 6;
+constexpr int kMapSlots = WG_STAGES + 2;
+constexpr int kMaxWgradCtas = 512;
+constexpr size_t kMapSlotBytes = (size_t)kMaxWgradCtas * kMapSlots * 2 * sizeof(CUtensorMap);
 
-struct alignas(8) WgradBars {
-    uint64_t full[WG_STAGES];      // leader: both CTAs' copies of a k-block landed
-    uint64_t lastfull[WG_STAGES];  // this CTA's copy of a tile's last k-block landed
-    uint64_t ready[WG_STAGES];     // leader: both fixers repaired a last k-block
-    uint64_t empty[WG_STAGES];     // the leader's MMAs are done with the stage
+struct alignas(128) WgradBars {
+    CUtensorMap stage_map[2];   // the producer's copies being bounded (A, B)
+    uint64_t full[WG_STAGES];   // leader: both CTAs' copies of a k-block landed
+    uint64_t empty[WG_STAGES];  // the leader's MMAs are done with the stage
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint32_t tmem_base;
     int abort;
 };
 
-constexpr int WG_THREADS = 64 + kEpiThreads + 32;  // + the fixer warp
-constexpr int WG_FIXER = 2 + P_EPI_WARPS;          // its warp index
+constexpr int WG_THREADS = 64 + kEpiThreads;
 
 constexpr int WG_STG_BYTES = P_EPI_WARPS * 32 * 32 * 4;  // one 32 x 32 fp32 block per warp
 
@@ -523,7 +519,25 @@ constexpr size_t smem_bytes_wgrad_pair() {
     return 1024 + (size_t)WG_STAGES * P_STAGE_BYTES + WG_STG_BYTES + sizeof(WgradBars) + 16;
 }
 
-__device__ __forceinline__ uint32_t stage_parity(uint32_t bits, int s) { return (bits >> s) & 1u; }
+// Row extent (dimension 1) of the map copy at smem address `map`.
+__device__ __forceinline__ void tmap_set_rows(uint32_t map, int rows) {
+    asm volatile("tensormap.replace.tile.global_dim.shared::cta.b1024.b32 [%0], 1, %1;" ::"r"(map),
+                 "r"(rows)
+                 : "memory");
+}
+// The whole warp: copies the 128-byte map at smem `src` to global `dst` and
+// releases it to the tensormap proxy at GPU scope.
+__device__ __forceinline__ void tmap_publish(CUtensorMap *dst, uint32_t src) {
+    asm volatile(
+        "tensormap.cp_fenceproxy.global.shared::cta.tensormap::generic.release.gpu.sync.aligned"
+        " [%0], [%1], 128;" ::"l"(dst),
+        "r"(src)
+        : "memory");
+}
+// The thread about to load through the map at `map` acquires its contents.
+__device__ __forceinline__ void tmap_acquire(const CUtensorMap *map) {
+    asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(map) : "memory");
+}
 
 template <int MODE>
 __global__ void __launch_bounds__(WG_THREADS, 1)
@@ -549,8 +563,6 @@ grouped_wgrad_pair(const __grid_constant__ CUtensorMap tm_a0, const __grid_const
     if (threadIdx.x == 0) {
         for (int s = 0; s < WG_STAGES; ++s) {
             mbar_init(smem_u32(&bars->full[s]), 1);
-            mbar_init(smem_u32(&bars->lastfull[s]), 1);
-            mbar_init(smem_u32(&bars->ready[s]), 2);
             mbar_init(smem_u32(&bars->empty[s]), 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -570,64 +582,72 @@ grouped_wgrad_pair(const __grid_constant__ CUtensorMap tm_a0, const __grid_const
     const int mt_half = (p.h + PM - 1) / PM;  // gate/up: 256-row tiles per half
 
     if (warp == 0) {
-        // ------------------------------------------------------ TMA producer
+        // ------------------------------------- TMA producer (the whole warp
+        // bounds the maps; lane 0 waits and loads)
         if (lane == 0) {
             tma_prefetch_desc(&tm_a0);
             tma_prefetch_desc(&tm_b0);
-            int stage = 0;
-            uint32_t phase = 0;                    // empty barriers: every use
-            uint32_t par_full = 0, par_last = 0;   // next-use parity per stage
-            uint32_t last_kind = 0;                // stage's latest use was a last k-block
-            int issued = 0;
-            bool ok = true;
-            for (int g = unit0; g < total && ok; g += units) {
-                const Tile t = map_wgrad_tile(g, p);
-                const int cnt = p.count[t.e], off = p.offset[t.e];
-                const int nk = k_blocks<MODE>(p, cnt);
-                const bool up = MODE == WGRAD_GATEUP && t.m >= mt_half;
-                const int mcol = (up ? t.m - mt_half : t.m) * PM + (int)rank * BM;
-                const int ncol = t.n * MMA_N + (int)rank * (MMA_N / 2);
-                const CUtensorMap *ma = up ? &tm_a1 : &tm_a0;
+        }
+        CUtensorMap *slots = p.map_slots + (size_t)blockIdx.x * kMapSlots * 2;
+        const uint32_t sm_a = smem_u32(&bars->stage_map[0]), sm_b = smem_u32(&bars->stage_map[1]);
+        int stage = 0;
+        uint32_t phase = 0;
+        int issued = 0, slot = 0;
+        bool ok = true;
+        for (int g = unit0; g < total && ok; g += units) {
+            const Tile t = map_wgrad_tile(g, p);
+            const int cnt = p.count[t.e], off = p.offset[t.e];
+            const int nk = k_blocks<MODE>(p, cnt);
+            if (nk == 0) continue;
+            const bool up = MODE == WGRAD_GATEUP && t.m >= mt_half;
+            const int mcol = (up ? t.m - mt_half : t.m) * PM + (int)rank * BM;
+            const int ncol = t.n * MMA_N + (int)rank * (MMA_N / 2);
+            const CUtensorMap *ma = up ? &tm_a1 : &tm_a0;
+            CUtensorMap *ga = slots + 2 * slot, *gb = ga + 1;
+            if (++slot == kMapSlots) slot = 0;
+            if (lane == 0) {
+                // never past the buffer's own extent, whatever the counts say
+                const int end = max(1, min(off + cnt, p.rows));
+                bars->stage_map[0] = *ma;
+                bars->stage_map[1] = tm_b0;
+                tmap_set_rows(sm_a, end);
+                tmap_set_rows(sm_b, end);
+            }
+            __syncwarp();
+            tmap_publish(ga, sm_a);
+            tmap_publish(gb, sm_b);
+            __syncwarp();
+            if (lane == 0) {
+                tmap_acquire(ga);
+                tmap_acquire(gb);
                 for (int kb = 0; kb < nk; ++kb) {
                     if (!mbar_wait(smem_u32(&bars->empty[stage]), phase ^ 1, status, abort)) {
                         ok = false;
                         break;
                     }
+                    const uint32_t own_full = smem_u32(&bars->full[stage]);
+                    const uint32_t full = cluster_map(own_full, 0);
                     const uint32_t sa = smem_u32(smem + (size_t)stage * P_STAGE_BYTES);
                     const uint32_t sb = sa + A_BYTES;
                     const int row = off + kb * BK;
-                    if (kb == nk - 1) {
-                        const uint32_t bar = smem_u32(&bars->lastfull[stage]);
-                        mbar_arrive_expect_tx(bar, P_STAGE_BYTES);
-                        tma_load_3d(sa, ma, bar, 0, row, mcol / 64);
-                        tma_load_3d(sb, &tm_b0, bar, 0, row, ncol / 64);
-                        par_last ^= 1u << stage;
-                        last_kind |= 1u << stage;
-                    } else {
-                        const uint32_t own_full = smem_u32(&bars->full[stage]);
-                        const uint32_t full = cluster_map(own_full, 0);
-                        if (leader) mbar_arrive_expect_tx(own_full, 2 * P_STAGE_BYTES);
-                        tma_load_3d_pair(sa, ma, full, 0, row, mcol / 64);
-                        tma_load_3d_pair(sb, &tm_b0, full, 0, row, ncol / 64);
-                        par_full ^= 1u << stage;
-                        last_kind &= ~(1u << stage);
-                    }
+                    const bool last = kb == nk - 1;  // rows past the expert load as zeros
+                    if (leader) mbar_arrive_expect_tx(own_full, 2 * P_STAGE_BYTES);
+                    tma_load_3d_pair(sa, last ? ga : ma, full, 0, row, mcol / 64);
+                    tma_load_3d_pair(sb, last ? gb : &tm_b0, full, 0, row, ncol / 64);
                     ++issued;
                     if (++stage == WG_STAGES) { stage = 0; phase ^= 1; }
                 }
             }
-            if (!ok) {
-                // let the copies already issued land before the CTA leaves: the
-                // latest use of each stage completes on its own barrier (a last
-                // k-block) or on the leader's full barrier (the leader waits)
-                for (int s = 0; s < WG_STAGES && s < issued; ++s) {
+            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+        }
+        if (lane == 0) {
+            if (!ok && leader) {
+                // the leader's full barriers count both CTAs' copies: let the
+                // ones already issued land before the pair leaves
+                for (int s = 0; s < WG_STAGES; ++s) {
                     volatile int no_abort = 0;
-                    if (last_kind >> s & 1u)
-                        mbar_wait(smem_u32(&bars->lastfull[s]), stage_parity(par_last, s) ^ 1u, status,
-                                  &no_abort);
-                    else if (leader)
-                        mbar_wait(smem_u32(&bars->full[s]), stage_parity(par_full, s) ^ 1u, status,
-                                  &no_abort);
+                    mbar_wait(smem_u32(&bars->full[s]), phase ^ (s >= stage ? 1 : 0), status,
+                              &no_abort);
                 }
             }
             // the leader's MMAs read this CTA's stages: wait until every use
@@ -643,7 +663,7 @@ grouped_wgrad_pair(const __grid_constant__ CUtensorMap tm_a0, const __grid_const
         if (leader && lane == 0) {
             constexpr uint32_t idesc = idesc_bf16_f32_major(PM, MMA_N, 1, 1);
             int stage = 0;
-            uint32_t par_full = 0, par_ready = 0;
+            uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
@@ -655,21 +675,9 @@ grouped_wgrad_pair(const __grid_constant__ CUtensorMap tm_a0, const __grid_const
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * ACC_COLS);
                 for (int kb = 0; kb < nk; ++kb) {
-                    int steps = BK / 16;
-                    bool got;
-                    if (kb == nk - 1) {
-                        steps = (cnt - kb * BK + 15) / 16;
-                        // both fixers zeroed rows with ordinary stores and
-                        // arrived with release at cluster scope: acquire there
-                        got = mbar_wait<true>(smem_u32(&bars->ready[stage]),
-                                              stage_parity(par_ready, stage), status, abort);
-                        par_ready ^= 1u << stage;
-                    } else {
-                        got = mbar_wait(smem_u32(&bars->full[stage]), stage_parity(par_full, stage),
-                                        status, abort);
-                        par_full ^= 1u << stage;
-                    }
-                    if (!got) {
+                    // the last block's steps cover its valid rows (the rest are zeros)
+                    const int steps = kb == nk - 1 ? (cnt - kb * BK + 15) / 16 : BK / 16;
+                    if (!mbar_wait(smem_u32(&bars->full[stage]), phase, status, abort)) {
                         ok = false;
                         break;
                     }
@@ -681,44 +689,12 @@ grouped_wgrad_pair(const __grid_constant__ CUtensorMap tm_a0, const __grid_const
                                          sw128_mnmajor_desc(sb + kk * 2048), idesc,
                                          (kb | kk) != 0 ? 1u : 0u);
                     tc_commit_pair(smem_u32(&bars->empty[stage]));
-                    if (++stage == WG_STAGES) stage = 0;
+                    if (++stage == WG_STAGES) { stage = 0; phase ^= 1; }
                 }
                 if (!ok) break;
                 tc_commit_pair(smem_u32(&bars->tfull[acc]));
                 if (++acc == 2) { acc = 0; acc_phase ^= 1; }
             }
-        }
-    } else if (warp == WG_FIXER) {
-        // ------------------------------------- last k-block repair (both CTAs)
-        int kc = 0;  // k-blocks of the tiles before this one
-        uint32_t par_last = 0;
-        for (int g = unit0; g < total; g += units) {
-            const Tile t = map_wgrad_tile(g, p);
-            const int cnt = p.count[t.e];
-            const int nk = k_blocks<MODE>(p, cnt);
-            if (nk == 0) continue;
-            const int s = (kc + nk - 1) % WG_STAGES;
-            kc += nk;
-            if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bars->lastfull[s]),
-                                                   stage_parity(par_last, s), status, abort)))
-                break;
-            par_last ^= 1u << s;
-            const int rv = cnt - (nk - 1) * BK;  // valid rows, 1..64
-            const int r16 = (rv + 15) / 16 * 16;
-            if (rv < r16) {
-                // zero rows rv..r16-1 of this CTA's 4 MN-major blocks (2 of A, 2 of B)
-                uint8_t *base = smem + (size_t)s * P_STAGE_BYTES;
-                const int nrow = r16 - rv;
-                for (int i = lane; i < 4 * nrow * 8; i += 32) {
-                    const int blk = i / (nrow * 8), rr = i % (nrow * 8);
-                    const int row = rv + rr / 8, chunk = rr % 8;
-                    *reinterpret_cast<uint4 *>(base + blk * BLK + row * 128 + chunk * 16) =
-                        make_uint4(0, 0, 0, 0);
-                }
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(cluster_map(smem_u32(&bars->ready[s]), 0));
         }
     } else {
         // --------------------------------------------------------- epilogue
@@ -796,7 +772,8 @@ moe_status launch_wgrad_pair(const CUtensorMap &a0, const CUtensorMap &a1, const
     static PerDeviceOnce smem_attr;
     if (!device_once(smem_attr, [smem] { return set_smem_limit(grouped_wgrad_pair<MODE>, smem); }))
         return MOE_ERR_CUDA;
-    const int pairs = std::min(num_sms() / 2, std::max(max_units, 1));
+    // at most kMaxWgradCtas CTAs: the workspace holds that many map rings
+    const int pairs = std::min(std::min(num_sms(), kMaxWgradCtas) / 2, std::max(max_units, 1));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(2 * pairs));
     cfg.blockDim = dim3(WG_THREADS);
@@ -825,7 +802,7 @@ using namespace moe;
 MOE_API size_t moe_expert_ffn_backward_workspace_bytes(const moe_shape *s) {
     if (check_shape(s) != MOE_OK) return 0;
     const size_t R = (size_t)buffer_rows(s);
-    return 256 + 2 * align256(R * s->h * 2);
+    return 256 + 2 * align256(R * s->h * 2) + kMapSlotBytes;
 }
 
 MOE_API moe_status moe_expert_ffn_backward(
@@ -858,9 +835,12 @@ MOE_API moe_status moe_expert_ffn_backward(
     p.count = expert_count;
     p.offset = expert_offset;
     p.status = static_cast<int *>(ws);
+    p.rows = (int)buffer_rows(s);
     uint16_t *dG = reinterpret_cast<uint16_t *>(static_cast<char *>(ws) + 256);
     uint16_t *dU = reinterpret_cast<uint16_t *>(static_cast<char *>(ws) + 256 +
                                                 align256((size_t)R * s->h * 2));
+    p.map_slots = reinterpret_cast<CUtensorMap *>(static_cast<char *>(ws) + 256 +
+                                                  2 * align256((size_t)R * s->h * 2));
     const int64_t rows = std::min<int64_t>(R, (int64_t)s->T * s->K);
     const int row_tiles = (int)((rows + BM - 1) / BM + s->N);
     const int wg_mt = 2 * ((s->h + 2 * BM - 1) / (2 * BM));

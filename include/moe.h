@@ -229,8 +229,10 @@ moe_status moe_expert_ffn_gather(const moe_shape *s, const moe_bf16 *x, const in
                                  moe_bf16 *u_save, moe_bf16 *y_disp, void *ws, size_t ws_bytes,
                                  cudaStream_t stream);
 
-/* Bytes of workspace moe_expert_ffn_backward needs: the device status word
- * and the two [R, h] bf16 intermediates dG and dU. */
+/* Bytes of workspace moe_expert_ffn_backward needs: the device status word,
+ * the two [R, h] bf16 intermediates dG and dU, and 1 MiB of tensor-map copies
+ * (the weight-gradient kernels bound each tile's last k-block to its expert's
+ * rows through per-CTA copies of their maps). */
 size_t moe_expert_ffn_backward_workspace_bytes(const moe_shape *s);
 
 /*
