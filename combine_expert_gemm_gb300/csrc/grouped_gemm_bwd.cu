@@ -23,14 +23,14 @@
 // activations in wgrad) are read MN-major: a TMA box of 64 M/N elements x 64 K
 // rows lands as 64 swizzled 128-byte rows and the MMA descriptor walks it with
 // K rows 128 B apart, 8-row groups 1 KB apart and 64-element M/N blocks 8 KB
-// apart.  No transposed copy of anything is made.
+// apart; each CTA's two blocks of a k-block arrive by one 3-D box.  No
+// transposed copy of anything is made.
 //
 // In wgrad the reduction runs over an expert's rows, so the last k-block of a
 // tile can reach into the next expert's rows or the tail (which may hold NaN).
-// The leader issues only the 16-row MMA steps that hold valid rows; inside the
-// last of those steps each CTA's fixer warp first writes zeros over the
-// invalid rows of its own operand blocks, fencing them to the tensor core's
-// async proxy.
+// That block loads through copies of its maps whose row extent ends at the
+// expert's last row, so the copy engine fills the rows past it with zeros; the
+// leader issues only the 16-row MMA steps that hold valid rows.
 #include <algorithm>
 
 #include "moe_common.cuh"
