@@ -280,3 +280,20 @@ def test_binding_refuses_tensors_of_another_device(moe, monkeypatch):
         moe._ptr(t, torch.int32, "route_row")
     with pytest.raises(ValueError, match="must be a CUDA tensor"):
         moe._ptr(torch.zeros(4), None, "x")
+
+
+def test_expert_backward_workspace_holds_map_slots(moe):
+    """moe_expert_ffn_backward's workspace is the status word, dG and dU
+    ([R, h] bf16 each, 256-byte aligned) and 1 MiB of tensor-map copies for
+    the weight-gradient kernels; one byte short is refused before anything is
+    enqueued (every call here fails validation, so nothing reaches a GPU)."""
+    s = _shape(moe)
+    lib = moe.lib()
+    align = lambda n: (n + 255) // 256 * 256
+    ws = lib.moe_expert_ffn_backward_workspace_bytes(ctypes.byref(s))
+    assert ws == 256 + 2 * align(s.R * s.h * 2) + (1 << 20)
+    A = ctypes.c_void_p(4096)
+    args = [A] * 14                                     # x_disp .. dw_down
+    assert lib.moe_expert_ffn_backward(ctypes.byref(s), *args, A, ws - 1, None) == 3
+    assert lib.moe_expert_ffn_backward(ctypes.byref(s), *args, ctypes.c_void_p(4096 + 128), ws,
+                                       None) == 3
