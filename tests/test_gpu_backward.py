@@ -133,6 +133,31 @@ def test_expert_backward_full_size(moe):
     assert_close_f32(dwd[e], rdwd, "dw_down[e]")
     assert_close_bf16(dx[sl], oracle.bf16_from_f64(rdx), "dx_disp rows of e")
 
+    # the same call six more times on device-resident inputs: every output bit
+    # for bit the first run's (the weight gradients bound each tile's last
+    # k-block through map copies rewritten on the device, tile after tile)
+    s = moe.Shape(cfg.T, cfg.d, cfg.N, cfg.K, cfg.h, cfg.cap)
+    ins = [bf(a) for a in (xd, wg, wu, wd, gs, us, ha, dyd)]
+    cnt_d, off_d = i32(cnt), i32(off)
+    ws = torch.zeros(moe.expert_ffn_backward_workspace_bytes(s), dtype=torch.uint8, device=DEV)
+    first = None
+    for _ in range(6):
+        dxr = torch.full((cfg.R, cfg.d), NAN, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+        outs = [torch.full((cfg.N, cfg.h, cfg.d), float("nan"), dtype=torch.float32, device=DEV)
+                for _ in range(2)]
+        outs.append(torch.full((cfg.N, cfg.d, cfg.h), float("nan"), dtype=torch.float32,
+                               device=DEV))
+        moe.expert_ffn_backward(s, ins[0], cnt_d, off_d, ins[1], ins[2], ins[3], ins[4], ins[5],
+                                ins[6], ins[7], dxr, outs[0], outs[1], outs[2], ws)
+        got = [dxr.view(torch.int16)[:A]] + outs
+        if first is None:
+            first = got
+            assert np.array_equal(got[0].cpu().numpy().view(np.uint16), dx[:A])
+        else:
+            assert all(torch.equal(a, b) for a, b in zip(got, first))
+    torch.cuda.synchronize()
+    assert moe.read_device_error(ws) == 0
+
 
 def test_training_step_chain_full_size(moe):
     """Forward with saving, then combine backward, expert backward and dispatch
